@@ -1,0 +1,174 @@
+/*
+ * moe_warp.h — C ABI of libmoewarp.so: one mixture-of-experts layer evaluated
+ * over one speculative-decoding verification pass of n tokens, on one GB300
+ * (sm_103a).
+ *
+ * The operation, as the sources state it:
+ *   - "Deep Dive into Mixture of Experts: From 1991 to DeepSeek-V3", §2 "The
+ *     Sparse-Gating Leap" (the top-k gating sketch): logits = x·W_g, keep the
+ *     k largest, softmax over those k logits only, output = Σ weight·expert(x).
+ *   - same post, §5 "DeepSeek-V3 and the Current State of the Art" (the routing
+ *     sketch): always-on shared experts are added unweighted.
+ *   - "Building a Terminal Based LLM Inference Internals Explorer - Part 3:
+ *     Speculative Decoding", section "The Flow": the verifier scores the
+ *     γ drafted tokens plus the bonus position in one batched call, so a
+ *     verification pass holds n = γ+1 tokens.
+ *   - "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes, Kernel
+ *     Bandwidth and the Best Draft Length", abstract: a per-slot engine reads a
+ *     selected expert once per token; a deduplicating engine reads each
+ *     selected expert once per pass.
+ * Each expert is a SwiGLU FFN without biases:
+ *   FFN_e(x) = W_down,e · ( silu(W_gate,e · x) ⊙ (W_up,e · x) ),  silu(z) = z/(1+e^−z).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument except `desc`, `weights`, `u` (host structs, read
+ *     during the call only) is a DEVICE pointer. The caller owns all memory;
+ *     the library never allocates device memory on these paths.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream). No call synchronises the host with the device
+ *     except moe_last_device_error.
+ *   - Arguments are checked on the host before any launch: a bad argument
+ *     returns MOE_EINVAL (nothing is launched); a shape the kernels do not
+ *     cover returns MOE_EUNSUPPORTED; a launch failure returns MOE_ECUDA.
+ *   - Inputs must be finite. Behaviour on NaN/Inf inputs is unspecified.
+ *   - Limits: 1 ≤ n ≤ MOE_MAX_TOKENS, n·k ≤ MOE_MAX_PAIRS, 1 ≤ k ≤ E ≤
+ *     MOE_MAX_EXPERTS, k ≤ MOE_MAX_TOPK, 0 ≤ s ≤ MOE_MAX_SHARED, d and I
+ *     multiples of 64, every device pointer 16-byte aligned.
+ */
+#ifndef MOE_WARP_H
+#define MOE_WARP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_MAX_TOKENS 128
+#define MOE_MAX_PAIRS 512
+#define MOE_MAX_EXPERTS 256
+#define MOE_MAX_TOPK 16
+#define MOE_MAX_SHARED 4
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_EINVAL = 1,       /* bad argument: null pointer, misalignment, out-of-range size */
+  MOE_ECUDA = 2,        /* a CUDA runtime call failed; moe_last_cuda_error_string() says which */
+  MOE_ETIMEOUT = 3,     /* a bounded device-side wait expired (reported by moe_last_device_error) */
+  MOE_EUNSUPPORTED = 4, /* valid arguments that no kernel here covers */
+  MOE_EDEVICE = 5       /* a kernel recorded a failed device-side check */
+} moe_status;
+
+typedef enum { MOE_W_F32 = 0, MOE_W_BF16 = 1 } moe_wdtype;
+
+/* Shape of one MoE layer. Plain data, caller-owned. */
+typedef struct {
+  int32_t d;         /* model dimension (length of a hidden state x_t) */
+  int32_t n_experts; /* E, routed experts */
+  int32_t top_k;     /* k, experts selected per token */
+  int32_t inter;     /* I, SwiGLU intermediate size of every expert (routed and shared) */
+  int32_t n_shared;  /* s, always-on shared experts (0 if none) */
+  int32_t wdtype;    /* moe_wdtype of the expert weights; the router W_g is always fp32 */
+} moe_layer_desc;
+
+/* Device pointers to one layer's weights, row-major, caller-owned.
+ * Element type of the expert matrices is desc->wdtype (bf16 = raw 16-bit
+ * bfloat16 bit patterns).                                                    */
+typedef struct {
+  const float* w_router; /* W_g  [E][d]     fp32: logit of expert e is Σ_i x_i·W_g[e][i] */
+  const void* w_gate;    /* [E][I][d]  W_gate,e rows (output i, input d contiguous) */
+  const void* w_up;      /* [E][I][d]  W_up,e */
+  const void* w_down;    /* [E][d][I]  W_down,e rows (output j, input I contiguous) */
+  const void* ws_gate;   /* [s][I][d]  shared experts; NULL iff s == 0 */
+  const void* ws_up;     /* [s][I][d] */
+  const void* ws_down;   /* [s][d][I] */
+} moe_layer_weights;
+
+/* Device outputs of moe_build_union: the union U of the experts selected in
+ * one pass, and the (token, slot) pairs grouped by expert.                  */
+typedef struct {
+  int32_t* union_ids;   /* [E]    distinct selected experts, ascending; first *union_count valid */
+  int32_t* union_count; /* [1]    |U| */
+  int32_t* offsets;     /* [E+1]  pairs of union_ids[u] are rows offsets[u] .. offsets[u+1]-1 */
+  int32_t* pair_tok;    /* [n*k]  token t of each pair, grouped by expert, tokens ascending */
+  int32_t* pair_slot;   /* [n*k]  slot j of each pair (topk_idx[t][j] == its expert) */
+  uint64_t* bytes;      /* [3]    requested expert-weight bytes of this pass:
+                                  {per-slot = n·k·E_b, dedup = |U|·E_b, shared = s·E_b},
+                                  E_b = 3·d·I·sizeof(weight) bytes per expert */
+} moe_union;
+
+/* Bytes of device scratch ("workspace") the engine and routing calls need
+ * for passes of up to n_max tokens. 0 on invalid arguments. The workspace is
+ * caller-owned, 256-byte aligned, needs no initialisation, and may be reused
+ * by consecutive calls on one stream; two calls that overlap on the device
+ * must not share one.                                                       */
+size_t moe_workspace_bytes(const moe_layer_desc* desc, int32_t n_max);
+
+/* Gate GEMV, top-k and renormalised softmax
+ * ("Deep Dive into Mixture of Experts", §2, top-k gating sketch).
+ *   x        [n][d] fp32 hidden states of the pass
+ *   w_router [E][d] fp32 W_g
+ *   topk_idx [n][k] int32 out: the k experts with the largest logits, in
+ *            descending logit order; equal logits are ordered by ascending
+ *            expert index (so ties select the lower index).
+ *   topk_w   [n][k] fp32 out: softmax of the k selected logits (sums to 1).
+ * Logits are accumulated with a compensated (error-free-transformation) dot
+ * product, so the selection agrees with an exact computation except where
+ * two logits lie within ~1e-12 relative of each other.                      */
+moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const float* x, int32_t n,
+                     int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* Union of the selected experts and the pairs grouped by expert
+ * ("Speculative Decoding for Mixture-of-Experts Models", abstract: the
+ * deduplicating engine reads each selected expert once per pass).
+ *   topk_idx [n][k] as written by moe_route (values must be in [0, E)).
+ *   u        device arrays sized as documented in moe_union.
+ * Integer-exact; the result does not depend on thread scheduling.          */
+moe_status moe_build_union(const moe_layer_desc* desc, const int32_t* topk_idx, int32_t n,
+                           const moe_union* u, void* stream);
+
+/* Per-slot engine: every (token t, slot j) runs its own expert FFN, reading
+ * that expert's weights for that slot alone (requested bytes n·k·E_b), and
+ * every shared expert runs once over all n tokens.
+ *   x        [n][d] fp32;  topk_idx/topk_w as written by moe_route.
+ *   y_slot   [n][k+s][d] fp32 out: slot j < k holds topk_w[t][j]·FFN_e(x_t)
+ *            with e = topk_idx[t][j]; slot k+i holds FFN_shared_i(x_t).     */
+moe_status moe_verify_perslot(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                              const float* x, int32_t n, const int32_t* topk_idx,
+                              const float* topk_w, void* workspace, size_t workspace_bytes,
+                              float* y_slot, void* stream);
+
+/* Deduplicating engine: each distinct selected expert's weights are streamed
+ * from HBM once per pass and applied to every token that selected it
+ * (requested bytes |U|·E_b), plus the shared experts as above.
+ *   u        the moe_build_union result for the same topk_idx (read on the
+ *            device only; no host synchronisation).
+ *   y_slot   same layout and meaning as moe_verify_perslot.               */
+moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                            const float* x, int32_t n, const moe_union* u, const float* topk_w,
+                            void* workspace, size_t workspace_bytes, float* y_slot,
+                            void* stream);
+
+/* Weighted combine ("Deep Dive into Mixture of Experts", §2 and §5 sketches:
+ * output = shared experts + Σ weight·expert):
+ *   y[t] = Σ_{j=0}^{k+s-1} y_slot[t][j]   (fixed order j = 0, 1, …; deterministic)
+ *   y_slot [n][k+s][d] fp32 in;  y [n][d] fp32 out.                         */
+moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t n, float* y,
+                       void* stream);
+
+/* Synchronises `stream`, then reads and clears the library's device error
+ * word: MOE_ETIMEOUT if a bounded device-side wait expired, MOE_EDEVICE if a
+ * kernel recorded a failed check, MOE_ECUDA if the stream reports an error,
+ * else MOE_OK.                                                             */
+moe_status moe_last_device_error(void* stream);
+
+const char* moe_status_str(moe_status s);
+const char* moe_last_cuda_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_WARP_H */

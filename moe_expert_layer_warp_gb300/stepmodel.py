@@ -1,0 +1,234 @@
+"""Host step-time model of a speculative-decoding step on an MoE model.
+
+Host analytics only: it consumes measured kernel times and byte counts and
+runs no part of the layer itself.
+
+Sources:
+  [A] "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
+      Kernel Bandwidth and the Best Draft Length", abstract: a step's time is
+      the bytes each kernel requests over its effective bandwidth, plus fixed
+      time; dedup is faster exactly where its byte share ū(n) of the per-slot
+      bytes is below its bandwidth ratio r(n); the crossover is the first pass
+      size at which dedup is faster; the best draft length is a monotone
+      staircase in the acceptance rate under geometric acceptance.
+  [O] overdisp README (over-dispersed acceptance in greedy speculative
+      decoding), opening paragraph: under i.i.d. acceptance with rate α a
+      block of draft length γ yields E[k] = (1 − α^(γ+1))/(1 − α) tokens.
+  [L] "Is Speculative Decoding's Speedup a Hardware Problem or a Model
+      Problem?", Hypothesis 1: Leviathan et al.'s expected speedup
+      (1 − α^(γ+1)) / ((1 − α)(γ·c + 1)) for a draft/verify cost ratio c.
+  [F] "Building a Terminal Based LLM Inference Internals Explorer - Part 3:
+      Speculative Decoding", section "The Flow": one verification pass scores
+      the γ drafts and the bonus position, n = γ + 1 tokens.
+
+Readings (the abstract gives no formulas):
+  - per engine e, the expert kernels' effective bandwidth at pass size n is
+    BW_e(n) = Σ requested expert-weight bytes / Σ expert-kernel time over the
+    measured passes; the step's time for one layer is
+    T_e(n) = B_e(n)/BW_e(n) + t_fix(n), with t_fix (routing, union, combine)
+    the same for both engines. B_e counts the bytes the engine's kernels
+    request, shared experts included for both engines, so that
+    ū(n) = mean B_dd / mean B_ps and dedup is faster ⇔ ū(n) < r(n) exactly.
+  - a drafted token costs t_draft; a speculative step with draft length γ
+    takes γ·t_draft + T(γ+1) and advances E[k](α, γ) tokens; plain decoding
+    (γ = 0) advances 1 token in T(1). γ* maximises tokens per second, ties
+    going to the smaller γ.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Callable, Dict, Iterable, List, Optional, Sequence
+
+
+def expected_tokens(alpha: float, gamma: int) -> float:
+    """[O] E[k] = (1 − α^(γ+1))/(1 − α), tokens a verification step yields
+    (the accepted run plus the verifier's own token); γ+1 at α = 1."""
+    if not 0.0 <= alpha <= 1.0 or gamma < 0:
+        raise ValueError("need 0 <= alpha <= 1 and gamma >= 0")
+    if alpha == 1.0:
+        return float(gamma + 1)
+    return (1.0 - alpha ** (gamma + 1)) / (1.0 - alpha)
+
+
+def leviathan_speedup(alpha: float, gamma: int, c: float) -> float:
+    """[L] expected speedup with a flat verify cost and draft cost ratio c."""
+    return expected_tokens(alpha, gamma) / (gamma * c + 1.0)
+
+
+def breakeven_alpha(gamma: int, c: float, tol: float = 1e-12) -> float:
+    """Smallest α at which leviathan_speedup reaches 1 (bisection; the speedup
+    is increasing in α)."""
+    lo, hi = 0.0, 1.0
+    if leviathan_speedup(hi, gamma, c) < 1.0:
+        return float("nan")
+    while hi - lo > tol:
+        mid = 0.5 * (lo + hi)
+        if leviathan_speedup(mid, gamma, c) >= 1.0:
+            hi = mid
+        else:
+            lo = mid
+    return hi
+
+
+def effective_bandwidth(bytes_: Iterable[float], seconds: Iterable[float]) -> float:
+    """[A] Σ requested bytes / Σ kernel time (bytes/s)."""
+    b = float(sum(bytes_))
+    s = float(sum(seconds))
+    if s <= 0.0:
+        raise ValueError("non-positive total time")
+    return b / s
+
+
+def byte_share(dedup_bytes: Iterable[float], perslot_bytes: Iterable[float]) -> float:
+    """[A] ū(n): dedup bytes as a share of per-slot bytes (ratio of sums)."""
+    ps = float(sum(perslot_bytes))
+    if ps <= 0.0:
+        raise ValueError("no per-slot bytes")
+    return float(sum(dedup_bytes)) / ps
+
+
+def dedup_faster(u_bar: float, r: float) -> bool:
+    """[A] dedup is faster exactly where ū(n) < r(n)."""
+    return u_bar < r
+
+
+def crossover(ns: Sequence[int], u_bar: Dict[int, float], r: Dict[int, float]) -> Optional[int]:
+    """[A] the first pass size n ≥ 2 at which dedup is faster, or None."""
+    for n in sorted(ns):
+        if n >= 2 and dedup_faster(u_bar[n], r[n]):
+            return n
+    return None
+
+
+@dataclass
+class EngineFit:
+    """Per-engine fit: effective bandwidth per pass size and fixed time."""
+    bw: Dict[int, float]                    # n -> bytes/s of the expert kernels
+    t_fix: Dict[int, float]                 # n -> seconds (route + union + combine)
+    bytes_per_layer: Dict[int, float] = field(default_factory=dict)  # n -> mean B_e(n)
+
+    def layer_time(self, n: int, bytes_: Optional[float] = None) -> float:
+        """[A] T_e(n) = B_e(n)/BW_e(n) + t_fix(n) for one layer."""
+        b = self.bytes_per_layer[n] if bytes_ is None else bytes_
+        return b / self.bw[n] + self.t_fix[n]
+
+
+def step_time(fit: EngineFit, n: int, bytes_per_layer: Sequence[float]) -> float:
+    """[A] a pass of n tokens through a stack: Σ_layers B_ℓ(n)/BW(n) + L·t_fix(n)."""
+    return sum(b / fit.bw[n] for b in bytes_per_layer) + len(bytes_per_layer) * fit.t_fix[n]
+
+
+def tokens_per_second(alpha: float, gamma: int, verify_time: Callable[[int], float],
+                      t_draft: float) -> float:
+    """Tokens advanced per second with draft length γ ([F]: n = γ+1)."""
+    return expected_tokens(alpha, gamma) / (gamma * t_draft + verify_time(gamma + 1))
+
+
+def speculation_faster(alpha: float, gamma: int, verify_time: Callable[[int], float],
+                       t_draft: float) -> bool:
+    """[A] speculation with draft length γ beats plain decoding:
+    E[k](α,γ)/(γ·t_draft + T(γ+1)) > 1/T(1)."""
+    return (tokens_per_second(alpha, gamma, verify_time, t_draft)
+            > 1.0 / verify_time(1))
+
+
+def best_draft_length(alpha: float, verify_time: Callable[[int], float], t_draft: float,
+                      gamma_max: int) -> int:
+    """[A] γ*(α) = argmax over γ ∈ {0..gamma_max} of tokens per second
+    (γ = 0 is plain decoding); ties go to the smaller γ."""
+    best_g, best_v = 0, tokens_per_second(alpha, 0, verify_time, t_draft)
+    for g in range(1, gamma_max + 1):
+        v = tokens_per_second(alpha, g, verify_time, t_draft)
+        if v > best_v:
+            best_g, best_v = g, v
+    return best_g
+
+
+def staircase(alphas: Sequence[float], verify_time: Callable[[int], float], t_draft: float,
+              gamma_max: int) -> List[int]:
+    """[A] γ*(α) over a grid of acceptance rates."""
+    return [best_draft_length(a, verify_time, t_draft, gamma_max) for a in alphas]
+
+
+def acceptance_grid(lo: float = 0.50, hi: float = 0.95, steps: int = 22) -> List[float]:
+    """The 22 evenly spaced acceptance rates from 0.50 to 0.95."""
+    return [lo + (hi - lo) * i / (steps - 1) for i in range(steps)]
+
+
+def interpolated(times: Dict[int, float]) -> Callable[[int], float]:
+    """A verify-time function over the measured pass sizes (n outside the
+    measured range is rejected)."""
+    def T(n: int) -> float:
+        if n not in times:
+            raise KeyError("pass size %d not measured" % n)
+        return times[n]
+    return T
+
+
+@dataclass
+class StepModelReport:
+    ns: List[int]
+    u_bar: Dict[int, float]
+    r: Dict[int, float]
+    bw_ps: Dict[int, float]
+    bw_dd: Dict[int, float]
+    t_fix: Dict[int, float]
+    crossover: Optional[int]
+    alphas: List[float]
+    gamma_star_ps: List[int]
+    gamma_star_dd: List[int]
+    gamma_star_best: List[int]
+    t_draft: float
+
+    def as_dict(self) -> dict:
+        return {
+            "n": self.ns,
+            "u_bar": [round(self.u_bar[n], 6) for n in self.ns],
+            "r": [round(self.r[n], 6) for n in self.ns],
+            "bw_perslot_GBs": [round(self.bw_ps[n] / 1e9, 2) for n in self.ns],
+            "bw_dedup_GBs": [round(self.bw_dd[n] / 1e9, 2) for n in self.ns],
+            "t_fix_us": [round(self.t_fix[n] * 1e6, 3) for n in self.ns],
+            "crossover_n": self.crossover,
+            "t_draft_us": round(self.t_draft * 1e6, 3),
+            "alphas": [round(a, 5) for a in self.alphas],
+            "gamma_star_perslot": self.gamma_star_ps,
+            "gamma_star_dedup": self.gamma_star_dd,
+            "gamma_star_best_engine": self.gamma_star_best,
+        }
+
+
+def build_report(samples: Dict[str, Dict[int, List[tuple]]], t_fix: Dict[int, float],
+                 layers: int = 1, draft_cost_ratio: float = 0.0,
+                 alphas: Optional[Sequence[float]] = None) -> StepModelReport:
+    """Fit and evaluate the model from measured passes.
+
+    samples[engine][n] = list of (requested_bytes, expert_kernel_seconds) per
+    pass, engine in {"perslot", "dedup"}; t_fix[n] in seconds per layer.
+    The draft cost per drafted token is draft_cost_ratio × T_best(1)."""
+    ns = sorted(set(samples["perslot"]) & set(samples["dedup"]))
+    bw_ps = {n: effective_bandwidth([b for b, _ in samples["perslot"][n]],
+                                    [s for _, s in samples["perslot"][n]]) for n in ns}
+    bw_dd = {n: effective_bandwidth([b for b, _ in samples["dedup"][n]],
+                                    [s for _, s in samples["dedup"][n]]) for n in ns}
+    u = {n: byte_share([b for b, _ in samples["dedup"][n]],
+                       [b for b, _ in samples["perslot"][n]]) for n in ns}
+    r = {n: bw_dd[n] / bw_ps[n] for n in ns}
+    mean_b = {e: {n: sum(b for b, _ in samples[e][n]) / len(samples[e][n]) for n in ns}
+              for e in ("perslot", "dedup")}
+    fit_ps = EngineFit(bw_ps, t_fix, mean_b["perslot"])
+    fit_dd = EngineFit(bw_dd, t_fix, mean_b["dedup"])
+    T_ps = {n: layers * fit_ps.layer_time(n) for n in ns}
+    T_dd = {n: layers * fit_dd.layer_time(n) for n in ns}
+    T_best = {n: min(T_ps[n], T_dd[n]) for n in ns}
+    if 1 not in T_best:
+        raise ValueError("pass size 1 (plain decoding) must be measured")
+    t_draft = draft_cost_ratio * T_best[1]
+    gmax = max(ns) - 1
+    al = list(alphas) if alphas is not None else acceptance_grid()
+    return StepModelReport(
+        ns=ns, u_bar=u, r=r, bw_ps=bw_ps, bw_dd=bw_dd, t_fix=dict(t_fix),
+        crossover=crossover(ns, u, r), alphas=al,
+        gamma_star_ps=staircase(al, interpolated(T_ps), t_draft, gmax),
+        gamma_star_dd=staircase(al, interpolated(T_dd), t_draft, gmax),
+        gamma_star_best=staircase(al, interpolated(T_best), t_draft, gmax),
+        t_draft=t_draft)

@@ -1,0 +1,125 @@
+"""Pins of the host step-time model against the pages' worked numbers and
+closed forms, plus properties the method states.
+
+Sources: "Is Speculative Decoding's Speedup a Hardware Problem or a Model
+Problem?" (Hypothesis 1 and 2 tables); overdisp README, opening paragraph
+(E[k]); "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
+Kernel Bandwidth and the Best Draft Length", abstract (ū < r criterion,
+crossover, monotone staircase).
+"""
+import json
+import os
+import random
+
+import pytest
+
+from moe_expert_layer_warp_gb300 import stepmodel as sm
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                   "speculative_worked_examples.json")))
+
+
+def test_cost_ratio_from_flops():
+    c = GOLD["cost_ratio_flops"]
+    assert round(c["draft_flops_per_token"] / c["verifier_flops_per_token"], 4) == c["c_printed"]
+
+
+@pytest.mark.parametrize("table", ["hypothesis1_theoretical", "hypothesis2_theoretical"])
+def test_leviathan_table_values(table):
+    tab = GOLD[table]
+    for row in tab["rows"]:
+        v = sm.leviathan_speedup(row["alpha"], row["gamma"], tab["c"])
+        assert round(v, 2) == row["speedup"], (row, v)
+
+
+def test_breakeven_span():
+    b = GOLD["hypothesis2_breakeven"]
+    lo = sm.breakeven_alpha(b["gamma_lo"], b["c"])
+    hi = sm.breakeven_alpha(b["gamma_hi"], b["c"])
+    assert round(100 * lo) == b["alpha_lo_percent"]
+    assert round(100 * hi) == b["alpha_hi_percent"]
+    seq = [sm.breakeven_alpha(g, b["c"]) for g in range(b["gamma_lo"], b["gamma_hi"] + 1)]
+    assert all(a < b_ for a, b_ in zip(seq, seq[1:]))
+
+
+def test_expected_tokens_limits_and_series():
+    for g in range(0, 12):
+        assert sm.expected_tokens(0.0, g) == 1.0
+        assert sm.expected_tokens(1.0, g) == g + 1
+        assert abs(sm.expected_tokens(1.0 - 1e-9, g) - (g + 1)) < 1e-6
+        for a in (0.1, 0.5, 0.93):
+            # capped geometric run: E[k] = Σ_{i=0}^{γ} α^i
+            assert abs(sm.expected_tokens(a, g) - sum(a ** i for i in range(g + 1))) < 1e-12
+
+
+def test_flat_verify_cost_reduces_to_leviathan():
+    """With T(n) ≡ T(1) and t_draft = c·T(1), tokens/s relative to plain
+    decoding is Leviathan's speedup."""
+    T1 = 3.7e-3
+    for a in (0.3, 0.6, 0.9):
+        for g in (1, 4, 8):
+            for c in (0.0, 0.1601, 0.5002):
+                v = sm.tokens_per_second(a, g, lambda n: T1, c * T1) * T1
+                assert abs(v - sm.leviathan_speedup(a, g, c)) < 1e-12
+
+
+def test_dedup_faster_iff_u_below_r():
+    """Step time per engine is B/BW + t_fix with the same t_fix: dedup has the
+    smaller time exactly when ū < r."""
+    rnd = random.Random(1)
+    for _ in range(2000):
+        ps = rnd.uniform(1e8, 1e10)
+        dd = ps * rnd.uniform(0.05, 1.0)
+        bw_ps = rnd.uniform(1e12, 8e12)
+        bw_dd = bw_ps * rnd.uniform(0.2, 1.5)
+        tf = rnd.uniform(0, 1e-5)
+        t_ps = sm.EngineFit({1: bw_ps}, {1: tf}).layer_time(1, ps)
+        t_dd = sm.EngineFit({1: bw_dd}, {1: tf}).layer_time(1, dd)
+        u, r = dd / ps, bw_dd / bw_ps
+        if abs(u - r) > 1e-9:
+            assert (t_dd < t_ps) == sm.dedup_faster(u, r)
+
+
+def test_crossover_is_first_n_where_u_below_r():
+    ns = list(range(1, 10))
+    u = {n: 1.0 / n ** 0.5 for n in ns}
+    r = {n: 0.5 for n in ns}
+    assert sm.crossover(ns, u, r) == 5          # 1/sqrt(5) = 0.447 < 0.5
+    assert sm.crossover(ns, u, {n: 0.2 for n in ns}) is None
+
+
+def test_staircase_is_monotone_in_alpha():
+    rnd = random.Random(7)
+    alphas = sm.acceptance_grid()
+    assert len(alphas) == 22 and alphas[0] == 0.5 and abs(alphas[-1] - 0.95) < 1e-12
+    for _ in range(200):
+        # verify time increasing and concave-ish in n, as for byte-bound passes
+        base = rnd.uniform(1e-4, 1e-2)
+        slope = rnd.uniform(0.0, 0.3)
+        T = {n: base * (1.0 + slope * (n - 1) ** rnd.uniform(0.5, 1.0)) for n in range(1, 17)}
+        td = rnd.choice([0.0, 0.05, 0.1, 0.2]) * T[1]
+        st = sm.staircase(alphas, sm.interpolated(T), td, 15)
+        assert all(a <= b for a, b in zip(st, st[1:])), st
+
+
+def test_best_draft_length_ties_go_to_smaller_gamma():
+    # α = 0: every γ yields one token; with free drafting and flat T they tie
+    assert sm.best_draft_length(0.0, lambda n: 1.0, 0.0, 8) == 0
+
+
+def test_build_report_end_to_end():
+    samples = {"perslot": {}, "dedup": {}}
+    for n in range(1, 10):
+        ps = n * 6 * 17_301_504 + 2 * 17_301_504
+        dd = min(64, 6 + 2 * (n - 1)) * 17_301_504 + 2 * 17_301_504
+        samples["perslot"][n] = [(ps, ps / 6.0e12)]
+        samples["dedup"][n] = [(dd, dd / 5.0e12)]
+    rep = sm.build_report(samples, {n: 5e-6 for n in range(1, 10)})
+    d = rep.as_dict()
+    assert d["r"][0] == pytest.approx(5.0 / 6.0)
+    assert d["u_bar"][0] == pytest.approx(1.0)
+    n_star = rep.crossover
+    assert n_star is not None
+    assert rep.u_bar[n_star] < rep.r[n_star]
+    assert all(not (rep.u_bar[n] < rep.r[n]) for n in range(2, n_star))
+    assert len(rep.gamma_star_best) == 22
