@@ -1,0 +1,472 @@
+"""Benchmark: verify-pass tokens/s and expert-weight HBM GB/s, dedup vs
+per-slot, on the DeepSeek-V2-Lite-shaped MoE layer (d=2048, 64 routed experts
+top-6 + 2 shared, SwiGLU I=1408, bf16 weights, fp32 accumulate).
+
+One step = one verification pass at every pass size n = 1..9 (AR(1) hidden
+states, rho = 0.9) through each engine (per-slot and dedup): 18 passes of
+route → union → experts → combine, 90 tokens. The layer's weights exist in
+several independently seeded replicas and consecutive passes use different
+replicas, so every pass reads its expert weights cold from HBM (inputs larger
+than L2). The step is captured once in a CUDA graph and replayed.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the float64 CPU
+oracle on the same workload instead (a bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify-pass tokens/s and expert-weight HBM GB/s vs 8 TB/s, dedup vs per-slot"
+UNIT = "tokens/s"
+WORKLOAD = "deepseek-v2-lite-shaped MoE layer: d=2048, 64 routed experts top-6 + 2 shared, " \
+           "SwiGLU I=1408, bf16 weights / fp32 accumulate; verify passes n=1..9 at rho=0.9 " \
+           "through the per-slot and the dedup engine"
+REPLICAS = 4
+N_PASSES_PER_N = 2        # distinct hidden-state passes per n, alternated across steps
+EXPERT_BYTES = 3 * 2048 * 1408 * 2
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed
+    region (every 200 ms)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our engine --
+def build_workload(dev):
+    import torch
+    from moe_expert_layer_warp_gb300 import configs, synth
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    w = configs.V2_LITE
+    reps = [synth.make_layer(w.shape, w.weight_seed + 7919 * r, dev) for r in range(REPLICAS)]
+    runners = [PassRunner(L, max(w.pass_sizes)) for L in reps]
+    xs = {}
+    for n in w.pass_sizes:
+        xs[n] = [torch.from_numpy(synth.make_pass(w.shape.d, n, w.rhos[0],
+                                                  [w.x_seed_base + 1000 * q + n]))
+                 .to(dev) for q in range(N_PASSES_PER_N)]
+    return w, runners, xs
+
+
+def step_plan(w, step_idx):
+    """(replica, n, engine, x variant) for the 18 passes of a step; consecutive
+    passes always use different replicas."""
+    plan = []
+    i = 0
+    for n in w.pass_sizes:
+        for eng in ("perslot", "dedup"):
+            plan.append(((step_idx + i) % REPLICAS, n, eng, step_idx % N_PASSES_PER_N))
+            i += 1
+    return plan
+
+
+def enqueue_step(w, runners, xs, step_idx, stream):
+    for rep, n, eng, q in step_plan(w, step_idx):
+        runners[rep].forward(xs[n][q], eng, stream)
+
+
+def kernels_per_pass():
+    # moe_route: gate GEMV + top-k; moe_build_union: 1; engine: 2 phases; combine: 1
+    return 2 + 1 + 2 + 1
+
+
+def measure_breakdown(w, runners, xs, reps=3):
+    """Per-pass timing with CUDA events around the engine call and the whole
+    pass, on the launching stream; returns samples for the step-time model and
+    the expert-engine roofline numbers."""
+    import torch
+    stream = torch.cuda.current_stream()
+    samples = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
+    tfix = {n: [] for n in w.pass_sizes}
+    pass_ms = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
+    alg_bytes, eng_ms = 0.0, 0.0
+    launches = 0
+    for r in range(reps):
+        for rep, n, eng, q in step_plan(w, r):
+            R = runners[rep]
+            x = xs[n][q]
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            R.route(x, stream)
+            R.build_union(n, stream)
+            ev[1].record(stream)
+            R.experts(x, eng, stream)
+            ev[2].record(stream)
+            R.combine(n, stream)
+            ev[3].record(stream)
+            torch.cuda.synchronize()
+            t_exp = ev[1].elapsed_time(ev[2]) * 1e-3
+            t_all = ev[0].elapsed_time(ev[3]) * 1e-3
+            b = [int(v) for v in R.bytes.cpu().tolist()]
+            sh = R.shape
+            req = (b[0] if eng == "perslot" else b[1]) + b[2]
+            samples[eng][n].append((req, t_exp))
+            tfix[n].append(t_all - t_exp)
+            pass_ms[eng][n].append(t_all * 1e3)
+            act = n * sh.d * 4 + n * (sh.top_k + sh.n_shared) * sh.d * 4
+            alg_bytes += req + act
+            eng_ms += t_exp * 1e3
+            launches += 1
+    t_fix = {n: statistics.median(v) for n, v in tfix.items()}
+    return samples, t_fix, pass_ms, alg_bytes / launches, eng_ms / launches
+
+
+def e2e_measure(w, runners, xs, steps, warmup):
+    """End to end through the public API with host buffers: every pass copies
+    its hidden states from pinned host memory and reads y back to pinned host
+    memory, inside the timed region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    hx = {n: [x.cpu().pin_memory() for x in xs[n]] for n in xs}
+    hy = {n: torch.empty((n, w.shape.d), dtype=torch.float32).pin_memory() for n in xs}
+    dx = {n: torch.empty((n, w.shape.d), dtype=torch.float32, device=xs[n][0].device)
+          for n in xs}
+    h2d = d2h = 0
+    for n in w.pass_sizes:
+        h2d += 2 * n * w.shape.d * 4
+        d2h += 2 * n * w.shape.d * 4
+
+    def one(step_idx):
+        for rep, n, eng, q in step_plan(w, step_idx):
+            dx[n].copy_(hx[n][q], non_blocking=True)
+            y = runners[rep].forward(dx[n], eng, stream)
+            hy[n].copy_(y, non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        one(i)
+    t1.record(stream)
+    t1.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    return ms, h2d, d2h
+
+
+def load_traffic(kernel_key: str):
+    """DRAM traffic per launch from a committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(kernel_key)
+    except ValueError:
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "moe_expert_layer_warp_gb300", "csrc", rec.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec.get("bytes_per_launch") if h == rec.get("source_sha") else None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        j = json.load(open(path))
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def cpu_baseline_sample(budget_s=20.0):
+    """The oracle as it stands on this host's cores (one thread): route and
+    layer output for the tokens of passes n = 1, 2, … of the same workload
+    until the budget is spent. Returns tokens/s and a description."""
+    from moe_expert_layer_warp_gb300 import configs, synth
+    from oracle import oracle
+    import torch
+    w = configs.V2_LITE
+    L = synth.make_layer(w.shape, w.weight_seed, "cpu")
+    H = {k: synth.weights_numpy(getattr(L, a)) for k, a in
+         (("wg", "w_gate"), ("wu", "w_up"), ("wd", "w_down"), ("sg", "ws_gate"),
+          ("su", "ws_up"), ("sd", "ws_down"))}
+    wr = L.w_router.numpy()
+    tokens = 0
+    t0 = time.perf_counter()
+    n_done = []
+    for n in w.pass_sizes:
+        x = synth.make_pass(w.shape.d, n, w.rhos[0], [w.x_seed_base + n])
+        r = oracle.route(x, wr, w.shape.top_k)
+        oracle.union(r["idx"], w.shape.n_experts)
+        oracle.moe_tokens(x, r["idx"], r["w"], H["wg"], H["wu"], H["wd"], H["sg"], H["su"],
+                          H["sd"])
+        tokens += n
+        n_done.append(n)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    del L, H
+    return tokens / el, "float64 oracle: routing, union and layer output of every token of " \
+        "one pass at each n in %s of the same layer shape (%d tokens, %.1f s)" % (
+            n_done, tokens, el), el
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from __graft_entry__ import build
+    build()
+    from moe_expert_layer_warp_gb300 import api, stepmodel
+
+    w, runners, xs = build_workload(dev)
+    stream = torch.cuda.current_stream()
+    tokens_per_step = 2 * sum(w.pass_sizes)
+
+    # warm-up (also configures the kernels before graph capture)
+    for i in range(max(3, args.warmup)):
+        enqueue_step(w, runners, xs, i, stream)
+    torch.cuda.synchronize()
+    st = api.moe_last_device_error()
+    if st != api.MOE_OK:
+        raise RuntimeError("device error during warm-up: %s" % api.status_str(st))
+
+    # one graph per step variant (replica rotation and x variant depend on the step index)
+    n_variants = REPLICAS * N_PASSES_PER_N // math.gcd(REPLICAS, N_PASSES_PER_N)
+    graphs = []
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        for v in range(n_variants):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                enqueue_step(w, runners, xs, v, cap_stream)
+            graphs.append(g)
+    stream.wait_stream(cap_stream)
+    torch.cuda.synchronize()
+    for v in range(n_variants):
+        graphs[v].replay()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[i % n_variants].replay()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_step = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+        dist.barrier()
+    value = world * tokens_per_step / (ms_step * 1e-3)
+
+    st = api.moe_last_device_error()
+    if st != api.MOE_OK:
+        raise RuntimeError("device error in the timed region: %s" % api.status_str(st))
+
+    # breakdown for the step-time model and the engine roofline (outside the timed region)
+    samples, t_fix, pass_ms, alg_b, eng_ms = measure_breakdown(w, runners, xs)
+    rep = stepmodel.build_report(samples, t_fix)
+    e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    achieved = alg_b / (eng_ms * 1e-3) / 1e9
+    per_engine = {}
+    for eng in ("perslot", "dedup"):
+        per_engine[eng] = {
+            "tokens_per_s": [round(n / (statistics.median(pass_ms[eng][n]) * 1e-3), 1)
+                             for n in w.pass_sizes],
+            "pass_us": [round(statistics.median(pass_ms[eng][n]) * 1e3, 2) for n in w.pass_sizes],
+            "expert_GBs": [round(sum(b for b, _ in samples[eng][n]) /
+                                 sum(s for _, s in samples[eng][n]) / 1e9, 1)
+                           for n in w.pass_sizes],
+        }
+        per_engine[eng]["expert_frac_of_peak"] = [round(g / peak, 3)
+                                                  for g in per_engine[eng]["expert_GBs"]]
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, desc, _ = cpu_baseline_sample()
+        cpu = {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1/sqrt(fan_in)) weights, AR(1) hidden states)",
+        "config": {"workload": WORKLOAD, "tokens_per_step": tokens_per_step,
+                   "passes_per_step": 2 * len(w.pass_sizes), "pass_sizes": list(w.pass_sizes),
+                   "rho": w.rhos[0], "weight_replicas": REPLICAS,
+                   "l2": "inputs larger than L2: %d weight replicas of 1.14 GB rotated so "
+                         "consecutive passes read different replicas" % REPLICAS,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "timing": "CUDA-graph replay of each step, CUDA events on the stream"},
+        "roofline": {"kernel": "expert engine call (phase-0 up/gate + phase-1 down launches)",
+                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": load_traffic("expert_engine_v2lite")},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * tokens_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 2 * len(w.pass_sizes) * kernels_per_pass(),
+        "clocks": clk,
+        "engines": per_engine,
+        "stepmodel": rep.as_dict(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from moe_expert_layer_warp_gb300 import configs, synth
+    from oracle import oracle
+    w = configs.V2_LITE
+    L = synth.make_layer(w.shape, w.weight_seed, "cpu")
+    H = {k: synth.weights_numpy(getattr(L, a)) for k, a in
+         (("wg", "w_gate"), ("wu", "w_up"), ("wd", "w_down"), ("sg", "ws_gate"),
+          ("su", "ws_up"), ("sd", "ws_down"))}
+    wr = L.w_router.numpy()
+    passes = {n: synth.make_pass(w.shape.d, n, w.rhos[0], [w.x_seed_base + n])
+              for n in w.pass_sizes}
+
+    def one_token(n, t):
+        x = passes[n]
+        r = oracle.route(x, wr, w.shape.top_k)
+        oracle.union(r["idx"], w.shape.n_experts)
+        oracle.moe_tokens(x, r["idx"], r["w"], H["wg"], H["wu"], H["wd"], H["sg"], H["su"],
+                          H["sd"], tokens=[t])
+
+    t0 = time.perf_counter()
+    one_token(1, 0)
+    t_tok = time.perf_counter() - t0
+    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    per_step = max(1, min(2 * sum(w.pass_sizes), int(budget / max(t_tok, 1e-3))))
+    order = [(n, t) for n in w.pass_sizes for t in range(n)] * 2
+
+    def step():
+        for (n, t) in order[:per_step]:
+            one_token(n, t)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = (time.perf_counter() - t0) / args.steps
+    v = per_step / el
+    desc = ("float64 oracle on the host (1 thread): per step, routing of the pass and the "
+            "layer output of %d tokens taken from the n=1..9 passes of the workload" % per_step)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": per_step},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc, "value": round(v, 4),
+                         "unit": UNIT},
+        "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

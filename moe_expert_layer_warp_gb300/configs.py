@@ -38,7 +38,7 @@ class LayerShape:
 class Workload:
     name: str
     shape: LayerShape
-    pass_sizes: Tuple[int, ...]      # n values
+    pass_sizes: Tuple[int, ...]      # tokens per stream; a pass holds streams × n tokens
     rhos: Tuple[float, ...]          # AR(1) correlation of the hidden states
     weight_seed: int
     x_seed_base: int
@@ -71,7 +71,7 @@ V2_LITE_STACK = Workload(
 
 V3 = Workload(
     name="deepseek-v3-layer", shape=LayerShape(7168, 256, 8, 2048, 1, W_BF16),
-    pass_sizes=(64,), rhos=(0.9,), weight_seed=3, x_seed_base=400, streams=4, passes=8,
+    pass_sizes=(16,), rhos=(0.9,), weight_seed=3, x_seed_base=400, streams=4, passes=8,
     notes="d=7168, 256 routed top-8 + 1 shared, I=2048, bf16 (~22.6 GB); 4 AR(1) streams "
           "x 16 tokens = 64 tokens per pass")
 

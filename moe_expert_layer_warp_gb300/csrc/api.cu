@@ -1,0 +1,274 @@
+// api.cu — the extern "C" entry points of libmoewarp.so declared in
+// include/moe_warp.h: argument checks, scratch layout, kernel launches.
+// Nothing here allocates device memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/moe_warp.h"
+#include "launch.h"
+
+namespace {
+
+// Device error word written by kernels (see common.cuh). One per device the
+// library runs on; host code reaches it through cudaGetSymbolAddress.
+__device__ unsigned int g_moe_err;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned int* err = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+thread_local char g_last_cuda_err[256] = "";
+
+moe_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_cuda_err, sizeof g_last_cuda_err, "%s: %s", where, cudaGetErrorString(e));
+  return MOE_ECUDA;
+}
+
+moe_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_moe_err);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    d.err = static_cast<unsigned int*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_desc(const moe_layer_desc* d) {
+  if (!d) return MOE_EINVAL;
+  if (d->d <= 0 || d->inter <= 0 || d->n_experts <= 0 || d->top_k <= 0) return MOE_EINVAL;
+  if (d->top_k > d->n_experts || d->n_experts > MOE_MAX_EXPERTS || d->top_k > MOE_MAX_TOPK)
+    return MOE_EINVAL;
+  if (d->n_shared < 0 || d->n_shared > MOE_MAX_SHARED) return MOE_EINVAL;
+  if (d->wdtype != MOE_W_F32 && d->wdtype != MOE_W_BF16) return MOE_EINVAL;
+  if (d->d % 64 != 0 || d->inter % 64 != 0) return MOE_EUNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_n(const moe_layer_desc* d, int32_t n) {
+  if (n < 1 || n > MOE_MAX_TOKENS || (int64_t)n * d->top_k > MOE_MAX_PAIRS) return MOE_EINVAL;
+  return MOE_OK;
+}
+
+// Scratch layout for passes of up to n_max tokens (every region 256-byte
+// aligned relative to the workspace base):
+//   logits  [n_max][E] fp32                 routing
+//   h       [n_max·k + s·n_max][I] fp32     SwiGLU activations
+struct WsLayout {
+  size_t logits, h, total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
+  WsLayout L;
+  size_t off = 0;
+  L.logits = off;
+  off = align256(off + (size_t)n_max * d->n_experts * 4);
+  L.h = off;
+  off = align256(off + ((size_t)n_max * d->top_k + (size_t)d->n_shared * n_max) * d->inter * 4);
+  L.total = off;
+  return L;
+}
+
+moe_status check_ws(const moe_layer_desc* d, int32_t n, const void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_EINVAL;
+  if (ws_bytes < ws_layout(d, n).total) return MOE_EINVAL;
+  return MOE_OK;
+}
+
+moe_status check_weights(const moe_layer_desc* d, const moe_layer_weights* w) {
+  if (!w) return MOE_EINVAL;
+  if (!w->w_gate || !w->w_up || !w->w_down) return MOE_EINVAL;
+  if (!aligned16(w->w_gate) || !aligned16(w->w_up) || !aligned16(w->w_down)) return MOE_EINVAL;
+  if (d->n_shared > 0) {
+    if (!w->ws_gate || !w->ws_up || !w->ws_down) return MOE_EINVAL;
+    if (!aligned16(w->ws_gate) || !aligned16(w->ws_up) || !aligned16(w->ws_down))
+      return MOE_EINVAL;
+  }
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                  \
+  do {                                 \
+    moe_status _st = (expr);           \
+    if (_st != MOE_OK) return _st;     \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_layer_desc* desc, int32_t n_max) {
+  if (check_desc(desc) != MOE_OK || check_n(desc, n_max) != MOE_OK) return 0;
+  return ws_layout(desc, n_max).total;
+}
+
+moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const float* x,
+                     int32_t n, int32_t* topk_idx, float* topk_w, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_n(desc, n));
+  if (!w_router || !x || !topk_idx || !topk_w) return MOE_EINVAL;
+  if (!aligned16(w_router) || !aligned16(x)) return MOE_EINVAL;
+  MOE_TRY(check_ws(desc, n, workspace, workspace_bytes));
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  WsLayout L = ws_layout(desc, n);
+  float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.logits);
+  cudaError_t e = moe::launch_route(desc->d, desc->n_experts, desc->top_k, n, x, w_router, logits,
+                                    topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
+}
+
+moe_status moe_build_union(const moe_layer_desc* desc, const int32_t* topk_idx, int32_t n,
+                           const moe_union* u, void* stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_n(desc, n));
+  if (!topk_idx || !u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok ||
+      !u->pair_slot || !u->bytes)
+    return MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(u->bytes) & 7u) != 0) return MOE_EINVAL;
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  cudaError_t e = moe::launch_union(desc->d, desc->inter, desc->n_experts, desc->top_k,
+                                    desc->n_shared, desc->wdtype == MOE_W_F32 ? 4 : 2, n,
+                                    topk_idx, u->union_ids, u->union_count, u->offsets,
+                                    u->pair_tok, u->pair_slot, u->bytes, di->err,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_build_union launch");
+}
+
+static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_layer_weights* w,
+                             const float* x, int32_t n, const int32_t* topk_idx,
+                             const moe_union* u, const float* topk_w, void* workspace,
+                             size_t workspace_bytes, float* y_slot, void* stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_n(desc, n));
+  MOE_TRY(check_weights(desc, w));
+  if (!x || !topk_w || !y_slot || !aligned16(x)) return MOE_EINVAL;
+  MOE_TRY(check_ws(desc, n, workspace, workspace_bytes));
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  WsLayout L = ws_layout(desc, n);
+  moe::ExpertArgs a;
+  memset(&a, 0, sizeof a);
+  a.d = desc->d;
+  a.I = desc->inter;
+  a.E = desc->n_experts;
+  a.k = desc->top_k;
+  a.s = desc->n_shared;
+  a.n = n;
+  a.wdtype = desc->wdtype;
+  a.engine = engine;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_w;
+  if (u) {
+    a.union_ids = u->union_ids;
+    a.union_count = u->union_count;
+    a.offsets = u->offsets;
+    a.pair_tok = u->pair_tok;
+    a.pair_slot = u->pair_slot;
+  }
+  a.x = x;
+  a.w_gate = w->w_gate;
+  a.w_up = w->w_up;
+  a.w_down = w->w_down;
+  a.ws_gate = w->ws_gate;
+  a.ws_up = w->ws_up;
+  a.ws_down = w->ws_down;
+  a.h = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.h);
+  a.y_slot = y_slot;
+  a.err = di->err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = moe::launch_expert_stream(a, 0, di->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert phase 0 launch");
+  e = moe::launch_expert_stream(a, 1, di->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert phase 1 launch");
+  return MOE_OK;
+}
+
+moe_status moe_verify_perslot(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                              const float* x, int32_t n, const int32_t* topk_idx,
+                              const float* topk_w, void* workspace, size_t workspace_bytes,
+                              float* y_slot, void* stream) {
+  if (!topk_idx) return MOE_EINVAL;
+  return run_engine(0, desc, weights, x, n, topk_idx, nullptr, topk_w, workspace,
+                    workspace_bytes, y_slot, stream);
+}
+
+moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                            const float* x, int32_t n, const moe_union* u, const float* topk_w,
+                            void* workspace, size_t workspace_bytes, float* y_slot,
+                            void* stream) {
+  if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot)
+    return MOE_EINVAL;
+  return run_engine(1, desc, weights, x, n, nullptr, u, topk_w, workspace, workspace_bytes,
+                    y_slot, stream);
+}
+
+moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t n, float* y,
+                       void* stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_n(desc, n));
+  if (!y_slot || !y || !aligned16(y_slot) || !aligned16(y)) return MOE_EINVAL;
+  cudaError_t e = moe::launch_combine(desc->d, desc->top_k + desc->n_shared, n, y_slot, y,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
+}
+
+moe_status moe_last_device_error(void* stream) {
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_moe_err, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol");
+  if (word != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_moe_err, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol");
+    snprintf(g_last_cuda_err, sizeof g_last_cuda_err, "device error word 0x%08x", word);
+    return (word & 0xffu) == 3u ? MOE_ETIMEOUT : MOE_EDEVICE;
+  }
+  return MOE_OK;
+}
+
+const char* moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_EINVAL: return "MOE_EINVAL: invalid argument";
+    case MOE_ECUDA: return "MOE_ECUDA: CUDA runtime error";
+    case MOE_ETIMEOUT: return "MOE_ETIMEOUT: a bounded device wait expired";
+    case MOE_EUNSUPPORTED: return "MOE_EUNSUPPORTED: shape not covered";
+    case MOE_EDEVICE: return "MOE_EDEVICE: a device-side check failed";
+  }
+  return "unknown moe_status";
+}
+
+const char* moe_last_cuda_error_string(void) { return g_last_cuda_err; }
+
+}  // extern "C"

@@ -1,0 +1,390 @@
+// expert_stream.cu — the expert FFNs of one verification pass on CUDA cores,
+// with each expert's weights streamed from HBM through a ring of shared-memory
+// stages filled by the TMA engine (cp.async.bulk), one persistent CTA per SM.
+//
+// Sources: "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
+// Kernel Bandwidth and the Best Draft Length", abstract — the per-slot engine
+// reads a selected expert once per token, the deduplicating engine reads each
+// selected expert once per pass for all tokens that chose it; "Deep Dive into
+// Mixture of Experts: From 1991 to DeepSeek-V3", §2 (weighted sum of the
+// selected experts) and §5 (shared experts, unweighted). Each expert is
+// W_down(silu(W_gate x) ⊙ W_up x).
+//
+// Work decomposition. A "group" is one expert applied to a set of ≤ kMaxM
+// tokens; its activation rows live in h (one fp32 row of I per token):
+//   per-slot: one group per (token, slot) pair, rows in pair order t·k + j;
+//   dedup:    one group per union expert (split into groups of ≤ kMaxM
+//             tokens), rows in the union's (expert, token) order;
+//   both:     each shared expert over all n tokens, rows n·k + i·n + t.
+// Phase 0 computes h = silu(W_gate x) ⊙ (W_up x) in tiles of 16 rows of I;
+// phase 1 computes y_slot = w · (W_down h) in tiles of 32 rows of d. A job is
+// (group, tile); CTA b takes jobs b, b+G, b+2G, …
+//
+// Per stage the producer warp copies 32 row chunks of 512 bytes (16 gate + 16
+// up rows, or 32 down rows, K_s = 256 bf16 / 128 fp32 columns) and the
+// matching K_s columns of the group's ≤ kMaxM input rows (x or h, fp32). Each
+// of the 8 consumer warps owns 4 row chunks: lane l holds 16 bytes of each and
+// the same columns of every token, so every weight byte is read from shared
+// memory once and used for all tokens of the group.
+#include <math.h>
+
+#include "../../include/moe_warp.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRowChunks = 32;
+constexpr int kChunkBytes = 512;
+constexpr int kMaxM = 8;
+constexpr int kStages = 6;
+constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
+constexpr int kMaxEntries = MOE_MAX_PAIRS + MOE_MAX_SHARED * (MOE_MAX_TOKENS / kMaxM);
+constexpr int kRowsPhase0 = 16;  // rows of I per phase-0 tile (gate and up)
+constexpr int kRowsPhase1 = 32;  // rows of d per phase-1 tile
+
+struct Entry {
+  int src;   // routed expert id (>= 0), or -(i+1) for shared expert i
+  int row0;  // first activation row
+  int m;     // tokens (1..kMaxM)
+};
+
+template <int WB>
+struct Layout {
+  static constexpr int EPL = 16 / WB;           // weight elements per lane per chunk
+  static constexpr int KS = 32 * EPL;           // K columns per stage
+  static constexpr int kWBytes = kRowChunks * kChunkBytes;
+  static constexpr int kXBytes = kMaxM * KS * 4;
+  static constexpr int kStageBytes = kWBytes + kXBytes;
+  static constexpr int kOffBar = kStages * kStageBytes;
+  static constexpr int kOffPlan = kOffBar + 2 * kStages * 8;
+  static constexpr int kOffRowTok = kOffPlan + kMaxEntries * (int)sizeof(Entry);
+  static constexpr int kOffRowOut = kOffRowTok + kMaxRows * 4;
+  static constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
+  static constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
+  static constexpr int kBytes = kOffMisc + 64 * 4;
+};
+
+// Exclusive prefix sum over the block (one value per thread). Returns the
+// thread's offset; *total receives the sum. Uses scratch[0..warps].
+MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = scratch[w];
+      scratch[w] = run;
+      run += c;
+    }
+    scratch[nwarps] = run;
+  }
+  __syncthreads();
+  const int r = scratch[warp] + inc - v;
+  *total = scratch[nwarps];
+  __syncthreads();
+  return r;
+}
+
+// Builds the group table and the per-row maps (token, output slot row,
+// combine weight) in shared memory. Returns the number of groups.
+MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_tok, int* row_out,
+                       float* row_w, int* scratch) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int P = a.n * a.k, S = a.k + a.s;
+  int nr;
+  if (a.engine == 0) {
+    for (int p = tid; p < P; p += nt) {
+      const int t = p / a.k, j = p - t * a.k;
+      plan[p] = Entry{a.topk_idx[p], p, 1};
+      row_tok[p] = t;
+      row_out[p] = t * S + j;
+      row_w[p] = a.topk_w[p];
+    }
+    nr = P;
+  } else {
+    int U = *a.union_count;
+    if (U < 0 || U > a.E) {  // not a union of this layer: run nothing, flag it
+      if (tid == 0) report_error(a.err, ERR_CHECK, 0x230);
+      U = 0;
+    }
+    int m = 0, e = 0, r0 = 0;
+    if (tid < U) {
+      r0 = a.offsets[tid];
+      m = a.offsets[tid + 1] - r0;
+      e = a.union_ids[tid];
+    }
+    const int nsub = (m + kMaxM - 1) / kMaxM;
+    const int pos = block_exclusive_scan(nsub, scratch, &nr);
+    for (int q = 0; q < nsub; ++q)
+      plan[pos + q] = Entry{e, r0 + q * kMaxM, min(kMaxM, m - q * kMaxM)};
+    for (int r = tid; r < P; r += nt) {
+      const int t = a.pair_tok[r], j = a.pair_slot[r];
+      row_tok[r] = t;
+      row_out[r] = t * S + j;
+      row_w[r] = a.topk_w[t * a.k + j];
+    }
+  }
+  const int per = (a.n + kMaxM - 1) / kMaxM;
+  for (int q = tid; q < a.s * per; q += nt) {
+    const int i = q / per, c = q - (q / per) * per;
+    plan[nr + q] = Entry{-(i + 1), P + i * a.n + c * kMaxM, min(kMaxM, a.n - c * kMaxM)};
+  }
+  for (int r = tid; r < a.s * a.n; r += nt) {
+    const int i = r / a.n, t = r - (r / a.n) * a.n;
+    row_tok[P + r] = t;
+    row_out[P + r] = t * S + a.k + i;
+    row_w[P + r] = 1.f;
+  }
+  return nr + a.s * per;
+}
+
+template <int EPL>
+MOE_DEV void load_w(const char* p, float (&w)[EPL]);
+
+template <>
+MOE_DEV void load_w<8>(const char* p, float (&w)[8]) {  // 8 bf16
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  w[0] = bf16lo(v.x); w[1] = bf16hi(v.x);
+  w[2] = bf16lo(v.y); w[3] = bf16hi(v.y);
+  w[4] = bf16lo(v.z); w[5] = bf16hi(v.z);
+  w[6] = bf16lo(v.w); w[7] = bf16hi(v.w);
+}
+
+template <>
+MOE_DEV void load_w<4>(const char* p, float (&w)[4]) {  // 4 fp32
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+}
+
+template <int EPL>
+MOE_DEV void load_x(const float* p, float (&x)[EPL]) {
+#pragma unroll
+  for (int i = 0; i < EPL; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p + i);
+    x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+  }
+}
+
+template <int WB, int PHASE>
+__global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const ExpertArgs a) {
+  using L = Layout<WB>;
+  constexpr int EPL = L::EPL, KS = L::KS;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* empty = full + kStages;
+  Entry* plan = reinterpret_cast<Entry*>(smem + L::kOffPlan);
+  int* row_tok = reinterpret_cast<int*>(smem + L::kOffRowTok);
+  int* row_out = reinterpret_cast<int*>(smem + L::kOffRowOut);
+  float* row_w = reinterpret_cast<float*>(smem + L::kOffRowW);
+  int* misc = reinterpret_cast<int*>(smem + L::kOffMisc);  // [0..31] scan scratch
+  volatile int* abort_flag = misc + 40;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  const int n_groups = build_plan(a, plan, row_tok, row_out, row_w, misc);
+  __syncthreads();
+
+  const int K = PHASE == 0 ? a.d : a.I;         // reduction length
+  const int rows_out = PHASE == 0 ? a.I : a.d;  // output rows per expert
+  const int tile_rows = PHASE == 0 ? kRowsPhase0 : kRowsPhase1;
+  const int n_tiles = rows_out / tile_rows;
+  const int n_jobs = n_groups * n_tiles;
+  const int nks = (K + KS - 1) / KS;
+  const size_t mat = (size_t)a.I * a.d * WB;    // bytes of one expert matrix
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------- producer warp --
+    const uint64_t pol_w = l2_evict_first_policy();
+    const uint64_t pol_x = l2_evict_last_policy();
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int job = blockIdx.x; job < n_jobs && ok; job += gridDim.x) {
+      const Entry en = plan[job / n_tiles];
+      const int tile = job - (job / n_tiles) * n_tiles;
+      const char* w0;
+      const char* w1;
+      if (PHASE == 0) {
+        const char* g = en.src >= 0 ? (const char*)a.w_gate + (size_t)en.src * mat
+                                    : (const char*)a.ws_gate + (size_t)(-en.src - 1) * mat;
+        const char* u = en.src >= 0 ? (const char*)a.w_up + (size_t)en.src * mat
+                                    : (const char*)a.ws_up + (size_t)(-en.src - 1) * mat;
+        const size_t rowoff = (size_t)(tile * kRowsPhase0 + (lane & 15)) * K * WB;
+        w0 = (lane < 16 ? g : u) + rowoff;
+        w1 = nullptr;
+      } else {
+        const char* dn = en.src >= 0 ? (const char*)a.w_down + (size_t)en.src * mat
+                                     : (const char*)a.ws_down + (size_t)(-en.src - 1) * mat;
+        w0 = dn + (size_t)(tile * kRowsPhase1 + lane) * K * WB;
+        w1 = nullptr;
+      }
+      (void)w1;
+      const float* xrow = nullptr;
+      if (lane < en.m) {
+        xrow = PHASE == 0 ? a.x + (size_t)row_tok[en.row0 + lane] * a.d
+                          : a.h + (size_t)(en.row0 + lane) * a.I;
+      }
+      for (int ks = 0; ks < nks; ++ks) {
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const int k0 = ks * KS;
+        const int klen = min(KS, K - k0);
+        if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x200 + PHASE)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        unsigned char* st = smem + stage * L::kStageBytes;
+        const uint32_t wbytes = (uint32_t)klen * WB;
+        const uint32_t xbytes = (uint32_t)klen * 4;
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], kRowChunks * wbytes + en.m * xbytes);
+        __syncwarp();
+        bulk_g2s(st + lane * kChunkBytes, w0 + (size_t)k0 * WB, wbytes, &full[stage], pol_w);
+        if (lane < en.m)
+          bulk_g2s(st + L::kWBytes + lane * KS * 4, xrow + k0, xbytes, &full[stage], pol_x);
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // Give copies already issued a bounded chance to land before the CTA
+      // exits, so that none writes into shared memory after it is released.
+      const int outstanding = min(issued, kStages);
+      for (int i = 1; i <= outstanding; ++i) {
+        const int idx = issued - i;
+        mbar_wait(&full[idx % kStages], (uint32_t)((idx / kStages) & 1), a.err, 0x210 + PHASE);
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------- consumer warps --
+  int chunk[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    chunk[q] = PHASE == 0 ? (q < 2 ? 2 * warp + q : 16 + 2 * warp + (q - 2)) : 4 * warp + q;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int job = blockIdx.x; job < n_jobs; job += gridDim.x) {
+    const Entry en = plan[job / n_tiles];
+    const int tile = job - (job / n_tiles) * n_tiles;
+    const int m = en.m;
+    float acc[4][kMaxM];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int t = 0; t < kMaxM; ++t) acc[q][t] = 0.f;
+    for (int ks = 0; ks < nks; ++ks) {
+      const int klen = min(KS, K - ks * KS);
+      if (!mbar_wait(&full[stage], phase, a.err, 0x220 + PHASE)) {
+        *abort_flag = 1;
+        return;
+      }
+      if (lane * EPL < klen) {
+        const unsigned char* st = smem + stage * L::kStageBytes;
+        const float* sx = reinterpret_cast<const float*>(st + L::kWBytes) + lane * EPL;
+        float wv[4][EPL];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          load_w<EPL>(reinterpret_cast<const char*>(st) + chunk[q] * kChunkBytes + lane * 16, wv[q]);
+#pragma unroll
+        for (int t = 0; t < kMaxM; ++t) {
+          if (t < m) {
+            float xv[EPL];
+            load_x<EPL>(sx + t * KS, xv);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) acc[q][t] = fmaf(wv[q][e], xv[e], acc[q][t]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int t = 0; t < kMaxM; ++t)
+        if (t < m) acc[q][t] = warp_sum(acc[q][t]);
+    if (lane == 0) {
+      if (PHASE == 0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int row = tile * kRowsPhase0 + 2 * warp + q;
+#pragma unroll
+          for (int t = 0; t < kMaxM; ++t)
+            if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(acc[q][t]) * acc[q + 2][t];
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int row = tile * kRowsPhase1 + 4 * warp + q;
+#pragma unroll
+          for (int t = 0; t < kMaxM; ++t) {
+            if (t < m) {
+              const int r = en.row0 + t;
+              a.y_slot[(size_t)row_out[r] * a.d + row] = row_w[r] * acc[q][t];
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int WB, int PHASE>
+cudaError_t launch_one(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
+  auto kern = expert_stream_kernel<WB, PHASE>;
+  constexpr int bytes = Layout<WB>::kBytes;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  kern<<<num_sms, kThreads, bytes, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_expert_stream(const ExpertArgs& a, int phase, int num_sms,
+                                 cudaStream_t stream) {
+  if (a.wdtype == 1)
+    return phase == 0 ? launch_one<2, 0>(a, num_sms, stream) : launch_one<2, 1>(a, num_sms, stream);
+  return phase == 0 ? launch_one<4, 0>(a, num_sms, stream) : launch_one<4, 1>(a, num_sms, stream);
+}
+
+}  // namespace moe

@@ -1,0 +1,285 @@
+// route_union.cu — routing (gate GEMV + top-k + softmax over the kept
+// logits), the union of selected experts, and the weighted combine.
+//
+// Sources: "Deep Dive into Mixture of Experts: From 1991 to DeepSeek-V3",
+// §2 (top-k gating sketch: logits = x·W_g, topk, softmax over the k kept
+// logits, output = Σ weight·expert(x)) and §5 (shared experts added
+// unweighted); "Speculative Decoding for Mixture-of-Experts Models: Expert
+// Bytes, Kernel Bandwidth and the Best Draft Length", abstract (the union of
+// selected experts is what a deduplicating engine reads once per pass).
+#include <math.h>
+
+#include "../../include/moe_warp.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------------ gate --
+// One warp per expert row of W_g, kGateTokens tokens per CTA. The dot is
+// accumulated with error-free transformations (TwoProd by FMA, Knuth's
+// TwoSum) — the compensated dot of Ogita, Rump and Oishi (2005) — so the
+// returned fp32 logit is the exact dot rounded once, up to a term of order
+// u²·Σ|x_i·w_i|. That keeps the top-k selection identical to an exact
+// computation except at near-ties far below fp32 resolution.
+constexpr int kGateWarps = 8;
+constexpr int kGateTokens = 8;
+
+MOE_DEV void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+MOE_DEV void dot2_step(float a, float b, float& s, float& c) {
+  const float p = __fmul_rn(a, b);
+  const float ep = __fmaf_rn(a, b, -p);  // exact: a·b = p + ep
+  float es;
+  two_sum(s, p, s, es);                  // exact: s_old + p = s + es
+  c = __fadd_rn(c, __fadd_rn(ep, es));
+}
+
+__global__ void __launch_bounds__(kGateWarps * 32)
+    gate_logits_kernel(int d, int E, int n, const float* __restrict__ x,
+                       const float* __restrict__ wg, float* __restrict__ logits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kGateWarps + warp;
+  const int t0 = blockIdx.y * kGateTokens;
+  if (e >= E) return;
+  const int nt = min(kGateTokens, n - t0);
+  float s[kGateTokens], c[kGateTokens];
+#pragma unroll
+  for (int t = 0; t < kGateTokens; ++t) s[t] = c[t] = 0.f;
+  const float4* wrow = reinterpret_cast<const float4*>(wg + (size_t)e * d);
+  const int d4 = d >> 2;
+#pragma unroll 2
+  for (int i = lane; i < d4; i += 32) {
+    const float4 w = __ldg(wrow + i);
+#pragma unroll
+    for (int t = 0; t < kGateTokens; ++t) {
+      if (t < nt) {
+        const float4 xv = __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + t) * d) + i);
+        dot2_step(w.x, xv.x, s[t], c[t]);
+        dot2_step(w.y, xv.y, s[t], c[t]);
+        dot2_step(w.z, xv.z, s[t], c[t]);
+        dot2_step(w.w, xv.w, s[t], c[t]);
+      }
+    }
+  }
+  // Butterfly combine of the (sum, compensation) pairs; TwoSum is exact and
+  // commutative, so every lane ends with the same pair.
+#pragma unroll
+  for (int t = 0; t < kGateTokens; ++t) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float so = __shfl_xor_sync(0xffffffffu, s[t], o);
+      const float co = __shfl_xor_sync(0xffffffffu, c[t], o);
+      float sn, en;
+      two_sum(s[t], so, sn, en);
+      c[t] = __fadd_rn(__fadd_rn(c[t], co), en);
+      s[t] = sn;
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int t = 0; t < kGateTokens; ++t)
+      if (t < nt) logits[(size_t)(t0 + t) * E + e] = __fadd_rn(s[t], c[t]);
+  }
+}
+
+// ------------------------------------------------------------------ top-k --
+// One warp per token. Expert e lives in lane e%32, register e/32. k rounds of
+// warp argmax; the larger logit wins, equal logits go to the lower index.
+constexpr int kTopkWarps = 8;
+constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
+
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    topk_kernel(int E, int k, int n, const float* __restrict__ logits,
+                int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t >= n) return;
+  float v[kPerLane];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int r = 0; r < kPerLane; ++r) {
+    const int e = lane + 32 * r;
+    if (e < E) {
+      v[r] = logits[(size_t)t * E + e];
+    } else {
+      v[r] = -INFINITY;
+      taken |= 1u << r;
+    }
+  }
+  float my_v = 0.f, v0 = 0.f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int r = 0; r < kPerLane; ++r) {
+      if (!((taken >> r) & 1u)) {
+        const int e = lane + 32 * r;
+        if (v[r] > bv || (v[r] == bv && e < be)) {
+          bv = v[r];
+          be = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (j == 0) v0 = bv;
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  const float ej = (lane < k) ? expf(my_v - v0) : 0.f;
+  const float z = warp_sum(ej);
+  if (lane < k) {
+    topk_idx[(size_t)t * k + lane] = my_e;
+    topk_w[(size_t)t * k + lane] = ej / z;
+  }
+}
+
+// ------------------------------------------------------------------ union --
+// One CTA. Counting sort of the n·k (token, slot) pairs by expert; the rank of
+// a pair inside its expert is the number of earlier pairs (token-major order)
+// with the same expert, so the result is independent of scheduling.
+constexpr int kUnionThreads = 512;
+
+__global__ void __launch_bounds__(kUnionThreads)
+    union_kernel(int E, int k, int n, uint64_t expert_bytes, int s,
+                 const int32_t* __restrict__ topk_idx, int32_t* __restrict__ union_ids,
+                 int32_t* __restrict__ union_count, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ pair_tok, int32_t* __restrict__ pair_slot,
+                 uint64_t* __restrict__ bytes, unsigned int* err) {
+  __shared__ int sidx[MOE_MAX_PAIRS];
+  __shared__ int cnt[MOE_MAX_EXPERTS];
+  __shared__ int start[MOE_MAX_EXPERTS];
+  const int P = n * k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int p = tid; p < P; p += blockDim.x) {
+    int v = topk_idx[p];
+    if (v < 0 || v >= E) {
+      report_error(err, ERR_CHECK, 0x101);
+      v = 0;
+    }
+    sidx[p] = v;
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += blockDim.x) atomicAdd(&cnt[sidx[p]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // lane owns experts [8·lane, 8·lane+8)
+    constexpr int per = MOE_MAX_EXPERTS / 32;
+    int lc[per];
+    int sc = 0, sp = 0;
+#pragma unroll
+    for (int r = 0; r < per; ++r) {
+      const int e = lane * per + r;
+      lc[r] = (e < E) ? cnt[e] : 0;
+      sc += lc[r];
+      sp += (lc[r] > 0);
+    }
+    int ic = sc, ip = sp;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int tc = __shfl_up_sync(0xffffffffu, ic, o);
+      const int tp = __shfl_up_sync(0xffffffffu, ip, o);
+      if (lane >= o) {
+        ic += tc;
+        ip += tp;
+      }
+    }
+    int ec = ic - sc, ep = ip - sp;
+#pragma unroll
+    for (int r = 0; r < per; ++r) {
+      const int e = lane * per + r;
+      if (e < E) {
+        start[e] = ec;
+        if (lc[r] > 0) {
+          union_ids[ep] = e;
+          offsets[ep] = ec;
+          ++ep;
+        }
+        ec += lc[r];
+      }
+    }
+    if (lane == 31) {
+      offsets[ip] = ic;
+      *union_count = ip;
+      bytes[0] = (uint64_t)P * expert_bytes;
+      bytes[1] = (uint64_t)ip * expert_bytes;
+      bytes[2] = (uint64_t)s * expert_bytes;
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int e = sidx[p];
+    int rank = 0;
+    for (int q = 0; q < p; ++q) rank += (sidx[q] == e);
+    const int row = start[e] + rank;
+    pair_tok[row] = p / k;
+    pair_slot[row] = p - (p / k) * k;
+  }
+}
+
+// ---------------------------------------------------------------- combine --
+__global__ void __launch_bounds__(256)
+    combine_kernel(int d, int slots, const float* __restrict__ y_slot, float* __restrict__ y) {
+  const int t = blockIdx.y;
+  const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c4 * 4 >= d) return;
+  const float4* src = reinterpret_cast<const float4*>(y_slot + (size_t)t * slots * d) + c4;
+  float4 acc = __ldg(src);
+  for (int j = 1; j < slots; ++j) {
+    const float4 v = __ldg(src + (size_t)j * (d >> 2));
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  reinterpret_cast<float4*>(y + (size_t)t * d)[c4] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
+                         float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
+  dim3 g1((E + kGateWarps - 1) / kGateWarps, (n + kGateTokens - 1) / kGateTokens);
+  gate_logits_kernel<<<g1, kGateWarps * 32, 0, stream>>>(d, E, n, x, w_router, logits);
+  dim3 g2((n + kTopkWarps - 1) / kTopkWarps);
+  topk_kernel<<<g2, kTopkWarps * 32, 0, stream>>>(E, k, n, logits, topk_idx, topk_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
+                         const int32_t* topk_idx, int32_t* union_ids, int32_t* union_count,
+                         int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
+                         uint64_t* bytes, unsigned int* err, cudaStream_t stream) {
+  const uint64_t eb = 3ull * (uint64_t)d * (uint64_t)I * (uint64_t)wbytes;
+  union_kernel<<<1, kUnionThreads, 0, stream>>>(E, k, n, eb, s, topk_idx, union_ids,
+                                                union_count, offsets, pair_tok, pair_slot,
+                                                bytes, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,
+                           cudaStream_t stream) {
+  dim3 g((d / 4 + 255) / 256, n);
+  combine_kernel<<<g, 256, 0, stream>>>(d, slots, y_slot, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,93 @@
+"""Host-only checks of the C ABI: the library builds and loads, it exports
+every function include/moe_warp.h declares, and bad arguments are rejected on
+the host before any launch (these calls touch no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_layer_warp_gb300 import api, build
+from moe_expert_layer_warp_gb300.configs import ALL, LayerShape, W_BF16
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def _declared():
+    names = []
+    for h in sorted(os.listdir(HEADER_DIR)):
+        if h.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(moe_\w+)\s*\(", text,
+                                re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "moe_route" in names and "moe_verify_dedup" in names
+    for n in names:
+        assert hasattr(lib, n), "libmoewarp.so does not export %s" % n
+    assert set(api.EXPORTED) <= set(names)
+
+
+def test_workspace_bytes_closed_form(lib):
+    for w in ALL:
+        sh = w.shape
+        n = max(w.pass_sizes) * w.streams
+        got = api.moe_workspace_bytes(api.make_desc(sh), n)
+        a256 = lambda v: (v + 255) // 256 * 256
+        want = a256(n * sh.n_experts * 4) + a256((n * sh.top_k + sh.n_shared * n) * sh.inter * 4)
+        assert got == want, w.name
+
+
+def test_invalid_shapes_are_rejected(lib):
+    bad = [LayerShape(2048, 64, 0, 1408, 2, W_BF16),     # k = 0
+           LayerShape(2048, 4, 6, 1408, 2, W_BF16),      # k > E
+           LayerShape(2048, 300, 6, 1408, 2, W_BF16),    # E > 256
+           LayerShape(2048, 64, 6, 1408, 9, W_BF16),     # s > 4
+           LayerShape(2000, 64, 6, 1408, 2, W_BF16),     # d not a multiple of 64
+           LayerShape(2048, 64, 6, 1408, 2, 7)]          # unknown dtype
+    for sh in bad:
+        assert api.moe_workspace_bytes(api.make_desc(sh), 4) == 0
+    good = api.make_desc(LayerShape(2048, 64, 6, 1408, 2, W_BF16))
+    assert api.moe_workspace_bytes(good, 0) == 0        # n < 1
+    assert api.moe_workspace_bytes(good, 86) == 0       # n·k > 512
+    assert api.moe_workspace_bytes(good, 85) > 0
+
+
+def test_null_and_misaligned_pointers_return_einval(lib):
+    d = api.make_desc(LayerShape(256, 8, 2, 512, 0, 0))
+    z = ctypes.c_void_p(0)
+    one = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4096 + 4)
+    st = lib.moe_route(ctypes.byref(d), z, one, 4, one, one, one, 1 << 20, z)
+    assert st == api.MOE_EINVAL
+    st = lib.moe_route(ctypes.byref(d), one, odd, 4, one, one, one, 1 << 20, z)
+    assert st == api.MOE_EINVAL
+    st = lib.moe_route(ctypes.byref(d), one, one, 4, one, one, ctypes.c_void_p(4096 + 64),
+                       1 << 20, z)   # workspace not 256-byte aligned
+    assert st == api.MOE_EINVAL
+    st = lib.moe_route(ctypes.byref(d), one, one, 4, one, one, one, 16, z)   # too small
+    assert st == api.MOE_EINVAL
+    u = api.UnionC()
+    assert lib.moe_build_union(ctypes.byref(d), one, 4, ctypes.byref(u), z) == api.MOE_EINVAL
+    w = api.LayerWeightsC()
+    assert lib.moe_verify_perslot(ctypes.byref(d), ctypes.byref(w), one, 4, one, one, one,
+                                  1 << 20, one, z) == api.MOE_EINVAL
+    assert lib.moe_verify_dedup(ctypes.byref(d), ctypes.byref(w), one, 4, ctypes.byref(u), one,
+                                one, 1 << 20, one, z) == api.MOE_EINVAL
+    assert lib.moe_combine(ctypes.byref(d), z, 4, one, z) == api.MOE_EINVAL
+    assert lib.moe_combine(ctypes.byref(d), one, 0, one, z) == api.MOE_EINVAL
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert api.status_str(s).startswith("MOE_")

@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on
+the same seeded inputs.
+
+Small layers are compared on every output element; they span several row
+tiles and K stages with ragged K tails, groups split beyond 8 tokens, k = E,
+k = 1, the largest pass (n·k = 512), n = 1 and identical tokens. The five
+workload shapes run at full size in the launch configuration the benchmark
+times and are compared on sampled tokens (routing, union and bytes on every
+token). Both engines are checked, and against each other.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from moe_expert_layer_warp_gb300 import configs, synth
+from moe_expert_layer_warp_gb300.configs import LayerShape, W_BF16, W_F32
+from moe_expert_layer_warp_gb300.layer import DEDUP, PERSLOT, PassRunner
+from oracle import oracle
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from moe_expert_layer_warp_gb300 import api, build
+    build.build()
+    api.load()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def run_both(L, x_np, runner=None):
+    """Runs the pass through both engines; returns host copies of everything."""
+    dev = L.device
+    n = x_np.shape[0]
+    R = runner or PassRunner(L, n)
+    x = torch.from_numpy(x_np).to(dev)
+    out = {}
+    y_ps = R.forward(x, PERSLOT).cpu().numpy()
+    slots_ps = R.slots(n).cpu().numpy()
+    idx, w = (t.cpu().numpy() for t in R.routing(n))
+    u = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in R.union(n).items()}
+    y_dd = R.forward(x, DEDUP).cpu().numpy()
+    slots_dd = R.slots(n).cpu().numpy()
+    from moe_expert_layer_warp_gb300 import api
+    assert api.moe_last_device_error() == api.MOE_OK
+    out.update(y_ps=y_ps, y_dd=y_dd, slots_ps=slots_ps, slots_dd=slots_dd, idx=idx, w=w, u=u)
+    return out
+
+
+def check_pass(L, x_np, tokens=None, runner=None):
+    sh = L.shape
+    g = run_both(L, x_np, runner)
+    orc = oracle.route(x_np, L.w_router.cpu().numpy(), sh.top_k)
+    amb = pu.check_routing(g["idx"], g["w"], orc, sh.d)
+    assert amb <= max(1, x_np.shape[0] // 20), "too many tie-ambiguous tokens: %d" % amb
+    n = x_np.shape[0]
+    if amb == 0:
+        ou = oracle.union(orc["idx"], sh.n_experts)
+        u = g["u"]
+        assert u["count"] == ou["count"]
+        np.testing.assert_array_equal(u["union_ids"], ou["union_ids"])
+        np.testing.assert_array_equal(u["offsets"], ou["offsets"])
+        np.testing.assert_array_equal(u["pair_tok"], ou["pair_tok"])
+        np.testing.assert_array_equal(u["pair_slot"], ou["pair_slot"])
+        b = oracle.bytes_per_pass(sh.d, sh.inter, sh.top_k, sh.n_shared, n, sh.wdtype,
+                                  ou["count"])
+        assert [int(v) for v in u["bytes"]] == b
+    toks = list(range(n)) if tokens is None else list(tokens)
+    y_o, slots_o = pu.oracle_outputs(L, x_np, orc, toks)
+    tol = pu.y_tol(sh)
+    pu.assert_close_rms(g["y_ps"][toks], y_o, tol, "per-slot y")
+    pu.assert_close_rms(g["y_dd"][toks], y_o, tol, "dedup y")
+    pu.assert_close_rms(g["slots_ps"][toks], slots_o, tol, "per-slot slots")
+    pu.assert_close_rms(g["slots_dd"][toks], slots_o, tol, "dedup slots")
+    ref = g["y_ps"].astype(np.float64)
+    pu.assert_close_rms(g["y_dd"], ref, tol, "dedup vs per-slot")
+    return g
+
+
+SMALL = [
+    ("f32-ragged", LayerShape(192, 6, 3, 256, 1, W_F32), [1, 2, 7]),
+    ("bf16-ragged", LayerShape(576, 16, 4, 320, 1, W_BF16), [1, 5, 16, 33]),
+    ("k-equals-E", LayerShape(128, 4, 4, 128, 0, W_BF16), [3]),
+    ("top-1", LayerShape(128, 8, 1, 64, 2, W_F32), [5]),
+    ("max-pairs", LayerShape(256, 32, 4, 128, 1, W_BF16), [128]),
+]
+
+
+@pytest.mark.parametrize("name,shape,ns", SMALL, ids=[s[0] for s in SMALL])
+def test_small_layers_every_element(name, shape, ns):
+    L = synth.make_layer(shape, 17, "cuda")
+    R = PassRunner(L, max(ns))
+    for n in ns:
+        x = synth.make_pass(shape.d, n, 0.9, [123 + n])
+        check_pass(L, x, runner=R)
+
+
+def test_tiny_workload_every_element():
+    w = configs.TINY
+    L = synth.make_layer(w.shape, w.weight_seed, "cuda")
+    x = synth.make_pass(w.shape.d, w.pass_sizes[0], w.rhos[0], [w.x_seed_base])
+    check_pass(L, x)
+
+
+def test_identical_tokens_select_k_experts():
+    shape = LayerShape(512, 32, 4, 256, 1, W_BF16)
+    L = synth.make_layer(shape, 5, "cuda")
+    x = np.repeat(synth.make_pass(512, 1, 0.0, [3]), 9, axis=0)
+    g = check_pass(L, x)
+    assert g["u"]["count"] == 4
+
+
+def test_repeated_runs_are_bitwise_identical():
+    shape = LayerShape(576, 16, 4, 320, 1, W_BF16)
+    L = synth.make_layer(shape, 29, "cuda")
+    x = synth.make_pass(576, 11, 0.9, [77])
+    a = run_both(L, x)
+    b = run_both(L, x)
+    for key in ("y_ps", "y_dd", "idx", "w"):
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def _workload_pass(w, n, rho, p):
+    seeds = [w.x_seed_base + w.streams * p + s for s in range(w.streams)]
+    return synth.make_pass(w.shape.d, n, rho, seeds)
+
+
+def test_v2_lite_layer_full_size():
+    w = configs.V2_LITE
+    L = synth.make_layer(w.shape, w.weight_seed, "cuda")
+    R = PassRunner(L, max(w.pass_sizes))
+    for n in w.pass_sizes:
+        x = _workload_pass(w, n, w.rhos[0], 0)
+        check_pass(L, x, tokens=sorted({0, n - 1}), runner=R)
+    del L, R
+    torch.cuda.empty_cache()
+
+
+def test_mixtral_layer_full_size():
+    w = configs.MIXTRAL
+    L = synth.make_layer(w.shape, w.weight_seed, "cuda")
+    R = PassRunner(L, max(w.pass_sizes))
+    for n, rho in [(1, 0.9), (2, 0.0), (8, 0.5), (16, 0.9), (16, 0.0)]:
+        x = _workload_pass(w, n, rho, 0)
+        check_pass(L, x, tokens=[n - 1], runner=R)
+    del L, R
+    torch.cuda.empty_cache()
+
+
+def test_v3_layer_full_size():
+    w = configs.V3
+    L = synth.make_layer(w.shape, w.weight_seed, "cuda")
+    x = _workload_pass(w, w.pass_sizes[0], w.rhos[0], 0)
+    check_pass(L, x, tokens=[0, 37, 63])
+    del L
+    torch.cuda.empty_cache()
+
+
+def test_v2_lite_stack_layers_full_size():
+    """Two layers of the 26-layer stack (first and last seeds), each on the
+    same pass, as the stack runs them."""
+    w = configs.V2_LITE_STACK
+    for layer in (0, w.layers - 1):
+        L = synth.make_layer(w.shape, w.weight_seed + layer, "cuda")
+        x = _workload_pass(w, 9, 0.99, 0)
+        check_pass(L, x, tokens=[4])
+        del L
+        torch.cuda.empty_cache()
