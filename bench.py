@@ -46,6 +46,10 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--case", default=None,
+                   help="profiling case WORKLOAD:ENGINE:N (e.g. v2lite:perslot:1): runs "
+                        "--passes passes of one layer and prints their mean time")
+    p.add_argument("--passes", type=int, default=4)
     return p.parse_args()
 
 
@@ -460,9 +464,51 @@ def run_reference(args):
     }), flush=True)
 
 
+CASES = {"tiny": "TINY", "v2lite": "V2_LITE", "mixtral": "MIXTRAL", "v3": "V3"}
+
+
+def run_case(args):
+    """A small single-layer case for profilers: one layer, a few passes, no
+    graph, no replicas. Prints the mean pass and engine time."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    from moe_expert_layer_warp_gb300 import api, configs, synth
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    wname, eng, n = args.case.split(":")
+    w = getattr(configs, CASES[wname])
+    n = int(n)
+    L = synth.make_layer(w.shape, w.weight_seed, "cuda")
+    x = torch.from_numpy(synth.make_pass(w.shape.d, n, w.rhos[-1],
+                                         [w.x_seed_base + s for s in range(w.streams)])).cuda()
+    R = PassRunner(L, x.shape[0])
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(args.passes):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        R.route(x, st)
+        R.build_union(x.shape[0], st)
+        e[0].record(st)
+        R.experts(x, eng, st)
+        e[1].record(st)
+        R.combine(x.shape[0], st)
+        torch.cuda.synchronize()
+        ts.append(e[0].elapsed_time(e[1]))
+    if api.moe_last_device_error() != api.MOE_OK:
+        raise RuntimeError("device error")
+    b = [int(v) for v in R.bytes.cpu().tolist()]
+    req = (b[0] if eng == "perslot" else b[1]) + b[2]
+    ms = statistics.median(ts)
+    print(json.dumps({"case": args.case, "tokens": x.shape[0], "engine_ms": round(ms, 4),
+                      "requested_bytes": req, "GBs": round(req / ms / 1e6, 1),
+                      "union": int(R.union_count.item())}))
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -76,8 +76,9 @@ moe_status check_n(const moe_layer_desc* d, int32_t n) {
 // aligned relative to the workspace base):
 //   logits  [n_max][E] fp32                 routing
 //   h       [n_max·k + s·n_max][I] fp32     SwiGLU activations
+//   xg      [n_max·k][d] fp32                x rows gathered in union order
 struct WsLayout {
-  size_t logits, h, total;
+  size_t logits, h, xg, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -89,6 +90,8 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   off = align256(off + (size_t)n_max * d->n_experts * 4);
   L.h = off;
   off = align256(off + ((size_t)n_max * d->top_k + (size_t)d->n_shared * n_max) * d->inter * 4);
+  L.xg = off;
+  off = align256(off + (size_t)n_max * d->top_k * d->d * 4);
   L.total = off;
   return L;
 }
@@ -200,6 +203,7 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.ws_up = w->ws_up;
   a.ws_down = w->ws_down;
   a.h = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.h);
+  a.xg = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.xg);
   a.y_slot = y_slot;
   a.err = di->err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1,6 +1,6 @@
 // expert_stream.cu — the expert FFNs of one verification pass on CUDA cores,
-// with each expert's weights streamed from HBM through a ring of shared-memory
-// stages filled by the TMA engine (cp.async.bulk), one persistent CTA per SM.
+// with each expert's weights streamed from HBM by tensor-map TMA into a ring
+// of shared-memory stages, one persistent CTA per SM.
 //
 // Sources: "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
 // Kernel Bandwidth and the Best Draft Length", abstract — the per-slot engine
@@ -20,17 +20,20 @@
 // phase 1 computes y_slot = w · (W_down h) in tiles of 32 rows of d. A job is
 // (group, tile); CTA b takes jobs b, b+G, b+2G, …
 //
-// Per stage the producer warp copies 32 row chunks of 512 bytes (16 gate + 16
-// up rows, or 32 down rows, K_s = 256 bf16 / 128 fp32 columns) and the
-// matching K_s columns of the group's ≤ kMaxM input rows (x or h, fp32). Each
-// of the 8 consumer warps owns 4 row chunks: lane l holds 16 bytes of each and
-// the same columns of every token, so every weight byte is read from shared
-// memory once and used for all tokens of the group.
+// Per stage the producer thread issues one TMA box per weight matrix (16 rows
+// of W_gate and 16 of W_up, or 32 rows of W_down, × K_s = 256 bf16 / 128 fp32
+// columns: 16 KB) and one box of the group's input rows (1 or 8 rows × K_s
+// fp32 columns of x, of x gathered per union expert, or of h). Each of the 8
+// consumer warps owns 4 weight rows: lane l holds 16 bytes of each and the
+// same columns of every token, so every weight byte is read from shared
+// memory once and used for all tokens of the group. Columns beyond K arrive
+// zero-filled from the TMA and contribute nothing.
 #include <math.h>
 
 #include "../../include/moe_warp.h"
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -40,7 +43,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowChunks = 32;
 constexpr int kChunkBytes = 512;
 constexpr int kMaxM = 8;
-constexpr int kStages = 6;
+constexpr int kStages = 8;
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
 constexpr int kMaxEntries = MOE_MAX_PAIRS + MOE_MAX_SHARED * (MOE_MAX_TOKENS / kMaxM);
 constexpr int kRowsPhase0 = 16;  // rows of I per phase-0 tile (gate and up)
@@ -48,8 +51,21 @@ constexpr int kRowsPhase1 = 32;  // rows of d per phase-1 tile
 
 struct Entry {
   int src;   // routed expert id (>= 0), or -(i+1) for shared expert i
-  int row0;  // first activation row
+  int row0;  // first activation row (in h)
   int m;     // tokens (1..kMaxM)
+  int arow;  // first row of the input box (x row, gathered-x row or h row)
+};
+
+// Tensor maps of one launch. w0/w1: routed experts' matrices ([E][rows][K]);
+// sw0/sw1: shared experts'. a1/a8: input rows of routed groups with a box of
+// 1 or 8 rows; s1/s8: input rows of shared-expert groups.
+struct alignas(64) Maps {
+  CUtensorMap w0, w1, sw0, sw1, a1, a8, s1, s8;
+};
+
+struct Params {
+  Maps maps;
+  ExpertArgs a;
 };
 
 template <int WB>
@@ -61,8 +77,7 @@ struct Layout {
   static constexpr int kStageBytes = kWBytes + kXBytes;
   static constexpr int kOffBar = kStages * kStageBytes;
   static constexpr int kOffPlan = kOffBar + 2 * kStages * 8;
-  static constexpr int kOffRowTok = kOffPlan + kMaxEntries * (int)sizeof(Entry);
-  static constexpr int kOffRowOut = kOffRowTok + kMaxRows * 4;
+  static constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
   static constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
   static constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
   static constexpr int kBytes = kOffMisc + 64 * 4;
@@ -97,18 +112,18 @@ MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
   return r;
 }
 
-// Builds the group table and the per-row maps (token, output slot row,
-// combine weight) in shared memory. Returns the number of groups.
-MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_tok, int* row_out,
-                       float* row_w, int* scratch) {
+// Builds the group table and the per-row output maps (slot row, combine
+// weight) in shared memory. Returns the number of groups.
+template <int PHASE>
+MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* row_w,
+                       int* scratch) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int P = a.n * a.k, S = a.k + a.s;
   int nr;
   if (a.engine == 0) {
     for (int p = tid; p < P; p += nt) {
       const int t = p / a.k, j = p - t * a.k;
-      plan[p] = Entry{a.topk_idx[p], p, 1};
-      row_tok[p] = t;
+      plan[p] = Entry{a.topk_idx[p], p, 1, PHASE == 0 ? t : p};
       row_out[p] = t * S + j;
       row_w[p] = a.topk_w[p];
     }
@@ -127,11 +142,12 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_tok, int* row_
     }
     const int nsub = (m + kMaxM - 1) / kMaxM;
     const int pos = block_exclusive_scan(nsub, scratch, &nr);
-    for (int q = 0; q < nsub; ++q)
-      plan[pos + q] = Entry{e, r0 + q * kMaxM, min(kMaxM, m - q * kMaxM)};
+    for (int q = 0; q < nsub; ++q) {
+      const int rr = r0 + q * kMaxM;
+      plan[pos + q] = Entry{e, rr, min(kMaxM, m - q * kMaxM), rr};
+    }
     for (int r = tid; r < P; r += nt) {
       const int t = a.pair_tok[r], j = a.pair_slot[r];
-      row_tok[r] = t;
       row_out[r] = t * S + j;
       row_w[r] = a.topk_w[t * a.k + j];
     }
@@ -139,11 +155,11 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_tok, int* row_
   const int per = (a.n + kMaxM - 1) / kMaxM;
   for (int q = tid; q < a.s * per; q += nt) {
     const int i = q / per, c = q - (q / per) * per;
-    plan[nr + q] = Entry{-(i + 1), P + i * a.n + c * kMaxM, min(kMaxM, a.n - c * kMaxM)};
+    const int rr = P + i * a.n + c * kMaxM;
+    plan[nr + q] = Entry{-(i + 1), rr, min(kMaxM, a.n - c * kMaxM), PHASE == 0 ? c * kMaxM : rr};
   }
   for (int r = tid; r < a.s * a.n; r += nt) {
     const int i = r / a.n, t = r - (r / a.n) * a.n;
-    row_tok[P + r] = t;
     row_out[P + r] = t * S + a.k + i;
     row_w[P + r] = 1.f;
   }
@@ -151,10 +167,10 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_tok, int* row_
 }
 
 template <int EPL>
-MOE_DEV void load_w(const char* p, float (&w)[EPL]);
+MOE_DEV void load_w(const unsigned char* p, float (&w)[EPL]);
 
 template <>
-MOE_DEV void load_w<8>(const char* p, float (&w)[8]) {  // 8 bf16
+MOE_DEV void load_w<8>(const unsigned char* p, float (&w)[8]) {  // 8 bf16
   const uint4 v = *reinterpret_cast<const uint4*>(p);
   w[0] = bf16lo(v.x); w[1] = bf16hi(v.x);
   w[2] = bf16lo(v.y); w[3] = bf16hi(v.y);
@@ -163,7 +179,7 @@ MOE_DEV void load_w<8>(const char* p, float (&w)[8]) {  // 8 bf16
 }
 
 template <>
-MOE_DEV void load_w<4>(const char* p, float (&w)[4]) {  // 4 fp32
+MOE_DEV void load_w<4>(const unsigned char* p, float (&w)[4]) {  // 4 fp32
   const float4 v = *reinterpret_cast<const float4*>(p);
   w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
 }
@@ -178,14 +194,14 @@ MOE_DEV void load_x(const float* p, float (&x)[EPL]) {
 }
 
 template <int WB, int PHASE>
-__global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const ExpertArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid_constant__ Params prm) {
   using L = Layout<WB>;
   constexpr int EPL = L::EPL, KS = L::KS;
+  const ExpertArgs& a = prm.a;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* empty = full + kStages;
   Entry* plan = reinterpret_cast<Entry*>(smem + L::kOffPlan);
-  int* row_tok = reinterpret_cast<int*>(smem + L::kOffRowTok);
   int* row_out = reinterpret_cast<int*>(smem + L::kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + L::kOffRowW);
   int* misc = reinterpret_cast<int*>(smem + L::kOffMisc);  // [0..31] scan scratch
@@ -200,7 +216,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const Expert
     *abort_flag = 0;
     fence_mbar_init();
   }
-  const int n_groups = build_plan(a, plan, row_tok, row_out, row_w, misc);
+  if (threadIdx.x == kConsumerWarps * 32) {
+    prefetch_tmap(&prm.maps.w0);
+    if (PHASE == 0) prefetch_tmap(&prm.maps.w1);
+    prefetch_tmap(&prm.maps.a1);
+    prefetch_tmap(&prm.maps.a8);
+  }
+  const int n_groups = build_plan<PHASE>(a, plan, row_out, row_w, misc);
   __syncthreads();
 
   const int K = PHASE == 0 ? a.d : a.I;         // reduction length
@@ -209,75 +231,63 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const Expert
   const int n_tiles = rows_out / tile_rows;
   const int n_jobs = n_groups * n_tiles;
   const int nks = (K + KS - 1) / KS;
-  const size_t mat = (size_t)a.I * a.d * WB;    // bytes of one expert matrix
 
   if (warp == kConsumerWarps) {
-    // ------------------------------------------------------- producer warp --
-    const uint64_t pol_w = l2_evict_first_policy();
-    const uint64_t pol_x = l2_evict_last_policy();
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued = 0;
-    bool ok = true;
-    for (int job = blockIdx.x; job < n_jobs && ok; job += gridDim.x) {
-      const Entry en = plan[job / n_tiles];
-      const int tile = job - (job / n_tiles) * n_tiles;
-      const char* w0;
-      const char* w1;
-      if (PHASE == 0) {
-        const char* g = en.src >= 0 ? (const char*)a.w_gate + (size_t)en.src * mat
-                                    : (const char*)a.ws_gate + (size_t)(-en.src - 1) * mat;
-        const char* u = en.src >= 0 ? (const char*)a.w_up + (size_t)en.src * mat
-                                    : (const char*)a.ws_up + (size_t)(-en.src - 1) * mat;
-        const size_t rowoff = (size_t)(tile * kRowsPhase0 + (lane & 15)) * K * WB;
-        w0 = (lane < 16 ? g : u) + rowoff;
-        w1 = nullptr;
-      } else {
-        const char* dn = en.src >= 0 ? (const char*)a.w_down + (size_t)en.src * mat
-                                     : (const char*)a.ws_down + (size_t)(-en.src - 1) * mat;
-        w0 = dn + (size_t)(tile * kRowsPhase1 + lane) * K * WB;
-        w1 = nullptr;
-      }
-      (void)w1;
-      const float* xrow = nullptr;
-      if (lane < en.m) {
-        xrow = PHASE == 0 ? a.x + (size_t)row_tok[en.row0 + lane] * a.d
-                          : a.h + (size_t)(en.row0 + lane) * a.I;
-      }
-      for (int ks = 0; ks < nks; ++ks) {
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        const int k0 = ks * KS;
-        const int klen = min(KS, K - k0);
-        if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x200 + PHASE)) {
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        unsigned char* st = smem + stage * L::kStageBytes;
-        const uint32_t wbytes = (uint32_t)klen * WB;
-        const uint32_t xbytes = (uint32_t)klen * 4;
-        if (lane == 0) mbar_arrive_expect_tx(&full[stage], kRowChunks * wbytes + en.m * xbytes);
-        __syncwarp();
-        bulk_g2s(st + lane * kChunkBytes, w0 + (size_t)k0 * WB, wbytes, &full[stage], pol_w);
-        if (lane < en.m)
-          bulk_g2s(st + L::kWBytes + lane * KS * 4, xrow + k0, xbytes, &full[stage], pol_x);
-        ++issued;
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+    // ------------------------------------------------------ producer thread --
+    if (lane == 0) {
+      const uint64_t pol_w = l2_evict_first_policy();
+      const uint64_t pol_x = l2_evict_last_policy();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int job = blockIdx.x; job < n_jobs && ok; job += gridDim.x) {
+        const Entry en = plan[job / n_tiles];
+        const int tile = job - (job / n_tiles) * n_tiles;
+        const bool shared_expert = en.src < 0;
+        const int ecoord = shared_expert ? -en.src - 1 : en.src;
+        const CUtensorMap* m0 = shared_expert ? &prm.maps.sw0 : &prm.maps.w0;
+        const CUtensorMap* m1 = shared_expert ? &prm.maps.sw1 : &prm.maps.w1;
+        const CUtensorMap* mx = shared_expert ? (en.m == 1 ? &prm.maps.s1 : &prm.maps.s8)
+                                              : (en.m == 1 ? &prm.maps.a1 : &prm.maps.a8);
+        const uint32_t xbytes = (en.m == 1 ? 1 : kMaxM) * KS * 4;
+        for (int ks = 0; ks < nks; ++ks) {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x200 + PHASE)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          unsigned char* st = smem + stage * L::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], kRowChunks * kChunkBytes + xbytes);
+          const int k0 = ks * KS;
+          if (PHASE == 0) {
+            tma_load_3d(st, m0, k0, tile * kRowsPhase0, ecoord, &full[stage], pol_w);
+            tma_load_3d(st + 16 * kChunkBytes, m1, k0, tile * kRowsPhase0, ecoord, &full[stage],
+                        pol_w);
+          } else {
+            tma_load_3d(st, m0, k0, tile * kRowsPhase1, ecoord, &full[stage], pol_w);
+          }
+          tma_load_2d(st + L::kWBytes, mx, k0, en.arow, &full[stage], pol_x);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    if (!ok && lane == 0) {
-      // Give copies already issued a bounded chance to land before the CTA
-      // exits, so that none writes into shared memory after it is released.
-      const int outstanding = min(issued, kStages);
-      for (int i = 1; i <= outstanding; ++i) {
-        const int idx = issued - i;
-        mbar_wait(&full[idx % kStages], (uint32_t)((idx / kStages) & 1), a.err, 0x210 + PHASE);
+      if (!ok) {
+        // Give copies already issued a bounded chance to land before the CTA
+        // exits, so that none writes into shared memory after it is released.
+        const int outstanding = min(issued, kStages);
+        for (int i = 1; i <= outstanding; ++i) {
+          const int idx = issued - i;
+          mbar_wait(&full[idx % kStages], (uint32_t)((idx / kStages) & 1), a.err,
+                    0x210 + PHASE);
+        }
       }
     }
     return;
@@ -300,28 +310,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const Expert
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t) acc[q][t] = 0.f;
     for (int ks = 0; ks < nks; ++ks) {
-      const int klen = min(KS, K - ks * KS);
       if (!mbar_wait(&full[stage], phase, a.err, 0x220 + PHASE)) {
         *abort_flag = 1;
         return;
       }
-      if (lane * EPL < klen) {
-        const unsigned char* st = smem + stage * L::kStageBytes;
-        const float* sx = reinterpret_cast<const float*>(st + L::kWBytes) + lane * EPL;
-        float wv[4][EPL];
+      const unsigned char* st = smem + stage * L::kStageBytes;
+      const float* sx = reinterpret_cast<const float*>(st + L::kWBytes) + lane * EPL;
+      float wv[4][EPL];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          load_w<EPL>(reinterpret_cast<const char*>(st) + chunk[q] * kChunkBytes + lane * 16, wv[q]);
+      for (int q = 0; q < 4; ++q) load_w<EPL>(st + chunk[q] * kChunkBytes + lane * 16, wv[q]);
 #pragma unroll
-        for (int t = 0; t < kMaxM; ++t) {
-          if (t < m) {
-            float xv[EPL];
-            load_x<EPL>(sx + t * KS, xv);
+      for (int t = 0; t < kMaxM; ++t) {
+        if (t < m) {
+          float xv[EPL];
+          load_x<EPL>(sx + t * KS, xv);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < 4; ++q)
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) acc[q][t] = fmaf(wv[q][e], xv[e], acc[q][t]);
-          }
+            for (int e = 0; e < EPL; ++e) acc[q][t] = fmaf(wv[q][e], xv[e], acc[q][t]);
         }
       }
       __syncwarp();
@@ -362,10 +368,38 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const Expert
   }
 }
 
+// xg[r][:] = x[pair_tok[r]][:] for the n·k pair rows (union order).
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(int d, const float* __restrict__ x, const int32_t* __restrict__ pair_tok,
+                       float* __restrict__ xg) {
+  const int r = blockIdx.x;
+  const float4* src = reinterpret_cast<const float4*>(x + (size_t)pair_tok[r] * d);
+  float4* dst = reinterpret_cast<float4*>(xg + (size_t)r * d);
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+// ------------------------------------------------------------------ host --
+bool weight_map(CUtensorMap* m, const void* p, int WB, int n_mat, int rows, int K, int box_rows) {
+  const int ks = WB == 2 ? 256 : 128;
+  const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n_mat};
+  const uint64_t strides[2] = {(uint64_t)K * WB, (uint64_t)rows * K * WB};
+  const uint32_t box[3] = {(uint32_t)ks, (uint32_t)box_rows, 1};
+  return make_tmap(m, p, WB == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                   3, dims, strides, box);
+}
+
+bool act_map(CUtensorMap* m, const float* p, int rows, int K, int ks, int box_rows) {
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)K * 4};
+  const uint32_t box[2] = {(uint32_t)ks, (uint32_t)box_rows};
+  return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dims, strides, box);
+}
+
 template <int WB, int PHASE>
 cudaError_t launch_one(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   auto kern = expert_stream_kernel<WB, PHASE>;
   constexpr int bytes = Layout<WB>::kBytes;
+  constexpr int ks = Layout<WB>::KS;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -374,7 +408,38 @@ cudaError_t launch_one(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  kern<<<num_sms, kThreads, bytes, stream>>>(a);
+  Params prm;
+  memset(&prm, 0, sizeof prm);
+  prm.a = a;
+  const int P = a.n * a.k;
+  const int hrows = P + a.s * a.n;
+  bool ok = true;
+  if (PHASE == 0) {
+    ok &= weight_map(&prm.maps.w0, a.w_gate, WB, a.E, a.I, a.d, kRowsPhase0);
+    ok &= weight_map(&prm.maps.w1, a.w_up, WB, a.E, a.I, a.d, kRowsPhase0);
+    if (a.s > 0) {
+      ok &= weight_map(&prm.maps.sw0, a.ws_gate, WB, a.s, a.I, a.d, kRowsPhase0);
+      ok &= weight_map(&prm.maps.sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
+    }
+    if (a.engine == 0) {
+      ok &= act_map(&prm.maps.a1, a.x, a.n, a.d, ks, 1);
+      ok &= act_map(&prm.maps.a8, a.x, a.n, a.d, ks, kMaxM);
+    } else {
+      ok &= act_map(&prm.maps.a1, a.xg, P, a.d, ks, 1);
+      ok &= act_map(&prm.maps.a8, a.xg, P, a.d, ks, kMaxM);
+    }
+    ok &= act_map(&prm.maps.s1, a.x, a.n, a.d, ks, 1);
+    ok &= act_map(&prm.maps.s8, a.x, a.n, a.d, ks, kMaxM);
+  } else {
+    ok &= weight_map(&prm.maps.w0, a.w_down, WB, a.E, a.d, a.I, kRowsPhase1);
+    if (a.s > 0) ok &= weight_map(&prm.maps.sw0, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
+    ok &= act_map(&prm.maps.a1, a.h, hrows, a.I, ks, 1);
+    ok &= act_map(&prm.maps.a8, a.h, hrows, a.I, ks, kMaxM);
+    prm.maps.s1 = prm.maps.a1;
+    prm.maps.s8 = prm.maps.a8;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  kern<<<num_sms, kThreads, bytes, stream>>>(prm);
   return cudaGetLastError();
 }
 
@@ -382,6 +447,11 @@ cudaError_t launch_one(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
 
 cudaError_t launch_expert_stream(const ExpertArgs& a, int phase, int num_sms,
                                  cudaStream_t stream) {
+  if (a.engine == 1 && phase == 0) {
+    gather_rows_kernel<<<a.n * a.k, 256, 0, stream>>>(a.d, a.x, a.pair_tok, a.xg);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (a.wdtype == 1)
     return phase == 0 ? launch_one<2, 0>(a, num_sms, stream) : launch_one<2, 1>(a, num_sms, stream);
   return phase == 0 ? launch_one<4, 0>(a, num_sms, stream) : launch_one<4, 1>(a, num_sms, stream);

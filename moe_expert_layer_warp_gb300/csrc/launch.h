@@ -38,7 +38,8 @@ struct ExpertArgs {
   const void* ws_gate;
   const void* ws_up;
   const void* ws_down;
-  float* h;
+  float* h;             // [n·k + s·n][I] fp32 scratch
+  float* xg;            // [n·k][d] fp32 scratch: x rows gathered in union order (dedup)
   float* y_slot;
   unsigned int* err;
 };

@@ -44,7 +44,8 @@ def test_workspace_bytes_closed_form(lib):
         n = max(w.pass_sizes) * w.streams
         got = api.moe_workspace_bytes(api.make_desc(sh), n)
         a256 = lambda v: (v + 255) // 256 * 256
-        want = a256(n * sh.n_experts * 4) + a256((n * sh.top_k + sh.n_shared * n) * sh.inter * 4)
+        want = (a256(n * sh.n_experts * 4) + a256((n * sh.top_k + sh.n_shared * n) * sh.inter * 4)
+                + a256(n * sh.top_k * sh.d * 4))
         assert got == want, w.name
 
 
