@@ -158,6 +158,31 @@ moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights*
 moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t n, float* y,
                        void* stream);
 
+/* Allocation-free variant of moe_verify_dedup (the sources have no
+ * counterpart: this exists for callers, not for the method). Some callers
+ * cannot allocate device memory: a plugin whose host framework owns all GPU
+ * memory and hands it only input and output buffers, or a latency-critical
+ * serving loop where a device allocation, with its implicit synchronisation,
+ * is not allowed after start-up. This entry point takes no workspace: its
+ * scratch is a fixed array of moe_noalloc_scratch_limit() bytes (8 MiB)
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Same arguments, outputs and numerics as moe_verify_dedup, minus the
+ *     workspace. A pass whose scratch (moe_workspace_bytes(desc, n)) exceeds
+ *     the limit returns MOE_EINVAL; moe_last_cuda_error_string() says why.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (the device must be current); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind (nothing in it needs to start at zero). Calls that overlap on
+ *     the GPU — on two streams, or from two threads — race on it.          */
+moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                                    const float* x, int32_t n, const moe_union* u,
+                                    const float* topk_w, float* y_slot, void* stream);
+
+/* Size in bytes of the static scratch array of moe_verify_dedup_noalloc. */
+size_t moe_noalloc_scratch_limit(void);
+
 /* Synchronises `stream`, then reads and clears the library's device error
  * word: MOE_ETIMEOUT if a bounded device-side wait expired, MOE_EDEVICE if a
  * kernel recorded a failed check, MOE_ECUDA if the stream reports an error,

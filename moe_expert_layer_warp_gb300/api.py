@@ -23,7 +23,7 @@ MOE_MAX_TOKENS, MOE_MAX_PAIRS, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_MAX_SHARED = 1
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_build_union", "moe_verify_perslot",
             "moe_verify_dedup", "moe_combine", "moe_last_device_error", "moe_status_str",
-            "moe_last_cuda_error_string")
+            "moe_last_cuda_error_string", "moe_verify_dedup_noalloc", "moe_noalloc_scratch_limit")
 
 
 class MoeError(RuntimeError):
@@ -73,13 +73,16 @@ def load(path: str = LIB_PATH):
     lib.moe_verify_perslot.argtypes = [D, W, P, I32, P, P, P, SZ, P, P]
     lib.moe_verify_dedup.argtypes = [D, W, P, I32, U, P, P, SZ, P, P]
     lib.moe_combine.argtypes = [D, P, I32, P, P]
+    lib.moe_verify_dedup_noalloc.argtypes = [D, W, P, I32, U, P, P, P]
+    lib.moe_noalloc_scratch_limit.argtypes = []
+    lib.moe_noalloc_scratch_limit.restype = SZ
     lib.moe_last_device_error.argtypes = [P]
     lib.moe_status_str.argtypes = [ctypes.c_int]
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_last_cuda_error_string.argtypes = []
     lib.moe_last_cuda_error_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_build_union", "moe_verify_perslot", "moe_verify_dedup",
-              "moe_combine", "moe_last_device_error"):
+              "moe_combine", "moe_last_device_error", "moe_verify_dedup_noalloc"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -151,6 +154,19 @@ def moe_verify_dedup(desc, weights: LayerWeightsC, x, n, u: UnionC, topk_w, work
                                    ctypes.byref(u), _ptr(topk_w), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _ptr(y_slot),
                                    _stream(stream)), "moe_verify_dedup")
+
+
+def moe_verify_dedup_noalloc(desc, weights: LayerWeightsC, x, n, u: UnionC, topk_w, y_slot,
+                             stream=None):
+    """moe_verify_dedup without a workspace: scratch lives in the library's
+    static device array (see include/moe_warp.h)."""
+    _check(load().moe_verify_dedup_noalloc(ctypes.byref(desc), ctypes.byref(weights), _ptr(x), n,
+                                           ctypes.byref(u), _ptr(topk_w), _ptr(y_slot),
+                                           _stream(stream)), "moe_verify_dedup_noalloc")
+
+
+def moe_noalloc_scratch_limit() -> int:
+    return int(load().moe_noalloc_scratch_limit())
 
 
 def moe_combine(desc, y_slot, n, y, stream=None):

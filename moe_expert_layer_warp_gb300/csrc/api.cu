@@ -233,6 +233,69 @@ moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights*
                     y_slot, stream);
 }
 
+// ------------------------------------------------ allocation-free variant --
+// Scratch for moe_verify_dedup_noalloc: a fixed array in the library's own
+// device memory, so that a caller who cannot allocate device memory still
+// gets the dedup engine. Every GPU that loads the library holds this array
+// until the process exits. Host code must not pass the symbol itself to a
+// kernel: on the host, g_noalloc_scratch names a host-side stand-in, not the
+// device array. Its device address is looked up per device below.
+}  // extern "C"
+
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocSlot {
+  bool ready = false;
+  void* ptr = nullptr;
+};
+NoAllocSlot g_noalloc[kMaxDevices];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+moe_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return MOE_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  NoAllocSlot& s = g_noalloc[dev];
+  if (!s.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(g_noalloc_scratch)");
+    s.ptr = p;
+    s.ready = true;
+  }
+  *out = s.ptr;
+  return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t moe_noalloc_scratch_limit(void) { return kNoAllocScratchBytes; }
+
+moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                                    const float* x, int32_t n, const moe_union* u,
+                                    const float* topk_w, float* y_slot, void* stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_n(desc, n));
+  const size_t need = ws_layout(desc, n).total;
+  if (need > kNoAllocScratchBytes) {
+    snprintf(g_last_cuda_err, sizeof g_last_cuda_err,
+             "moe_verify_dedup_noalloc: this pass needs %zu bytes of scratch, above the "
+             "static maximum of %zu bytes; use moe_verify_dedup with a workspace",
+             need, kNoAllocScratchBytes);
+    return MOE_EINVAL;
+  }
+  void* scratch = nullptr;
+  MOE_TRY(noalloc_scratch(&scratch));
+  return moe_verify_dedup(desc, weights, x, n, u, topk_w, scratch, kNoAllocScratchBytes, y_slot,
+                          stream);
+}
+
 moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t n, float* y,
                        void* stream) {
   MOE_TRY(check_desc(desc));

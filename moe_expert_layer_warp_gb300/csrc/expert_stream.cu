@@ -59,7 +59,7 @@ struct Entry {
 // Tensor maps of one launch. w0/w1: routed experts' matrices ([E][rows][K]);
 // sw0/sw1: shared experts'. a1/a8: input rows of routed groups with a box of
 // 1 or 8 rows; s1/s8: input rows of shared-expert groups.
-struct alignas(64) Maps {
+struct Maps {
   CUtensorMap w0, w1, sw0, sw1, a1, a8, s1, s8;
 };
 
