@@ -37,6 +37,7 @@ WORKLOAD = "deepseek-v2-lite-shaped MoE layer: d=2048, 64 routed experts top-6 +
 REPLICAS = 4
 N_PASSES_PER_N = 2        # distinct hidden-state passes per n, alternated across steps
 EXPERT_BYTES = 3 * 2048 * 1408 * 2
+SPIN_CYCLES = 200_000     # ~0.1 ms of device spin before a timed pass (host queues meanwhile)
 
 
 def parse_args():
@@ -166,6 +167,7 @@ def measure_breakdown(w, runners, xs, reps=3):
             R = runners[rep]
             x = xs[n][q]
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            torch.cuda._sleep(SPIN_CYCLES)   # device busy while the host queues the pass
             ev[0].record(stream)
             R.route(x, stream)
             R.build_union(n, stream)
@@ -486,6 +488,7 @@ def run_case(args):
     ts = []
     for _ in range(args.passes):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda._sleep(SPIN_CYCLES)      # device busy while the host queues the pass
         R.route(x, st)
         R.build_union(x.shape[0], st)
         e[0].record(st)

@@ -77,8 +77,9 @@ moe_status check_n(const moe_layer_desc* d, int32_t n) {
 //   logits  [n_max][E] fp32                 routing
 //   h       [n_max·k + s·n_max][I] fp32     SwiGLU activations
 //   xg      [n_max·k][d] fp32                x rows gathered in union order
+//   sync    [kEngineSyncInts] int32          engine job counter, group counts
 struct WsLayout {
-  size_t logits, h, xg, total;
+  size_t logits, h, xg, sync, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -92,6 +93,8 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   off = align256(off + ((size_t)n_max * d->top_k + (size_t)d->n_shared * n_max) * d->inter * 4);
   L.xg = off;
   off = align256(off + (size_t)n_max * d->top_k * d->d * 4);
+  L.sync = off;
+  off = align256(off + (size_t)moe::kEngineSyncInts * 4);
   L.total = off;
   return L;
 }
@@ -204,13 +207,12 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.ws_down = w->ws_down;
   a.h = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.h);
   a.xg = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.xg);
+  a.sync = reinterpret_cast<int*>(static_cast<char*>(workspace) + L.sync);
   a.y_slot = y_slot;
   a.err = di->err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = moe::launch_expert_stream(a, 0, di->num_sms, s);
-  if (e != cudaSuccess) return cuda_fail(e, "expert phase 0 launch");
-  e = moe::launch_expert_stream(a, 1, di->num_sms, s);
-  if (e != cudaSuccess) return cuda_fail(e, "expert phase 1 launch");
+  cudaError_t e = moe::launch_expert_engine(a, di->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert engine launch");
   return MOE_OK;
 }
 

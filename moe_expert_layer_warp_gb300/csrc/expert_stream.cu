@@ -48,19 +48,23 @@ constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
 constexpr int kMaxEntries = MOE_MAX_PAIRS + MOE_MAX_SHARED * (MOE_MAX_TOKENS / kMaxM);
 constexpr int kRowsPhase0 = 16;  // rows of I per phase-0 tile (gate and up)
 constexpr int kRowsPhase1 = 32;  // rows of d per phase-1 tile
+constexpr int kSyncInts = 1 + kMaxEntries;  // job counter + per-group phase-0 tile counts
+static_assert(kSyncInts == kEngineSyncInts, "engine scratch size");
 
 struct Entry {
   int src;   // routed expert id (>= 0), or -(i+1) for shared expert i
   int row0;  // first activation row (in h)
   int m;     // tokens (1..kMaxM)
-  int arow;  // first row of the input box (x row, gathered-x row or h row)
+  int arow;  // first row of the phase-0 input box (x row or gathered-x row); phase 1 reads h at row0
 };
 
-// Tensor maps of one launch. w0/w1: routed experts' matrices ([E][rows][K]);
-// sw0/sw1: shared experts'. a1/a8: input rows of routed groups with a box of
-// 1 or 8 rows; s1/s8: input rows of shared-expert groups.
+// Tensor maps of one launch. w0/w1/w2: routed experts' W_gate, W_up, W_down
+// ([E][rows][K]); sw0/sw1/sw2: the shared experts'. a1/a8: phase-0 input rows
+// of routed groups (x, or x gathered in union order) with a box of 1 or 8
+// rows; s1/s8: phase-0 input rows of shared-expert groups (x); h1/h8: phase-1
+// input rows (h).
 struct Maps {
-  CUtensorMap w0, w1, sw0, sw1, a1, a8, s1, s8;
+  CUtensorMap w0, w1, w2, sw0, sw1, sw2, a1, a8, s1, s8, h1, h8;
 };
 
 struct Params {
@@ -114,7 +118,6 @@ MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
 
 // Builds the group table and the per-row output maps (slot row, combine
 // weight) in shared memory. Returns the number of groups.
-template <int PHASE>
 MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* row_w,
                        int* scratch) {
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -123,7 +126,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   if (a.engine == 0) {
     for (int p = tid; p < P; p += nt) {
       const int t = p / a.k, j = p - t * a.k;
-      plan[p] = Entry{a.topk_idx[p], p, 1, PHASE == 0 ? t : p};
+      plan[p] = Entry{a.topk_idx[p], p, 1, t};
       row_out[p] = t * S + j;
       row_w[p] = a.topk_w[p];
     }
@@ -156,7 +159,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   for (int q = tid; q < a.s * per; q += nt) {
     const int i = q / per, c = q - (q / per) * per;
     const int rr = P + i * a.n + c * kMaxM;
-    plan[nr + q] = Entry{-(i + 1), rr, min(kMaxM, a.n - c * kMaxM), PHASE == 0 ? c * kMaxM : rr};
+    plan[nr + q] = Entry{-(i + 1), rr, min(kMaxM, a.n - c * kMaxM), c * kMaxM};
   }
   for (int r = tid; r < a.s * a.n; r += nt) {
     const int i = r / a.n, t = r - (r / a.n) * a.n;
@@ -193,8 +196,25 @@ MOE_DEV void load_x(const float* p, float (&x)[EPL]) {
   }
 }
 
-template <int WB, int PHASE>
-__global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid_constant__ Params prm) {
+MOE_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+MOE_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// One launch runs both phases. Jobs 0 .. J0-1 are phase-0 jobs (group-major),
+// jobs J0 .. J0+J1-1 phase-1 jobs (group-major); the producer thread of each
+// CTA takes the next job from a global counter, so every job taken belongs to
+// a resident CTA. A phase-1 job may load its group's h rows only once all
+// phase-0 tiles of that group are written: consumer warps count them in
+// done0[group]; the producer waits for the count (bounded) before issuing
+// the h box, while the job's weight boxes are already in flight.
+template <int WB>
+__global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid_constant__ Params prm) {
   using L = Layout<WB>;
   constexpr int EPL = L::EPL, KS = L::KS;
   const ExpertArgs& a = prm.a;
@@ -205,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
   int* row_out = reinterpret_cast<int*>(smem + L::kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + L::kOffRowW);
   int* misc = reinterpret_cast<int*>(smem + L::kOffMisc);  // [0..31] scan scratch
-  volatile int* abort_flag = misc + 40;
+  volatile int* stage_job = misc + 32;                     // [kStages]
+  volatile int* abort_flag = misc + 48;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -218,19 +239,19 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
   }
   if (threadIdx.x == kConsumerWarps * 32) {
     prefetch_tmap(&prm.maps.w0);
-    if (PHASE == 0) prefetch_tmap(&prm.maps.w1);
+    prefetch_tmap(&prm.maps.w1);
+    prefetch_tmap(&prm.maps.w2);
     prefetch_tmap(&prm.maps.a1);
-    prefetch_tmap(&prm.maps.a8);
   }
-  const int n_groups = build_plan<PHASE>(a, plan, row_out, row_w, misc);
+  const int n_groups = build_plan(a, plan, row_out, row_w, misc);
   __syncthreads();
 
-  const int K = PHASE == 0 ? a.d : a.I;         // reduction length
-  const int rows_out = PHASE == 0 ? a.I : a.d;  // output rows per expert
-  const int tile_rows = PHASE == 0 ? kRowsPhase0 : kRowsPhase1;
-  const int n_tiles = rows_out / tile_rows;
-  const int n_jobs = n_groups * n_tiles;
-  const int nks = (K + KS - 1) / KS;
+  const int T0 = a.I / kRowsPhase0, T1 = a.d / kRowsPhase1;
+  const int J0 = n_groups * T0, J = J0 + n_groups * T1;
+  const int nks0 = (a.d + KS - 1) / KS, nks1 = (a.I + KS - 1) / KS;
+  int* job_counter = a.sync;
+  int* done0 = a.sync + 1;
+  const int done_target = T0 * kConsumerWarps;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------ producer thread --
@@ -241,37 +262,78 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int job = blockIdx.x; job < n_jobs && ok; job += gridDim.x) {
-        const Entry en = plan[job / n_tiles];
-        const int tile = job - (job / n_tiles) * n_tiles;
+      while (ok) {
+        int job = atomicAdd(job_counter, 1);
+        if (job >= J) {
+          // end marker for the consumers
+          if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x201)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          stage_job[stage] = -1;
+          mbar_arrive(&full[stage]);
+          break;
+        }
+        const int ph = job < J0 ? 0 : 1;
+        const int jj = ph == 0 ? job : job - J0;
+        const int T = ph == 0 ? T0 : T1;
+        const int g = jj / T, tile = jj - g * T;
+        const Entry en = plan[g];
         const bool shared_expert = en.src < 0;
         const int ecoord = shared_expert ? -en.src - 1 : en.src;
-        const CUtensorMap* m0 = shared_expert ? &prm.maps.sw0 : &prm.maps.w0;
-        const CUtensorMap* m1 = shared_expert ? &prm.maps.sw1 : &prm.maps.w1;
-        const CUtensorMap* mx = shared_expert ? (en.m == 1 ? &prm.maps.s1 : &prm.maps.s8)
-                                              : (en.m == 1 ? &prm.maps.a1 : &prm.maps.a8);
+        const CUtensorMap *m0, *m1 = nullptr, *mx;
+        if (ph == 0) {
+          m0 = shared_expert ? &prm.maps.sw0 : &prm.maps.w0;
+          m1 = shared_expert ? &prm.maps.sw1 : &prm.maps.w1;
+          mx = shared_expert ? (en.m == 1 ? &prm.maps.s1 : &prm.maps.s8)
+                             : (en.m == 1 ? &prm.maps.a1 : &prm.maps.a8);
+        } else {
+          m0 = shared_expert ? &prm.maps.sw2 : &prm.maps.w2;
+          mx = en.m == 1 ? &prm.maps.h1 : &prm.maps.h8;
+        }
+        const int arow = ph == 0 ? en.arow : en.row0;
         const uint32_t xbytes = (en.m == 1 ? 1 : kMaxM) * KS * 4;
+        const int nks = ph == 0 ? nks0 : nks1;
         for (int ks = 0; ks < nks; ++ks) {
           if (*abort_flag) {
             ok = false;
             break;
           }
-          if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x200 + PHASE)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x200)) {
             *abort_flag = 1;
             ok = false;
             break;
           }
           unsigned char* st = smem + stage * L::kStageBytes;
+          if (ks == 0) stage_job[stage] = job;
           mbar_arrive_expect_tx(&full[stage], kRowChunks * kChunkBytes + xbytes);
           const int k0 = ks * KS;
-          if (PHASE == 0) {
+          if (ph == 0) {
             tma_load_3d(st, m0, k0, tile * kRowsPhase0, ecoord, &full[stage], pol_w);
             tma_load_3d(st + 16 * kChunkBytes, m1, k0, tile * kRowsPhase0, ecoord, &full[stage],
                         pol_w);
           } else {
             tma_load_3d(st, m0, k0, tile * kRowsPhase1, ecoord, &full[stage], pol_w);
+            if (ks == 0) {
+              // the group's h rows must be complete before they are read
+              const unsigned long long t0 = global_ns();
+              unsigned int it = 0;
+              while (ld_acquire(done0 + g) < done_target) {
+                if ((++it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+                  report_error(a.err, ERR_TIMEOUT, 0x240);
+                  *abort_flag = 1;
+                  ok = false;
+                  break;
+                }
+              }
+              fence_proxy_async_global();
+            }
           }
-          tma_load_2d(st + L::kWBytes, mx, k0, en.arow, &full[stage], pol_x);
+          // On a failed dependency wait the box is still issued (it reads
+          // valid memory) so that the stage completes and nothing is left
+          // in flight; the abort flag stops everything after it.
+          tma_load_2d(st + L::kWBytes, mx, k0, arow, &full[stage], pol_x);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -285,8 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
         const int outstanding = min(issued, kStages);
         for (int i = 1; i <= outstanding; ++i) {
           const int idx = issued - i;
-          mbar_wait(&full[idx % kStages], (uint32_t)((idx / kStages) & 1), a.err,
-                    0x210 + PHASE);
+          mbar_wait(&full[idx % kStages], (uint32_t)((idx / kStages) & 1), a.err, 0x210);
         }
       }
     }
@@ -294,23 +355,34 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
   }
 
   // --------------------------------------------------------- consumer warps --
-  int chunk[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    chunk[q] = PHASE == 0 ? (q < 2 ? 2 * warp + q : 16 + 2 * warp + (q - 2)) : 4 * warp + q;
   int stage = 0;
   uint32_t phase = 0;
-  for (int job = blockIdx.x; job < n_jobs; job += gridDim.x) {
-    const Entry en = plan[job / n_tiles];
-    const int tile = job - (job / n_tiles) * n_tiles;
+  for (;;) {
+    if (!mbar_wait(&full[stage], phase, a.err, 0x220)) {
+      *abort_flag = 1;
+      return;
+    }
+    if (*abort_flag) return;
+    const int job = stage_job[stage];
+    if (job < 0) break;
+    const int ph = job < J0 ? 0 : 1;
+    const int jj = ph == 0 ? job : job - J0;
+    const int T = ph == 0 ? T0 : T1;
+    const int g = jj / T, tile = jj - g * T;
+    const Entry en = plan[g];
     const int m = en.m;
+    const int nks = ph == 0 ? nks0 : nks1;
+    int chunk[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      chunk[q] = ph == 0 ? (q < 2 ? 2 * warp + q : 16 + 2 * warp + (q - 2)) : 4 * warp + q;
     float acc[4][kMaxM];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t) acc[q][t] = 0.f;
     for (int ks = 0; ks < nks; ++ks) {
-      if (!mbar_wait(&full[stage], phase, a.err, 0x220 + PHASE)) {
+      if (ks > 0 && !mbar_wait(&full[stage], phase, a.err, 0x221)) {
         *abort_flag = 1;
         return;
       }
@@ -343,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
       for (int t = 0; t < kMaxM; ++t)
         if (t < m) acc[q][t] = warp_sum(acc[q][t]);
     if (lane == 0) {
-      if (PHASE == 0) {
+      if (ph == 0) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int row = tile * kRowsPhase0 + 2 * warp + q;
@@ -351,6 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_stream_kernel(const __grid
           for (int t = 0; t < kMaxM; ++t)
             if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(acc[q][t]) * acc[q + 2][t];
         }
+        // publish: these h values are read by TMA (async proxy) in other CTAs
+        fence_proxy_async_global();
+        __threadfence();
+        atomicAdd(done0 + g, 1);
       } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -395,9 +471,9 @@ bool act_map(CUtensorMap* m, const float* p, int rows, int K, int ks, int box_ro
   return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dims, strides, box);
 }
 
-template <int WB, int PHASE>
-cudaError_t launch_one(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
-  auto kern = expert_stream_kernel<WB, PHASE>;
+template <int WB>
+cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
+  auto kern = expert_engine_kernel<WB>;
   constexpr int bytes = Layout<WB>::kBytes;
   constexpr int ks = Layout<WB>::KS;
   static int configured_device = -1;
@@ -414,47 +490,38 @@ cudaError_t launch_one(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   const int P = a.n * a.k;
   const int hrows = P + a.s * a.n;
   bool ok = true;
-  if (PHASE == 0) {
-    ok &= weight_map(&prm.maps.w0, a.w_gate, WB, a.E, a.I, a.d, kRowsPhase0);
-    ok &= weight_map(&prm.maps.w1, a.w_up, WB, a.E, a.I, a.d, kRowsPhase0);
-    if (a.s > 0) {
-      ok &= weight_map(&prm.maps.sw0, a.ws_gate, WB, a.s, a.I, a.d, kRowsPhase0);
-      ok &= weight_map(&prm.maps.sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
-    }
-    if (a.engine == 0) {
-      ok &= act_map(&prm.maps.a1, a.x, a.n, a.d, ks, 1);
-      ok &= act_map(&prm.maps.a8, a.x, a.n, a.d, ks, kMaxM);
-    } else {
-      ok &= act_map(&prm.maps.a1, a.xg, P, a.d, ks, 1);
-      ok &= act_map(&prm.maps.a8, a.xg, P, a.d, ks, kMaxM);
-    }
-    ok &= act_map(&prm.maps.s1, a.x, a.n, a.d, ks, 1);
-    ok &= act_map(&prm.maps.s8, a.x, a.n, a.d, ks, kMaxM);
-  } else {
-    ok &= weight_map(&prm.maps.w0, a.w_down, WB, a.E, a.d, a.I, kRowsPhase1);
-    if (a.s > 0) ok &= weight_map(&prm.maps.sw0, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
-    ok &= act_map(&prm.maps.a1, a.h, hrows, a.I, ks, 1);
-    ok &= act_map(&prm.maps.a8, a.h, hrows, a.I, ks, kMaxM);
-    prm.maps.s1 = prm.maps.a1;
-    prm.maps.s8 = prm.maps.a8;
+  ok &= weight_map(&prm.maps.w0, a.w_gate, WB, a.E, a.I, a.d, kRowsPhase0);
+  ok &= weight_map(&prm.maps.w1, a.w_up, WB, a.E, a.I, a.d, kRowsPhase0);
+  ok &= weight_map(&prm.maps.w2, a.w_down, WB, a.E, a.d, a.I, kRowsPhase1);
+  if (a.s > 0) {
+    ok &= weight_map(&prm.maps.sw0, a.ws_gate, WB, a.s, a.I, a.d, kRowsPhase0);
+    ok &= weight_map(&prm.maps.sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
+    ok &= weight_map(&prm.maps.sw2, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
   }
+  const float* xa = a.engine == 0 ? a.x : a.xg;
+  const int xa_rows = a.engine == 0 ? a.n : P;
+  ok &= act_map(&prm.maps.a1, xa, xa_rows, a.d, ks, 1);
+  ok &= act_map(&prm.maps.a8, xa, xa_rows, a.d, ks, kMaxM);
+  ok &= act_map(&prm.maps.s1, a.x, a.n, a.d, ks, 1);
+  ok &= act_map(&prm.maps.s8, a.x, a.n, a.d, ks, kMaxM);
+  ok &= act_map(&prm.maps.h1, a.h, hrows, a.I, ks, 1);
+  ok &= act_map(&prm.maps.h8, a.h, hrows, a.I, ks, kMaxM);
   if (!ok) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(a.sync, 0, kSyncInts * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
   kern<<<num_sms, kThreads, bytes, stream>>>(prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_expert_stream(const ExpertArgs& a, int phase, int num_sms,
-                                 cudaStream_t stream) {
-  if (a.engine == 1 && phase == 0) {
+cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
+  if (a.engine == 1) {
     gather_rows_kernel<<<a.n * a.k, 256, 0, stream>>>(a.d, a.x, a.pair_tok, a.xg);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  if (a.wdtype == 1)
-    return phase == 0 ? launch_one<2, 0>(a, num_sms, stream) : launch_one<2, 1>(a, num_sms, stream);
-  return phase == 0 ? launch_one<4, 0>(a, num_sms, stream) : launch_one<4, 1>(a, num_sms, stream);
+  return a.wdtype == 1 ? launch_engine<2>(a, num_sms, stream) : launch_engine<4>(a, num_sms, stream);
 }
 
 }  // namespace moe

@@ -40,15 +40,18 @@ struct ExpertArgs {
   const void* ws_down;
   float* h;             // [n·k + s·n][I] fp32 scratch
   float* xg;            // [n·k][d] fp32 scratch: x rows gathered in union order (dedup)
+  int* sync;            // [kSyncInts] scratch: job counter and per-group counts (zeroed per call)
   float* y_slot;
   unsigned int* err;
 };
 
-// Expert FFN over the pass on CUDA cores, weights streamed through a ring of
-// shared-memory stages filled by the TMA engine. phase 0: h = silu(Wg x)⊙(Wu x);
-// phase 1: y_slot = w · (W_down h).
-cudaError_t launch_expert_stream(const ExpertArgs& a, int phase, int num_sms,
-                                 cudaStream_t stream);
+// Expert FFNs over the pass on CUDA cores in one persistent launch, weights
+// streamed through a ring of shared-memory stages filled by the TMA engine:
+// h = silu(Wg x)⊙(Wu x), then y_slot = w · (W_down h).
+cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream);
+
+// Ints of scratch the engine's job counter and group counts occupy.
+constexpr int kEngineSyncInts = 1 + 512 + 4 * 16;
 
 // y[t] = Σ_j y_slot[t][j] over the k+s slots, in slot order.
 cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,
