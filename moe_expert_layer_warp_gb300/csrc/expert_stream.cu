@@ -38,7 +38,7 @@
 namespace moe {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowChunks = 32;
 constexpr int kChunkBytes = 512;
@@ -169,32 +169,49 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   return nr + a.s * per;
 }
 
-template <int EPL>
-MOE_DEV void load_w(const unsigned char* p, float (&w)[EPL]);
+// Columns a lane owns inside a stage, chosen so that its shared-memory reads
+// are conflict-free: bf16 stages (256 columns) give lane l the runs
+// [4l, 4l+4) and [128+4l, 128+4l+4) — two 8-byte weight reads and two 16-byte
+// input reads; fp32 stages (128 columns) give it [4l, 4l+4). Values are
+// handled as float2 pairs for the packed fp32x2 FMA.
+template <int WB>
+struct LaneMap;
 
 template <>
-MOE_DEV void load_w<8>(const unsigned char* p, float (&w)[8]) {  // 8 bf16
-  const uint4 v = *reinterpret_cast<const uint4*>(p);
-  w[0] = bf16lo(v.x); w[1] = bf16hi(v.x);
-  w[2] = bf16lo(v.y); w[3] = bf16hi(v.y);
-  w[4] = bf16lo(v.z); w[5] = bf16hi(v.z);
-  w[6] = bf16lo(v.w); w[7] = bf16hi(v.w);
-}
-
-template <>
-MOE_DEV void load_w<4>(const unsigned char* p, float (&w)[4]) {  // 4 fp32
-  const float4 v = *reinterpret_cast<const float4*>(p);
-  w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-}
-
-template <int EPL>
-MOE_DEV void load_x(const float* p, float (&x)[EPL]) {
-#pragma unroll
-  for (int i = 0; i < EPL; i += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(p + i);
-    x[i] = v.x; x[i + 1] = v.y; x[i + 2] = v.z; x[i + 3] = v.w;
+struct LaneMap<2> {
+  static constexpr int NP = 4;  // float2 pairs per lane per row
+  static MOE_DEV void load_w(const unsigned char* row, int lane, float2 (&w)[NP]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(row + lane * 8);
+    const uint2 v = *reinterpret_cast<const uint2*>(row + 256 + lane * 8);
+    w[0] = make_float2(bf16lo(u.x), bf16hi(u.x));
+    w[1] = make_float2(bf16lo(u.y), bf16hi(u.y));
+    w[2] = make_float2(bf16lo(v.x), bf16hi(v.x));
+    w[3] = make_float2(bf16lo(v.y), bf16hi(v.y));
   }
-}
+  static MOE_DEV void load_x(const float* row, int lane, float2 (&x)[NP]) {
+    const float4 u = *reinterpret_cast<const float4*>(row + lane * 4);
+    const float4 v = *reinterpret_cast<const float4*>(row + 128 + lane * 4);
+    x[0] = make_float2(u.x, u.y);
+    x[1] = make_float2(u.z, u.w);
+    x[2] = make_float2(v.x, v.y);
+    x[3] = make_float2(v.z, v.w);
+  }
+};
+
+template <>
+struct LaneMap<4> {
+  static constexpr int NP = 2;
+  static MOE_DEV void load_w(const unsigned char* row, int lane, float2 (&w)[NP]) {
+    const float4 u = *reinterpret_cast<const float4*>(row + lane * 16);
+    w[0] = make_float2(u.x, u.y);
+    w[1] = make_float2(u.z, u.w);
+  }
+  static MOE_DEV void load_x(const float* row, int lane, float2 (&x)[NP]) {
+    const float4 u = *reinterpret_cast<const float4*>(row + lane * 4);
+    x[0] = make_float2(u.x, u.y);
+    x[1] = make_float2(u.z, u.w);
+  }
+};
 
 MOE_DEV int ld_acquire(const int* p) {
   int v;
@@ -216,7 +233,7 @@ MOE_DEV void fence_proxy_async_global() {
 template <int WB>
 __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid_constant__ Params prm) {
   using L = Layout<WB>;
-  constexpr int EPL = L::EPL, KS = L::KS;
+  constexpr int KS = L::KS;
   const ExpertArgs& a = prm.a;
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
@@ -355,6 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
 
   // --------------------------------------------------------- consumer warps --
+  // Warp w owns two weight rows of every stage: in phase 0 gate row w and up
+  // row w of the 16-row tile (so h for row w is finished inside the warp), in
+  // phase 1 rows 2w and 2w+1 of the 32-row tile.
+  using LM = LaneMap<WB>;
+  constexpr int NP = LM::NP;
   int stage = 0;
   uint32_t phase = 0;
   for (;;) {
@@ -372,34 +394,33 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     const Entry en = plan[g];
     const int m = en.m;
     const int nks = ph == 0 ? nks0 : nks1;
-    int chunk[4];
+    const int c0 = ph == 0 ? warp : 2 * warp;
+    const int c1 = ph == 0 ? 16 + warp : 2 * warp + 1;
+    float2 acc[2][kMaxM];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      chunk[q] = ph == 0 ? (q < 2 ? 2 * warp + q : 16 + 2 * warp + (q - 2)) : 4 * warp + q;
-    float acc[4][kMaxM];
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int t = 0; t < kMaxM; ++t) acc[q][t] = 0.f;
+      for (int t = 0; t < kMaxM; ++t) acc[q][t] = make_float2(0.f, 0.f);
     for (int ks = 0; ks < nks; ++ks) {
       if (ks > 0 && !mbar_wait(&full[stage], phase, a.err, 0x221)) {
         *abort_flag = 1;
         return;
       }
       const unsigned char* st = smem + stage * L::kStageBytes;
-      const float* sx = reinterpret_cast<const float*>(st + L::kWBytes) + lane * EPL;
-      float wv[4][EPL];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) load_w<EPL>(st + chunk[q] * kChunkBytes + lane * 16, wv[q]);
+      const float* sx = reinterpret_cast<const float*>(st + L::kWBytes);
+      float2 w0[NP], w1[NP];
+      LM::load_w(st + c0 * kChunkBytes, lane, w0);
+      LM::load_w(st + c1 * kChunkBytes, lane, w1);
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t) {
         if (t < m) {
-          float xv[EPL];
-          load_x<EPL>(sx + t * KS, xv);
+          float2 xv[NP];
+          LM::load_x(sx + t * KS, lane, xv);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[q][t] = fmaf(wv[q][e], xv[e], acc[q][t]);
+          for (int p = 0; p < NP; ++p) {
+            acc[0][t] = __ffma2_rn(w0[p], xv[p], acc[0][t]);
+            acc[1][t] = __ffma2_rn(w1[p], xv[p], acc[1][t]);
+          }
         }
       }
       __syncwarp();
@@ -409,33 +430,31 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         phase ^= 1u;
       }
     }
+    float r[2][kMaxM];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t)
-        if (t < m) acc[q][t] = warp_sum(acc[q][t]);
+        r[q][t] = (t < m) ? warp_sum(acc[q][t].x + acc[q][t].y) : 0.f;
     if (lane == 0) {
       if (ph == 0) {
+        const int row = tile * kRowsPhase0 + warp;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int row = tile * kRowsPhase0 + 2 * warp + q;
-#pragma unroll
-          for (int t = 0; t < kMaxM; ++t)
-            if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(acc[q][t]) * acc[q + 2][t];
-        }
+        for (int t = 0; t < kMaxM; ++t)
+          if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(r[0][t]) * r[1][t];
         // publish: these h values are read by TMA (async proxy) in other CTAs
         fence_proxy_async_global();
         __threadfence();
         atomicAdd(done0 + g, 1);
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int row = tile * kRowsPhase1 + 4 * warp + q;
+        for (int q = 0; q < 2; ++q) {
+          const int row = tile * kRowsPhase1 + 2 * warp + q;
 #pragma unroll
           for (int t = 0; t < kMaxM; ++t) {
             if (t < m) {
-              const int r = en.row0 + t;
-              a.y_slot[(size_t)row_out[r] * a.d + row] = row_w[r] * acc[q][t];
+              const int rr = en.row0 + t;
+              a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * r[q][t];
             }
           }
         }
