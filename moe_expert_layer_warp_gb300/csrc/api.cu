@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/moe_warp.h"
+#include "moe_warp.h"
 #include "launch.h"
 
 namespace {

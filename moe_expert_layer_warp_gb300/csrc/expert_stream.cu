@@ -30,7 +30,7 @@
 // zero-filled from the TMA and contribute nothing.
 #include <math.h>
 
-#include "../../include/moe_warp.h"
+#include "moe_warp.h"
 #include "common.cuh"
 #include "launch.h"
 #include "tmap.h"
@@ -219,6 +219,10 @@ MOE_DEV int ld_acquire(const int* p) {
   return v;
 }
 
+MOE_DEV void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 MOE_DEV void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -262,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
   const int n_groups = build_plan(a, plan, row_out, row_w, misc);
   __syncthreads();
+  // the prep kernel (counters zeroed, rows gathered) must be complete
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int T0 = a.I / kRowsPhase0, T1 = a.d / kRowsPhase1;
   const int J0 = n_groups * T0, J = J0 + n_groups * T1;
@@ -442,10 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
 #pragma unroll
         for (int t = 0; t < kMaxM; ++t)
           if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(r[0][t]) * r[1][t];
-        // publish: these h values are read by TMA (async proxy) in other CTAs
-        fence_proxy_async_global();
-        __threadfence();
-        atomicAdd(done0 + g, 1);
+        // publish: a release reduction orders the h stores above before the
+        // count; the reader acquires the count and fences the async proxy
+        // before its TMA reads h.
+        red_release_add(done0 + g, 1);
       } else {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -463,14 +469,24 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
 }
 
-// xg[r][:] = x[pair_tok[r]][:] for the n·k pair rows (union order).
+// Runs right before the engine kernel: zeroes the engine's job counter and
+// group counts and, for dedup, gathers xg[r][:] = x[pair_tok[r]][:] over the
+// n·k pair rows (union order). It lets the engine launch at once
+// (programmatic dependent launch); the engine waits for it before it touches
+// either.
 __global__ void __launch_bounds__(256)
-    gather_rows_kernel(int d, const float* __restrict__ x, const int32_t* __restrict__ pair_tok,
-                       float* __restrict__ xg) {
+    engine_prep_kernel(int d, int gather_rows, const float* __restrict__ x,
+                       const int32_t* __restrict__ pair_tok, float* __restrict__ xg,
+                       int* __restrict__ sync, int sync_ints) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < sync_ints; i += blockDim.x) sync[i] = 0;
   const int r = blockIdx.x;
-  const float4* src = reinterpret_cast<const float4*>(x + (size_t)pair_tok[r] * d);
-  float4* dst = reinterpret_cast<float4*>(xg + (size_t)r * d);
-  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) dst[i] = __ldg(src + i);
+  if (r < gather_rows) {
+    const float4* src = reinterpret_cast<const float4*>(x + (size_t)pair_tok[r] * d);
+    float4* dst = reinterpret_cast<float4*>(xg + (size_t)r * d);
+    for (int i = threadIdx.x; i < d / 4; i += blockDim.x) dst[i] = __ldg(src + i);
+  }
 }
 
 // ------------------------------------------------------------------ host --
@@ -526,20 +542,30 @@ cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream)
   ok &= act_map(&prm.maps.h1, a.h, hrows, a.I, ks, 1);
   ok &= act_map(&prm.maps.h8, a.h, hrows, a.I, ks, kMaxM);
   if (!ok) return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(a.sync, 0, kSyncInts * sizeof(int), stream);
+  const int gather = a.engine == 1 ? P : 0;
+  engine_prep_kernel<<<max(gather, 1), 256, 0, stream>>>(a.d, gather, a.x, a.pair_tok, a.xg,
+                                                          a.sync, kSyncInts);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kThreads, bytes, stream>>>(prm);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the engine's prologue overlaps the prep
+  // kernel; its griddepcontrol.wait orders every use of the prep's outputs.
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 }  // namespace
 
 cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
-  if (a.engine == 1) {
-    gather_rows_kernel<<<a.n * a.k, 256, 0, stream>>>(a.d, a.x, a.pair_tok, a.xg);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   return a.wdtype == 1 ? launch_engine<2>(a, num_sms, stream) : launch_engine<4>(a, num_sms, stream);
 }
 

@@ -9,7 +9,7 @@
 // selected experts is what a deduplicating engine reads once per pass).
 #include <math.h>
 
-#include "../../include/moe_warp.h"
+#include "moe_warp.h"
 #include "common.cuh"
 #include "launch.h"
 
@@ -17,12 +17,14 @@ namespace moe {
 namespace {
 
 // ------------------------------------------------------------------ gate --
-// One warp per expert row of W_g, kGateTokens tokens per CTA. The dot is
-// accumulated with error-free transformations (TwoProd by FMA, Knuth's
-// TwoSum) — the compensated dot of Ogita, Rump and Oishi (2005) — so the
-// returned fp32 logit is the exact dot rounded once, up to a term of order
-// u²·Σ|x_i·w_i|. That keeps the top-k selection identical to an exact
-// computation except at near-ties far below fp32 resolution.
+// One CTA per (expert, tile of kGateTokens tokens); its 8 warps split d into
+// 8 contiguous ranges. The dot is accumulated with error-free
+// transformations (TwoProd by FMA, Knuth's TwoSum) — the compensated dot of
+// Ogita, Rump and Oishi (2005) — so the returned fp32 logit is the exact dot
+// rounded once, up to a term of order u²·Σ|x_i·w_i|. That keeps the top-k
+// selection identical to an exact computation except at near-ties far below
+// fp32 resolution. Partial (sum, compensation) pairs are combined in a fixed
+// order, so the result does not depend on scheduling.
 constexpr int kGateWarps = 8;
 constexpr int kGateTokens = 8;
 
@@ -40,26 +42,35 @@ MOE_DEV void dot2_step(float a, float b, float& s, float& c) {
   c = __fadd_rn(c, __fadd_rn(ep, es));
 }
 
+// (s, c) += (s2, c2) with the sums combined exactly
+MOE_DEV void pair_add(float& s, float& c, float s2, float c2) {
+  float sn, en;
+  two_sum(s, s2, sn, en);
+  c = __fadd_rn(__fadd_rn(c, c2), en);
+  s = sn;
+}
+
 __global__ void __launch_bounds__(kGateWarps * 32)
     gate_logits_kernel(int d, int E, int n, const float* __restrict__ x,
                        const float* __restrict__ wg, float* __restrict__ logits) {
+  __shared__ float part[kGateWarps][kGateTokens][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kGateWarps + warp;
+  const int e = blockIdx.x;
   const int t0 = blockIdx.y * kGateTokens;
-  if (e >= E) return;
   const int nt = min(kGateTokens, n - t0);
+  const int chunk4 = (d / kGateWarps) >> 2;  // float4s per warp (d is a multiple of 64)
+  const int base4 = warp * chunk4;
   float s[kGateTokens], c[kGateTokens];
 #pragma unroll
   for (int t = 0; t < kGateTokens; ++t) s[t] = c[t] = 0.f;
-  const float4* wrow = reinterpret_cast<const float4*>(wg + (size_t)e * d);
-  const int d4 = d >> 2;
-#pragma unroll 2
-  for (int i = lane; i < d4; i += 32) {
+  const float4* wrow = reinterpret_cast<const float4*>(wg + (size_t)e * d) + base4;
+  for (int i = lane; i < chunk4; i += 32) {
     const float4 w = __ldg(wrow + i);
 #pragma unroll
     for (int t = 0; t < kGateTokens; ++t) {
       if (t < nt) {
-        const float4 xv = __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + t) * d) + i);
+        const float4 xv =
+            __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + t) * d) + base4 + i);
         dot2_step(w.x, xv.x, s[t], c[t]);
         dot2_step(w.y, xv.y, s[t], c[t]);
         dot2_step(w.z, xv.z, s[t], c[t]);
@@ -67,24 +78,30 @@ __global__ void __launch_bounds__(kGateWarps * 32)
       }
     }
   }
-  // Butterfly combine of the (sum, compensation) pairs; TwoSum is exact and
-  // commutative, so every lane ends with the same pair.
+  // Butterfly combine inside the warp; TwoSum is exact and commutative, so
+  // every lane ends with the same pair.
 #pragma unroll
   for (int t = 0; t < kGateTokens; ++t) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float so = __shfl_xor_sync(0xffffffffu, s[t], o);
       const float co = __shfl_xor_sync(0xffffffffu, c[t], o);
-      float sn, en;
-      two_sum(s[t], so, sn, en);
-      c[t] = __fadd_rn(__fadd_rn(c[t], co), en);
-      s[t] = sn;
+      pair_add(s[t], c[t], so, co);
     }
   }
   if (lane == 0) {
 #pragma unroll
-    for (int t = 0; t < kGateTokens; ++t)
-      if (t < nt) logits[(size_t)(t0 + t) * E + e] = __fadd_rn(s[t], c[t]);
+    for (int t = 0; t < kGateTokens; ++t) {
+      part[warp][t][0] = s[t];
+      part[warp][t][1] = c[t];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    const int t = threadIdx.x;
+    float ss = part[0][t][0], cc = part[0][t][1];
+    for (int w = 1; w < kGateWarps; ++w) pair_add(ss, cc, part[w][t][0], part[w][t][1]);
+    logits[(size_t)(t0 + t) * E + e] = __fadd_rn(ss, cc);
   }
 }
 
@@ -257,7 +274,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
                          float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
-  dim3 g1((E + kGateWarps - 1) / kGateWarps, (n + kGateTokens - 1) / kGateTokens);
+  dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
   gate_logits_kernel<<<g1, kGateWarps * 32, 0, stream>>>(d, E, n, x, w_router, logits);
   dim3 g2((n + kTopkWarps - 1) / kTopkWarps);
   topk_kernel<<<g2, kTopkWarps * 32, 0, stream>>>(E, k, n, logits, topk_idx, topk_w);
