@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -73,30 +74,55 @@ moe_status check_n(const moe_layer_desc* d, int32_t n) {
 }
 
 // Scratch layout for passes of up to n_max tokens (every region 256-byte
-// aligned relative to the workspace base):
-//   logits  [n_max][E] fp32                 routing
-//   h       [n_max·k + s·n_max][I] fp32     SwiGLU activations
-//   xg      [n_max·k][d] fp32                x rows gathered in union order
-//   sync    [kEngineSyncInts] int32          engine job counter, group counts
+// aligned relative to the workspace base); hrows = n_max·k + s·n_max:
+//   logits   [n_max][E] fp32          routing
+//   h        [hrows][I] fp32          SwiGLU activations, CUDA-core groups
+//   h16      [2][hrows][I] bf16       SwiGLU activations of tensor-core groups, hi and lo halves
+//   xg       [n_max·k][d] fp32        x rows gathered in union order
+//   xg16     [2][n_max·k][d] bf16     their hi and lo bf16 halves
+//   x16      [2][n_max][d] bf16       hi and lo bf16 halves of x
+//   sync     [kCcSyncInts] int32      CUDA-core kernel job counter, group counts
+//   sync_mma [kMmaSyncInts] int32     tensor-core kernel job counter, group counts
 struct WsLayout {
-  size_t logits, h, xg, sync, total;
+  size_t logits, h, h16, xg, xg16, x16, sync, sync_mma, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   WsLayout L;
+  const size_t hrows = (size_t)n_max * d->top_k + (size_t)d->n_shared * n_max;
+  const size_t pairs = (size_t)n_max * d->top_k;
   size_t off = 0;
   L.logits = off;
   off = align256(off + (size_t)n_max * d->n_experts * 4);
   L.h = off;
-  off = align256(off + ((size_t)n_max * d->top_k + (size_t)d->n_shared * n_max) * d->inter * 4);
+  off = align256(off + hrows * d->inter * 4);
+  L.h16 = off;
+  off = align256(off + 2 * hrows * d->inter * 2);
   L.xg = off;
-  off = align256(off + (size_t)n_max * d->top_k * d->d * 4);
+  off = align256(off + pairs * d->d * 4);
+  L.xg16 = off;
+  off = align256(off + 2 * pairs * d->d * 2);
+  L.x16 = off;
+  off = align256(off + 2 * (size_t)n_max * d->d * 2);
   L.sync = off;
-  off = align256(off + (size_t)moe::kEngineSyncInts * 4);
+  off = align256(off + (size_t)moe::kCcSyncInts * 4);
+  L.sync_mma = off;
+  off = align256(off + (size_t)moe::kMmaSyncInts * 4);
   L.total = off;
   return L;
+}
+
+// Smallest group that runs on tensor cores (bf16 weights). MOE_MMA_MIN_M in
+// the environment overrides the default (read once; for tuning).
+int mma_min_m() {
+  static int v = [] {
+    const char* e = getenv("MOE_MMA_MIN_M");
+    const int x = e ? atoi(e) : 0;
+    return x >= 2 ? x : moe::kDefaultMmaMinM;
+  }();
+  return v;
 }
 
 moe_status check_ws(const moe_layer_desc* d, int32_t n, const void* ws, size_t ws_bytes) {
@@ -206,8 +232,20 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.ws_up = w->ws_up;
   a.ws_down = w->ws_down;
   a.h = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.h);
-  a.xg = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.xg);
-  a.sync = reinterpret_cast<int*>(static_cast<char*>(workspace) + L.sync);
+  char* ws = static_cast<char*>(workspace);
+  a.xg = reinterpret_cast<float*>(ws + L.xg);
+  const size_t hrows = (size_t)n * desc->top_k + (size_t)desc->n_shared * n;
+  a.h16 = reinterpret_cast<uint16_t*>(ws + L.h16);
+  a.h16lo = a.h16 + hrows * desc->inter;
+  a.xg16 = reinterpret_cast<uint16_t*>(ws + L.xg16);
+  a.xg16lo = a.xg16 + (size_t)n * desc->top_k * desc->d;
+  a.x16 = reinterpret_cast<uint16_t*>(ws + L.x16);
+  a.x16lo = a.x16 + (size_t)n * desc->d;
+  a.sync = reinterpret_cast<int*>(ws + L.sync);
+  a.sync_mma = reinterpret_cast<int*>(ws + L.sync_mma);
+  // fp32 weights never go to the tensor cores (a tf32 product would miss the
+  // fp32 tolerance), so every fp32 group stays on the CUDA-core kernel.
+  a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m() : 0x7fffffff;
   a.y_slot = y_slot;
   a.err = di->err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1,0 +1,79 @@
+// engine.cu — one expert-engine call: the prep kernel and the launch order of
+// the tensor-core and CUDA-core expert kernels.
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "moe_warp.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Runs right before the expert kernels and lets them launch at once
+// (programmatic dependent launch); they wait for it before touching its
+// outputs. Block 0 zeroes both kernels' job counters and group counts.
+// Blocks [0, gather_rows): xg[r] = x[pair_tok[r]] (fp32) and its bf16 hi/lo
+// halves (dedup, union order). Blocks [gather_rows, gather_rows + n): the
+// bf16 hi/lo halves of x. hi = bf16(v), lo = bf16(v − hi).
+__global__ void __launch_bounds__(256)
+    engine_prep_kernel(int d, int n, int gather_rows, const float* __restrict__ x,
+                       const int32_t* __restrict__ pair_tok, float* __restrict__ xg,
+                       uint16_t* __restrict__ xg16, uint16_t* __restrict__ xg16lo,
+                       uint16_t* __restrict__ x16, uint16_t* __restrict__ x16lo,
+                       int* __restrict__ sync_cc, int* __restrict__ sync_mma) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < kCcSyncInts; i += blockDim.x) sync_cc[i] = 0;
+    for (int i = threadIdx.x; i < kMmaSyncInts; i += blockDim.x) sync_mma[i] = 0;
+  }
+  const int b = blockIdx.x;
+  const float* src;
+  float* dst32 = nullptr;
+  uint16_t *hi, *lo;
+  if (b < gather_rows) {
+    src = x + (size_t)pair_tok[b] * d;
+    dst32 = xg + (size_t)b * d;
+    hi = xg16 + (size_t)b * d;
+    lo = xg16lo + (size_t)b * d;
+  } else if (b < gather_rows + n) {
+    src = x + (size_t)(b - gather_rows) * d;
+    hi = x16 + (size_t)(b - gather_rows) * d;
+    lo = x16lo + (size_t)(b - gather_rows) * d;
+  } else {
+    return;
+  }
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(src) + i);
+    if (dst32) reinterpret_cast<float4*>(dst32)[i] = v;
+    const uint2 h = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    const uint2 l = make_uint2(pack_bf16x2(v.x - bf16lo(h.x), v.y - bf16hi(h.x)),
+                               pack_bf16x2(v.z - bf16lo(h.y), v.w - bf16hi(h.y)));
+    reinterpret_cast<uint2*>(hi)[i] = h;
+    reinterpret_cast<uint2*>(lo)[i] = l;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
+  const int gather = a.engine == 1 ? a.n * a.k : 0;
+  const int convert = a.wdtype == 1 ? a.n : 0;
+  engine_prep_kernel<<<max(gather + convert, 1), 256, 0, stream>>>(
+      a.d, convert, gather, a.x, a.pair_tok, a.xg, a.xg16, a.xg16lo, a.x16, a.x16lo, a.sync,
+      a.sync_mma);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.wdtype == 1 && a.mma_min_m <= MOE_MAX_TOKENS) {
+    e = launch_expert_mma(a, num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_expert_cc(a, num_sms, stream);
+}
+
+}  // namespace moe

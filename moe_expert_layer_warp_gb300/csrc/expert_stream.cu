@@ -33,6 +33,7 @@
 #include "moe_warp.h"
 #include "common.cuh"
 #include "launch.h"
+#include "plan.cuh"
 #include "tmap.h"
 
 namespace moe {
@@ -42,29 +43,21 @@ constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowChunks = 32;
 constexpr int kChunkBytes = 512;
-constexpr int kMaxM = 8;
-constexpr int kStages = 8;
+constexpr int kMaxM = kCcSub;
+constexpr int kStages = 11;
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
-constexpr int kMaxEntries = MOE_MAX_PAIRS + MOE_MAX_SHARED * (MOE_MAX_TOKENS / kMaxM);
+constexpr int kMaxEntries = max_entries(kMaxM);
 constexpr int kRowsPhase0 = 16;  // rows of I per phase-0 tile (gate and up)
 constexpr int kRowsPhase1 = 32;  // rows of d per phase-1 tile
-constexpr int kSyncInts = 1 + kMaxEntries;  // job counter + per-group phase-0 tile counts
-static_assert(kSyncInts == kEngineSyncInts, "engine scratch size");
-
-struct Entry {
-  int src;   // routed expert id (>= 0), or -(i+1) for shared expert i
-  int row0;  // first activation row (in h)
-  int m;     // tokens (1..kMaxM)
-  int arow;  // first row of the phase-0 input box (x row or gathered-x row); phase 1 reads h at row0
-};
+static_assert(1 + kMaxEntries == kCcSyncInts, "engine scratch size");
 
 // Tensor maps of one launch. w0/w1/w2: routed experts' W_gate, W_up, W_down
-// ([E][rows][K]); sw0/sw1/sw2: the shared experts'. a1/a8: phase-0 input rows
+// ([E][rows][K]); sw0/sw1/sw2: the shared experts'. a1/aM: phase-0 input rows
 // of routed groups (x, or x gathered in union order) with a box of 1 or 8
-// rows; s1/s8: phase-0 input rows of shared-expert groups (x); h1/h8: phase-1
+// rows; s1/sM: phase-0 input rows of shared-expert groups (x); h1/hM: phase-1
 // input rows (h).
 struct Maps {
-  CUtensorMap w0, w1, w2, sw0, sw1, sw2, a1, a8, s1, s8, h1, h8;
+  CUtensorMap w0, w1, w2, sw0, sw1, sw2, a1, aM, s1, sM, h1, hM;
 };
 
 struct Params {
@@ -86,88 +79,6 @@ struct Layout {
   static constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
   static constexpr int kBytes = kOffMisc + 64 * 4;
 };
-
-// Exclusive prefix sum over the block (one value per thread). Returns the
-// thread's offset; *total receives the sum. Uses scratch[0..warps].
-MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += t;
-  }
-  if (lane == 31) scratch[warp] = inc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      const int c = scratch[w];
-      scratch[w] = run;
-      run += c;
-    }
-    scratch[nwarps] = run;
-  }
-  __syncthreads();
-  const int r = scratch[warp] + inc - v;
-  *total = scratch[nwarps];
-  __syncthreads();
-  return r;
-}
-
-// Builds the group table and the per-row output maps (slot row, combine
-// weight) in shared memory. Returns the number of groups.
-MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* row_w,
-                       int* scratch) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int P = a.n * a.k, S = a.k + a.s;
-  int nr;
-  if (a.engine == 0) {
-    for (int p = tid; p < P; p += nt) {
-      const int t = p / a.k, j = p - t * a.k;
-      plan[p] = Entry{a.topk_idx[p], p, 1, t};
-      row_out[p] = t * S + j;
-      row_w[p] = a.topk_w[p];
-    }
-    nr = P;
-  } else {
-    int U = *a.union_count;
-    if (U < 0 || U > a.E) {  // not a union of this layer: run nothing, flag it
-      if (tid == 0) report_error(a.err, ERR_CHECK, 0x230);
-      U = 0;
-    }
-    int m = 0, e = 0, r0 = 0;
-    if (tid < U) {
-      r0 = a.offsets[tid];
-      m = a.offsets[tid + 1] - r0;
-      e = a.union_ids[tid];
-    }
-    const int nsub = (m + kMaxM - 1) / kMaxM;
-    const int pos = block_exclusive_scan(nsub, scratch, &nr);
-    for (int q = 0; q < nsub; ++q) {
-      const int rr = r0 + q * kMaxM;
-      plan[pos + q] = Entry{e, rr, min(kMaxM, m - q * kMaxM), rr};
-    }
-    for (int r = tid; r < P; r += nt) {
-      const int t = a.pair_tok[r], j = a.pair_slot[r];
-      row_out[r] = t * S + j;
-      row_w[r] = a.topk_w[t * a.k + j];
-    }
-  }
-  const int per = (a.n + kMaxM - 1) / kMaxM;
-  for (int q = tid; q < a.s * per; q += nt) {
-    const int i = q / per, c = q - (q / per) * per;
-    const int rr = P + i * a.n + c * kMaxM;
-    plan[nr + q] = Entry{-(i + 1), rr, min(kMaxM, a.n - c * kMaxM), c * kMaxM};
-  }
-  for (int r = tid; r < a.s * a.n; r += nt) {
-    const int i = r / a.n, t = r - (r / a.n) * a.n;
-    row_out[P + r] = t * S + a.k + i;
-    row_w[P + r] = 1.f;
-  }
-  return nr + a.s * per;
-}
 
 // Columns a lane owns inside a stage, chosen so that its shared-memory reads
 // are conflict-free: bf16 stages (256 columns) give lane l the runs
@@ -213,20 +124,6 @@ struct LaneMap<4> {
   }
 };
 
-MOE_DEV int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-MOE_DEV void red_release_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-MOE_DEV void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // One launch runs both phases. Jobs 0 .. J0-1 are phase-0 jobs (group-major),
 // jobs J0 .. J0+J1-1 phase-1 jobs (group-major); the producer thread of each
 // CTA takes the next job from a global counter, so every job taken belongs to
@@ -264,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     prefetch_tmap(&prm.maps.w2);
     prefetch_tmap(&prm.maps.a1);
   }
-  const int n_groups = build_plan(a, plan, row_out, row_w, misc);
+  const int n_groups = build_plan<kMaxM, false>(a, plan, row_out, row_w, misc);
   __syncthreads();
   // the prep kernel (counters zeroed, rows gathered) must be complete
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -309,11 +206,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         if (ph == 0) {
           m0 = shared_expert ? &prm.maps.sw0 : &prm.maps.w0;
           m1 = shared_expert ? &prm.maps.sw1 : &prm.maps.w1;
-          mx = shared_expert ? (en.m == 1 ? &prm.maps.s1 : &prm.maps.s8)
-                             : (en.m == 1 ? &prm.maps.a1 : &prm.maps.a8);
+          mx = shared_expert ? (en.m == 1 ? &prm.maps.s1 : &prm.maps.sM)
+                             : (en.m == 1 ? &prm.maps.a1 : &prm.maps.aM);
         } else {
           m0 = shared_expert ? &prm.maps.sw2 : &prm.maps.w2;
-          mx = en.m == 1 ? &prm.maps.h1 : &prm.maps.h8;
+          mx = en.m == 1 ? &prm.maps.h1 : &prm.maps.hM;
         }
         const int arow = ph == 0 ? en.arow : en.row0;
         const uint32_t xbytes = (en.m == 1 ? 1 : kMaxM) * KS * 4;
@@ -469,26 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
 }
 
-// Runs right before the engine kernel: zeroes the engine's job counter and
-// group counts and, for dedup, gathers xg[r][:] = x[pair_tok[r]][:] over the
-// n·k pair rows (union order). It lets the engine launch at once
-// (programmatic dependent launch); the engine waits for it before it touches
-// either.
-__global__ void __launch_bounds__(256)
-    engine_prep_kernel(int d, int gather_rows, const float* __restrict__ x,
-                       const int32_t* __restrict__ pair_tok, float* __restrict__ xg,
-                       int* __restrict__ sync, int sync_ints) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < sync_ints; i += blockDim.x) sync[i] = 0;
-  const int r = blockIdx.x;
-  if (r < gather_rows) {
-    const float4* src = reinterpret_cast<const float4*>(x + (size_t)pair_tok[r] * d);
-    float4* dst = reinterpret_cast<float4*>(xg + (size_t)r * d);
-    for (int i = threadIdx.x; i < d / 4; i += blockDim.x) dst[i] = __ldg(src + i);
-  }
-}
-
 // ------------------------------------------------------------------ host --
 bool weight_map(CUtensorMap* m, const void* p, int WB, int n_mat, int rows, int K, int box_rows) {
   const int ks = WB == 2 ? 256 : 128;
@@ -536,17 +413,12 @@ cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream)
   const float* xa = a.engine == 0 ? a.x : a.xg;
   const int xa_rows = a.engine == 0 ? a.n : P;
   ok &= act_map(&prm.maps.a1, xa, xa_rows, a.d, ks, 1);
-  ok &= act_map(&prm.maps.a8, xa, xa_rows, a.d, ks, kMaxM);
+  ok &= act_map(&prm.maps.aM, xa, xa_rows, a.d, ks, kMaxM);
   ok &= act_map(&prm.maps.s1, a.x, a.n, a.d, ks, 1);
-  ok &= act_map(&prm.maps.s8, a.x, a.n, a.d, ks, kMaxM);
+  ok &= act_map(&prm.maps.sM, a.x, a.n, a.d, ks, kMaxM);
   ok &= act_map(&prm.maps.h1, a.h, hrows, a.I, ks, 1);
-  ok &= act_map(&prm.maps.h8, a.h, hrows, a.I, ks, kMaxM);
+  ok &= act_map(&prm.maps.hM, a.h, hrows, a.I, ks, kMaxM);
   if (!ok) return cudaErrorInvalidValue;
-  const int gather = a.engine == 1 ? P : 0;
-  engine_prep_kernel<<<max(gather, 1), 256, 0, stream>>>(a.d, gather, a.x, a.pair_tok, a.xg,
-                                                          a.sync, kSyncInts);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the engine's prologue overlaps the prep
   // kernel; its griddepcontrol.wait orders every use of the prep's outputs.
   cudaLaunchConfig_t cfg;
@@ -565,7 +437,7 @@ cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_expert_cc(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   return a.wdtype == 1 ? launch_engine<2>(a, num_sms, stream) : launch_engine<4>(a, num_sms, stream);
 }
 

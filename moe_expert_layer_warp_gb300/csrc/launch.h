@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "moe_warp.h"
+
 namespace moe {
 
 // Routing: gate GEMV with compensated fp32 dots (writes logits[n][E] into
@@ -38,20 +40,44 @@ struct ExpertArgs {
   const void* ws_gate;
   const void* ws_up;
   const void* ws_down;
-  float* h;             // [n·k + s·n][I] fp32 scratch
+  float* h;             // [n·k + s·n][I] fp32 scratch (CUDA-core groups)
   float* xg;            // [n·k][d] fp32 scratch: x rows gathered in union order (dedup)
-  int* sync;            // [kSyncInts] scratch: job counter and per-group counts (zeroed per call)
+  uint16_t* h16;        // [n·k + s·n][I] bf16 scratch (tensor-core groups): hi half of h
+  uint16_t* h16lo;      //   and lo half: h = hi + lo to ~16 extra mantissa bits
+  uint16_t* xg16;       // [n·k][d] bf16 scratch: hi half of xg
+  uint16_t* xg16lo;     //   and lo half
+  uint16_t* x16;        // [n][d] bf16 scratch: hi half of x
+  uint16_t* x16lo;      //   and lo half
+  int* sync;            // [kCcSyncInts] CUDA-core kernel's job counter and group counts
+  int* sync_mma;        // [kMmaSyncInts] tensor-core kernel's job counter and group counts
+  int mma_min_m;        // groups with at least this many tokens run on tensor cores
   float* y_slot;
   unsigned int* err;
 };
 
-// Expert FFNs over the pass on CUDA cores in one persistent launch, weights
-// streamed through a ring of shared-memory stages filled by the TMA engine:
-// h = silu(Wg x)⊙(Wu x), then y_slot = w · (W_down h).
+// The expert engine of one call: a prep kernel (counters zeroed, rows
+// gathered and rounded for the tensor cores), the tensor-core kernel (bf16
+// weights only) and the CUDA-core kernel.
 cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream);
 
-// Ints of scratch the engine's job counter and group counts occupy.
-constexpr int kEngineSyncInts = 1 + 512 + 4 * 16;
+// Expert FFNs of the groups below mma_min_m tokens on CUDA cores in one
+// persistent launch, weights streamed through a ring of shared-memory stages
+// filled by the TMA engine: h = silu(Wg x)⊙(Wu x), then y_slot = w·(W_down h).
+cudaError_t launch_expert_cc(const ExpertArgs& a, int num_sms, cudaStream_t stream);
+
+// Tokens per plan entry of the CUDA-core and tensor-core kernels, and the
+// ints of counter scratch each kernel uses (job counter + one per entry).
+constexpr int kCcSub = 2;
+constexpr int kMmaSub = 32;
+constexpr int kCcSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kCcSub - 1) / kCcSub);
+constexpr int kMmaSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kMmaSub - 1) / kMmaSub);
+
+// Smallest group (tokens) that runs on tensor cores when the weights are
+// bf16; fp32-weight layers always use the CUDA-core kernel.
+constexpr int kDefaultMmaMinM = 3;
+
+// Tensor-core expert kernel (tcgen05 + TMEM) for groups of ≥ mma_min_m tokens.
+cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t stream);
 
 // y[t] = Σ_j y_slot[t][j] over the k+s slots, in slot order.
 cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,

@@ -1,0 +1,146 @@
+// plan.cuh — the group table both expert kernels build at start-up.
+//
+// A "group" is one expert applied to a set of tokens whose activation rows
+// are consecutive rows of the h scratch:
+//   per-slot: one group per (token, slot) pair, rows in pair order t·k + j;
+//   dedup:    one group per union expert, rows in the union's (expert, token)
+//             order (moe_build_union's offsets);
+//   both:     each shared expert over all n tokens, rows n·k + i·n + t.
+// Groups with at least `mma_min_m` tokens belong to the tensor-core kernel,
+// the others to the CUDA-core kernel. Each kernel splits its groups into
+// sub-groups of at most SUB tokens (one plan entry each).
+#pragma once
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+
+struct Entry {
+  int src;   // routed expert id (>= 0), or -(i+1) for shared expert i
+  int row0;  // first activation row (in h)
+  int m;     // tokens of this sub-group
+  int arow;  // first row of the phase-0 input box (x row or gathered-x row); phase 1 reads h at row0
+};
+
+// Exclusive prefix sum over the block (one value per thread). Returns the
+// thread's offset; *total receives the sum. Uses scratch[0..warps].
+MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += t;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = scratch[w];
+      scratch[w] = run;
+      run += c;
+    }
+    scratch[nwarps] = run;
+  }
+  __syncthreads();
+  const int r = scratch[warp] + inc - v;
+  *total = scratch[nwarps];
+  __syncthreads();
+  return r;
+}
+
+// Builds this kernel's entries and the per-row output maps (slot row,
+// combine weight) in shared memory; returns the number of entries.
+// MMA_SIDE selects groups with m ≥ a.mma_min_m, else the others.
+// Needs blockDim.x ≥ MOE_MAX_EXPERTS (one thread per union expert).
+template <int SUB, bool MMA_SIDE>
+MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* row_w,
+                       int* scratch) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int P = a.n * a.k, S = a.k + a.s;
+  auto mine = [&](int m) { return (m >= a.mma_min_m) == MMA_SIDE; };
+  int nr = 0;
+  if (a.engine == 0) {
+    if (mine(1)) {
+      for (int p = tid; p < P; p += nt) plan[p] = Entry{a.topk_idx[p], p, 1, p / a.k};
+      nr = P;
+    }
+    for (int p = tid; p < P; p += nt) {
+      const int t = p / a.k, j = p - t * a.k;
+      row_out[p] = t * S + j;
+      row_w[p] = a.topk_w[p];
+    }
+  } else {
+    int U = *a.union_count;
+    if (U < 0 || U > a.E) {  // not a union of this layer: run nothing, flag it
+      if (tid == 0) report_error(a.err, ERR_CHECK, 0x230);
+      U = 0;
+    }
+    int m = 0, e = 0, r0 = 0;
+    if (tid < U) {
+      r0 = a.offsets[tid];
+      m = a.offsets[tid + 1] - r0;
+      e = a.union_ids[tid];
+    }
+    const int nsub = (m > 0 && mine(m)) ? (m + SUB - 1) / SUB : 0;
+    const int pos = block_exclusive_scan(nsub, scratch, &nr);
+    for (int q = 0; q < nsub; ++q) {
+      const int rr = r0 + q * SUB;
+      plan[pos + q] = Entry{e, rr, min(SUB, m - q * SUB), rr};
+    }
+    for (int r = tid; r < P; r += nt) {
+      const int t = a.pair_tok[r], j = a.pair_slot[r];
+      row_out[r] = t * S + j;
+      row_w[r] = a.topk_w[t * a.k + j];
+    }
+  }
+  const int per = mine(a.n) ? (a.n + SUB - 1) / SUB : 0;
+  for (int q = tid; q < a.s * per; q += nt) {
+    const int i = q / per, c = q - (q / per) * per;
+    const int rr = P + i * a.n + c * SUB;
+    plan[nr + q] = Entry{-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB};
+  }
+  for (int r = tid; r < a.s * a.n; r += nt) {
+    const int i = r / a.n, t = r - (r / a.n) * a.n;
+    row_out[P + r] = t * S + a.k + i;
+    row_w[P + r] = 1.f;
+  }
+  return nr + a.s * per;
+}
+
+// Upper bound of a kernel's entries for sub-groups of SUB tokens.
+constexpr int max_entries(int sub) {
+  return MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + sub - 1) / sub);
+}
+
+MOE_DEV int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+MOE_DEV void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+MOE_DEV void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until *p ≥ target (acquire). False on timeout (recorded).
+MOE_DEV bool wait_count(const int* p, int target, unsigned int* err, unsigned int site) {
+  const unsigned long long t0 = global_ns();
+  unsigned int it = 0;
+  while (ld_acquire(p) < target) {
+    if ((++it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+      report_error(err, ERR_TIMEOUT, site);
+      return false;
+    }
+  }
+  return true;
+}
+
+}  // namespace moe

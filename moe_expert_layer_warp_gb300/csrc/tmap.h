@@ -17,7 +17,7 @@ namespace moe {
 
 struct TmapKey {
   uint64_t ptr;
-  int dtype, rank;
+  int dtype, rank, swizzle;
   uint64_t dims[3];
   uint64_t strides[2];
   uint32_t box[3];
@@ -43,11 +43,12 @@ inline EncodeFn encode_fn() {
   return fn;
 }
 
-// Encodes (or fetches from the cache) a tiled, non-swizzled tensor map over a
-// row-major tensor. dims/box are innermost-first; strides (bytes) are those of
+// Encodes (or fetches from the cache) a tiled tensor map over a row-major
+// tensor (no swizzle unless asked). dims/box are innermost-first; strides (bytes) are those of
 // dims[1..rank-1]. Out-of-bounds elements of a box read as zero.
 inline bool make_tmap(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int rank,
-                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
   static std::mutex mu;
   static std::map<TmapKey, CUtensorMap> cache;
   TmapKey key;
@@ -55,6 +56,7 @@ inline bool make_tmap(CUtensorMap* out, const void* ptr, CUtensorMapDataType dty
   key.ptr = reinterpret_cast<uint64_t>(ptr);
   key.dtype = (int)dtype;
   key.rank = rank;
+  key.swizzle = (int)swizzle;
   for (int i = 0; i < rank; ++i) {
     key.dims[i] = dims[i];
     key.box[i] = box[i];
@@ -76,7 +78,7 @@ inline bool make_tmap(CUtensorMap* out, const void* ptr, CUtensorMapDataType dty
   }
   for (int i = 0; i + 1 < rank; ++i) s[i] = strides[i];
   CUresult r = fn(out, dtype, (cuuint32_t)rank, const_cast<void*>(ptr), d, s, b, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   if (cache.size() > 4096) cache.clear();

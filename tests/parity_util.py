@@ -62,8 +62,10 @@ def check_routing(gpu_idx: np.ndarray, gpu_w: np.ndarray, orc_route: dict, d: in
     return amb
 
 
-def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float, what: str):
-    rms = float(np.sqrt(np.mean(np.square(ref))))
+def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float, what: str, scale=None):
+    """max|got − ref| ≤ tol · rms(scale), scale defaulting to ref. Slot outputs
+    use rms(y) as their scale: the tolerance is stated on y."""
+    rms = float(np.sqrt(np.mean(np.square(ref if scale is None else scale))))
     err = float(np.max(np.abs(got.astype(np.float64) - ref)))
     assert err <= tol * rms, "%s: max|err| %.3e > %.1e · rms %.3e" % (what, err, tol, rms)
     return err / rms

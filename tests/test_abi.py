@@ -10,7 +10,8 @@ import pytest
 from moe_expert_layer_warp_gb300 import api, build
 from moe_expert_layer_warp_gb300.configs import ALL, LayerShape, W_BF16
 
-SYNC_INTS = 1 + 512 + 4 * 16     # engine job counter + per-group tile counts
+CC_SYNC_INTS = 1 + 512 + 4 * 64   # CUDA-core kernel: job counter + per-entry tile counts
+MMA_SYNC_INTS = 1 + 512 + 4 * 4   # tensor-core kernel: job counter + per-entry tile counts
 HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
@@ -45,8 +46,10 @@ def test_workspace_bytes_closed_form(lib):
         n = max(w.pass_sizes) * w.streams
         got = api.moe_workspace_bytes(api.make_desc(sh), n)
         a256 = lambda v: (v + 255) // 256 * 256
-        want = (a256(n * sh.n_experts * 4) + a256((n * sh.top_k + sh.n_shared * n) * sh.inter * 4)
-                + a256(n * sh.top_k * sh.d * 4) + a256(SYNC_INTS * 4))
+        hrows = n * sh.top_k + sh.n_shared * n
+        want = (a256(n * sh.n_experts * 4) + a256(hrows * sh.inter * 4) + a256(2 * hrows * sh.inter * 2)
+                + a256(n * sh.top_k * sh.d * 4) + a256(2 * n * sh.top_k * sh.d * 2)
+                + a256(2 * n * sh.d * 2) + a256(CC_SYNC_INTS * 4) + a256(MMA_SYNC_INTS * 4))
         assert got == want, w.name
 
 

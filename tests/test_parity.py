@@ -77,8 +77,8 @@ def check_pass(L, x_np, tokens=None, runner=None):
     tol = pu.y_tol(sh)
     pu.assert_close_rms(g["y_ps"][toks], y_o, tol, "per-slot y")
     pu.assert_close_rms(g["y_dd"][toks], y_o, tol, "dedup y")
-    pu.assert_close_rms(g["slots_ps"][toks], slots_o, tol, "per-slot slots")
-    pu.assert_close_rms(g["slots_dd"][toks], slots_o, tol, "dedup slots")
+    pu.assert_close_rms(g["slots_ps"][toks], slots_o, tol, "per-slot slots", scale=y_o)
+    pu.assert_close_rms(g["slots_dd"][toks], slots_o, tol, "dedup slots", scale=y_o)
     ref = g["y_ps"].astype(np.float64)
     pu.assert_close_rms(g["y_dd"], ref, tol, "dedup vs per-slot")
     return g
