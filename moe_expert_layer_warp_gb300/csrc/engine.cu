@@ -69,11 +69,17 @@ cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t 
       a.sync_mma);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.wdtype == 1 && a.mma_min_m <= MOE_MAX_TOKENS) {
-    e = launch_expert_mma(a, num_sms, stream);
+  // The tensor-core kernel runs only where a group can reach mma_min_m
+  // tokens: a group never holds more than the pass's n tokens, and per-slot
+  // routed groups hold one, so per-slot needs shared experts for it.
+  const bool mma = a.wdtype == 1 && a.n >= a.mma_min_m && (a.engine == 1 || a.s > 0);
+  ExpertArgs b = a;
+  b.cc_waits_prep = mma ? 0 : 1;
+  if (mma) {
+    e = launch_expert_mma(b, num_sms, stream);
     if (e != cudaSuccess) return e;
   }
-  return launch_expert_cc(a, num_sms, stream);
+  return launch_expert_cc(b, num_sms, stream);
 }
 
 }  // namespace moe

@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   __syncthreads();
   umma::fence_after_sync();
   asm volatile("griddepcontrol.wait;" ::: "memory");  // prep kernel's outputs
+  // The CUDA-core kernel may start now, on SMs this kernel leaves free: it
+  // needs nothing from this kernel, and the prep kernel is complete.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = *tmem_base;
 
   const int T0 = (a.I + kM - 1) / kM, T1 = (a.d + kM - 1) / kM;

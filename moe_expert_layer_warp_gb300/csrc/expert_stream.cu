@@ -163,8 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
   const int n_groups = build_plan<kMaxM, false>(a, plan, row_out, row_w, misc);
   __syncthreads();
-  // the prep kernel (counters zeroed, rows gathered) must be complete
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The prep kernel (counters zeroed, rows gathered) must be complete. When
+  // this kernel follows the tensor-core kernel, that kernel released it only
+  // after its own wait on the prep kernel, so there is nothing to wait for.
+  if (a.cc_waits_prep) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int T0 = a.I / kRowsPhase0, T1 = a.d / kRowsPhase1;
   const int J0 = n_groups * T0, J = J0 + n_groups * T1;

@@ -51,6 +51,7 @@ struct ExpertArgs {
   int* sync;            // [kCcSyncInts] CUDA-core kernel's job counter and group counts
   int* sync_mma;        // [kMmaSyncInts] tensor-core kernel's job counter and group counts
   int mma_min_m;        // groups with at least this many tokens run on tensor cores
+  int cc_waits_prep;    // 1: the CUDA-core kernel directly follows the prep kernel
   float* y_slot;
   unsigned int* err;
 };
