@@ -114,15 +114,23 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   return L;
 }
 
-// Smallest group that runs on tensor cores (bf16 weights). MOE_MMA_MIN_M in
-// the environment overrides the default (read once; for tuning).
-int mma_min_m() {
-  static int v = [] {
+// Smallest group (tokens) that runs on the tensor-core kernel (bf16 weights).
+// That kernel works in 128-row tiles of an expert (one job each, gate/up and
+// down); it pays off when its jobs fill the GPU. An expert with at least 64
+// such tiles (Mixtral- or DeepSeek-V3-shaped) gives enough work from groups of
+// 3 tokens; smaller experts (DeepSeek-V2-Lite-shaped: 27 tiles) stay on the
+// CUDA-core kernel, which reads a group's sub-groups tile by tile so that L2
+// serves the repeats, up to 16 tokens. MOE_MMA_MIN_M in the environment
+// overrides the choice (read once; for tuning).
+int mma_min_m(const moe_layer_desc* d) {
+  static const int forced = [] {
     const char* e = getenv("MOE_MMA_MIN_M");
     const int x = e ? atoi(e) : 0;
-    return x >= 2 ? x : moe::kDefaultMmaMinM;
+    return x >= 2 ? x : 0;
   }();
-  return v;
+  if (forced) return forced;
+  const int tiles = (d->inter + 127) / 128 + (d->d + 127) / 128;
+  return tiles >= 64 ? 3 : 17;
 }
 
 moe_status check_ws(const moe_layer_desc* d, int32_t n, const void* ws, size_t ws_bytes) {
@@ -245,7 +253,7 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.sync_mma = reinterpret_cast<int*>(ws + L.sync_mma);
   // fp32 weights never go to the tensor cores (a tf32 product would miss the
   // fp32 tolerance), so every fp32 group stays on the CUDA-core kernel.
-  a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m() : 0x7fffffff;
+  a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m(desc) : 0x7fffffff;
   a.y_slot = y_slot;
   a.err = di->err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -135,6 +135,15 @@ MOE_DEV void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Every kernel of a pass is launched with programmatic stream serialization.
+// pdl_wait() blocks until the previous kernel in the stream has completed and
+// its writes are visible; pdl_trigger() lets the next kernel be scheduled.
+// Each kernel calls pdl_wait() before it exits, so completion stays ordered
+// along the stream even where kernels overlap.
+MOE_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------- small utils --
 MOE_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 MOE_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

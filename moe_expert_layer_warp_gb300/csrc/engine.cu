@@ -15,9 +15,9 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Runs right before the expert kernels and lets them launch at once
-// (programmatic dependent launch); they wait for it before touching its
-// outputs. Block 0 zeroes both kernels' job counters and group counts.
+// Runs right before the expert kernels and lets them launch as soon as it
+// starts (programmatic dependent launch); they wait for it before touching
+// its outputs. Block 0 zeroes both kernels' job counters and group counts.
 // Blocks [0, gather_rows): xg[r] = x[pair_tok[r]] (fp32) and its bf16 hi/lo
 // halves (dedup, union order). Blocks [gather_rows, gather_rows + n): the
 // bf16 hi/lo halves of x. hi = bf16(v), lo = bf16(v − hi).
@@ -27,7 +27,8 @@ __global__ void __launch_bounds__(256)
                        uint16_t* __restrict__ xg16, uint16_t* __restrict__ xg16lo,
                        uint16_t* __restrict__ x16, uint16_t* __restrict__ x16lo,
                        int* __restrict__ sync_cc, int* __restrict__ sync_mma) {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_wait();     // the union (dedup) or routing that precedes it
+  pdl_trigger();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < kCcSyncInts; i += blockDim.x) sync_cc[i] = 0;
     for (int i = threadIdx.x; i < kMmaSyncInts; i += blockDim.x) sync_mma[i] = 0;
@@ -64,10 +65,9 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   const int gather = a.engine == 1 ? a.n * a.k : 0;
   const int convert = a.wdtype == 1 ? a.n : 0;
-  engine_prep_kernel<<<max(gather + convert, 1), 256, 0, stream>>>(
-      a.d, convert, gather, a.x, a.pair_tok, a.xg, a.xg16, a.xg16lo, a.x16, a.x16lo, a.sync,
-      a.sync_mma);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + convert, 1)), dim3(256), 0,
+                             stream, a.d, convert, gather, a.x, a.pair_tok, a.xg, a.xg16,
+                             a.xg16lo, a.x16, a.x16lo, a.sync, a.sync_mma);
   if (e != cudaSuccess) return e;
   // The tensor-core kernel runs only where a group can reach mma_min_m
   // tokens: a group never holds more than the pass's n tokens, and per-slot

@@ -122,10 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // prep kernel's outputs
+  pdl_wait();     // prep kernel's outputs
   // The CUDA-core kernel may start now, on SMs this kernel leaves free: it
   // needs nothing from this kernel, and the prep kernel is complete.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();
   const uint32_t tmem = *tmem_base;
 
   const int T0 = (a.I + kM - 1) / kM, T1 = (a.d + kM - 1) / kM;
@@ -156,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
         }
         const int ph = job < J0 ? 0 : 1;
         const int jj = ph == 0 ? job : job - J0;
-        const int T = ph == 0 ? T0 : T1;
-        const int g = jj / T, tile = jj - g * T;
+        int g, tile;
+        job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile);
         const Entry en = plan[g];
         const bool sh = en.src < 0;
         const int ec = sh ? -en.src - 1 : en.src;
@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
         }
         const int ph = job < J0 ? 0 : 1;
         const int jj = ph == 0 ? job : job - J0;
-        const int g = jj / (ph == 0 ? T0 : T1);
+        int g, tile_unused;
+        job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile_unused);
         const int m = plan[g].m;
         const uint32_t idesc = umma::idesc_bf16(kM, m <= 16 ? 16 : 32);
         const uint32_t dacc = tmem + slot * kSlotCols;
@@ -306,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       if (job < 0) break;
       const int ph = job < J0 ? 0 : 1;
       const int jj = ph == 0 ? job : job - J0;
-      const int T = ph == 0 ? T0 : T1;
-      const int g = jj / T, tile = jj - g * T;
+      int g, tile;
+      job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile);
       const Entry en = plan[g];
       const int m = en.m;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + slot * kSlotCols;

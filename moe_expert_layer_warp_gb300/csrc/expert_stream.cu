@@ -44,7 +44,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowChunks = 32;
 constexpr int kChunkBytes = 512;
 constexpr int kMaxM = kCcSub;
-constexpr int kStages = 11;
+constexpr int kStages = 10;
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
 constexpr int kMaxEntries = max_entries(kMaxM);
 constexpr int kRowsPhase0 = 16;  // rows of I per phase-0 tile (gate and up)
@@ -165,8 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   __syncthreads();
   // The prep kernel (counters zeroed, rows gathered) must be complete. When
   // this kernel follows the tensor-core kernel, that kernel released it only
-  // after its own wait on the prep kernel, so there is nothing to wait for.
-  if (a.cc_waits_prep) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // after its own wait on the prep kernel, so this kernel starts at once and
+  // waits for the tensor-core kernel only before it exits (below).
+  if (a.cc_waits_prep) pdl_wait();
+  pdl_trigger();
 
   const int T0 = a.I / kRowsPhase0, T1 = a.d / kRowsPhase1;
   const int J0 = n_groups * T0, J = J0 + n_groups * T1;
@@ -199,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         }
         const int ph = job < J0 ? 0 : 1;
         const int jj = ph == 0 ? job : job - J0;
-        const int T = ph == 0 ? T0 : T1;
-        const int g = jj / T, tile = jj - g * T;
+        int g, tile;
+        job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile);
         const Entry en = plan[g];
         const bool shared_expert = en.src < 0;
         const int ecoord = shared_expert ? -en.src - 1 : en.src;
@@ -273,6 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         }
       }
     }
+    // Every path out of this kernel passes here: the grid cannot complete
+    // before the tensor-core kernel it overlaps has completed.
+    if (!a.cc_waits_prep) pdl_wait();
     return;
   }
 
@@ -294,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     if (job < 0) break;
     const int ph = job < J0 ? 0 : 1;
     const int jj = ph == 0 ? job : job - J0;
-    const int T = ph == 0 ? T0 : T1;
-    const int g = jj / T, tile = jj - g * T;
+    int g, tile;
+    job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile);
     const Entry en = plan[g];
     const int m = en.m;
     const int nks = ph == 0 ? nks0 : nks1;

@@ -9,6 +9,24 @@
 
 namespace moe {
 
+// Launches `kernel` on `stream` with programmatic stream serialization, so
+// that it may start while the previous kernel in the stream finishes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Routing: gate GEMV with compensated fp32 dots (writes logits[n][E] into
 // scratch), then warp-per-token top-k + softmax over the k kept logits.
 cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
@@ -68,14 +86,10 @@ cudaError_t launch_expert_cc(const ExpertArgs& a, int num_sms, cudaStream_t stre
 
 // Tokens per plan entry of the CUDA-core and tensor-core kernels, and the
 // ints of counter scratch each kernel uses (job counter + one per entry).
-constexpr int kCcSub = 2;
+constexpr int kCcSub = 4;
 constexpr int kMmaSub = 32;
 constexpr int kCcSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kCcSub - 1) / kCcSub);
 constexpr int kMmaSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kMmaSub - 1) / kMmaSub);
-
-// Smallest group (tokens) that runs on tensor cores when the weights are
-// bf16; fp32-weight layers always use the CUDA-core kernel.
-constexpr int kDefaultMmaMinM = 3;
 
 // Tensor-core expert kernel (tcgen05 + TMEM) for groups of ≥ mma_min_m tokens.
 cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t stream);

@@ -8,7 +8,9 @@
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
 // Groups with at least `mma_min_m` tokens belong to the tensor-core kernel,
 // the others to the CUDA-core kernel. Each kernel splits its groups into
-// sub-groups of at most SUB tokens (one plan entry each).
+// sub-groups of at most SUB tokens (one plan entry each). Sibling sub-groups
+// of one group take consecutive jobs tile by tile (job_entry), so their CTAs
+// read each weight tile at nearly the same time and L2 serves the repeats.
 #pragma once
 
 #include "common.cuh"
@@ -17,11 +19,22 @@
 namespace moe {
 
 struct Entry {
-  int src;   // routed expert id (>= 0), or -(i+1) for shared expert i
-  int row0;  // first activation row (in h)
-  int m;     // tokens of this sub-group
-  int arow;  // first row of the phase-0 input box (x row or gathered-x row); phase 1 reads h at row0
+  int src;    // routed expert id (>= 0), or -(i+1) for shared expert i
+  int row0;   // first activation row (in h)
+  int m;      // tokens of this sub-group
+  int arow;   // first row of the phase-0 input box (x row or gathered-x row); phase 1 reads h at row0
+  int first;  // first entry of this group's sub-groups
+  int q;      // number of sub-groups of this group
 };
+
+// Job jj of a phase with T tiles per entry: the jobs of a group's q sub-groups
+// are the q·T consecutive jobs from first·T, ordered tile-major.
+MOE_DEV void job_entry(const Entry* plan, int jj, int T, int* entry, int* tile) {
+  const Entry& eg = plan[jj / T];
+  const int local = jj - eg.first * T;
+  *entry = eg.first + local % eg.q;
+  *tile = local / eg.q;
+}
 
 // Exclusive prefix sum over the block (one value per thread). Returns the
 // thread's offset; *total receives the sum. Uses scratch[0..warps].
@@ -65,7 +78,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   int nr = 0;
   if (a.engine == 0) {
     if (mine(1)) {
-      for (int p = tid; p < P; p += nt) plan[p] = Entry{a.topk_idx[p], p, 1, p / a.k};
+      for (int p = tid; p < P; p += nt) plan[p] = Entry{a.topk_idx[p], p, 1, p / a.k, p, 1};
       nr = P;
     }
     for (int p = tid; p < P; p += nt) {
@@ -89,7 +102,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
     const int pos = block_exclusive_scan(nsub, scratch, &nr);
     for (int q = 0; q < nsub; ++q) {
       const int rr = r0 + q * SUB;
-      plan[pos + q] = Entry{e, rr, min(SUB, m - q * SUB), rr};
+      plan[pos + q] = Entry{e, rr, min(SUB, m - q * SUB), rr, pos, nsub};
     }
     for (int r = tid; r < P; r += nt) {
       const int t = a.pair_tok[r], j = a.pair_slot[r];
@@ -101,7 +114,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   for (int q = tid; q < a.s * per; q += nt) {
     const int i = q / per, c = q - (q / per) * per;
     const int rr = P + i * a.n + c * SUB;
-    plan[nr + q] = Entry{-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB};
+    plan[nr + q] = Entry{-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB, nr + i * per, per};
   }
   for (int r = tid; r < a.s * a.n; r += nt) {
     const int i = r / a.n, t = r - (r / a.n) * a.n;

@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(kGateWarps * 32)
     gate_logits_kernel(int d, int E, int n, const float* __restrict__ x,
                        const float* __restrict__ wg, float* __restrict__ logits) {
   __shared__ float part[kGateWarps][kGateTokens][2];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x;
   const int t0 = blockIdx.y * kGateTokens;
@@ -114,6 +116,8 @@ constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
 __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_kernel(int E, int k, int n, const float* __restrict__ logits,
                 int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTopkWarps + warp;
   if (t >= n) return;
@@ -183,6 +187,8 @@ __global__ void __launch_bounds__(kUnionThreads)
   __shared__ int sidx[MOE_MAX_PAIRS];
   __shared__ int cnt[MOE_MAX_EXPERTS];
   __shared__ int start[MOE_MAX_EXPERTS];
+  pdl_wait();
+  pdl_trigger();
   const int P = n * k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
@@ -255,6 +261,8 @@ __global__ void __launch_bounds__(kUnionThreads)
 // ---------------------------------------------------------------- combine --
 __global__ void __launch_bounds__(256)
     combine_kernel(int d, int slots, const float* __restrict__ y_slot, float* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c4 * 4 >= d) return;
@@ -275,10 +283,12 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
                          float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
   dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
-  gate_logits_kernel<<<g1, kGateWarps * 32, 0, stream>>>(d, E, n, x, w_router, logits);
+  cudaError_t e = launch_pdl(gate_logits_kernel, g1, dim3(kGateWarps * 32), 0, stream, d, E, n, x,
+                             w_router, logits);
+  if (e != cudaSuccess) return e;
   dim3 g2((n + kTopkWarps - 1) / kTopkWarps);
-  topk_kernel<<<g2, kTopkWarps * 32, 0, stream>>>(E, k, n, logits, topk_idx, topk_w);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, g2, dim3(kTopkWarps * 32), 0, stream, E, k, n,
+                    static_cast<const float*>(logits), topk_idx, topk_w);
 }
 
 cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
@@ -286,17 +296,14 @@ cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
                          int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
                          uint64_t* bytes, unsigned int* err, cudaStream_t stream) {
   const uint64_t eb = 3ull * (uint64_t)d * (uint64_t)I * (uint64_t)wbytes;
-  union_kernel<<<1, kUnionThreads, 0, stream>>>(E, k, n, eb, s, topk_idx, union_ids,
-                                                union_count, offsets, pair_tok, pair_slot,
-                                                bytes, err);
-  return cudaGetLastError();
+  return launch_pdl(union_kernel, dim3(1), dim3(kUnionThreads), 0, stream, E, k, n, eb, s,
+                    topk_idx, union_ids, union_count, offsets, pair_tok, pair_slot, bytes, err);
 }
 
 cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,
                            cudaStream_t stream) {
   dim3 g((d / 4 + 255) / 256, n);
-  combine_kernel<<<g, 256, 0, stream>>>(d, slots, y_slot, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, g, dim3(256), 0, stream, d, slots, y_slot, y);
 }
 
 }  // namespace moe

@@ -10,7 +10,7 @@ import pytest
 from moe_expert_layer_warp_gb300 import api, build
 from moe_expert_layer_warp_gb300.configs import ALL, LayerShape, W_BF16
 
-CC_SYNC_INTS = 1 + 512 + 4 * 64   # CUDA-core kernel: job counter + per-entry tile counts
+CC_SYNC_INTS = 1 + 512 + 4 * 32   # CUDA-core kernel: job counter + per-entry tile counts
 MMA_SYNC_INTS = 1 + 512 + 4 * 4   # tensor-core kernel: job counter + per-entry tile counts
 HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
