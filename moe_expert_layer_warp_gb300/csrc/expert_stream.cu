@@ -40,7 +40,8 @@ namespace moe {
 namespace {
 
 constexpr int kConsumerWarps = 16;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + producer warp + publisher warp
+constexpr int kPubSlots = 8;                         // ring of finished phase-0 jobs
 constexpr int kRowChunks = 32;
 constexpr int kChunkBytes = 512;
 constexpr int kMaxM = kCcSub;
@@ -73,7 +74,7 @@ struct Layout {
   static constexpr int kXBytes = kMaxM * KS * 4;
   static constexpr int kStageBytes = kWBytes + kXBytes;
   static constexpr int kOffBar = kStages * kStageBytes;
-  static constexpr int kOffPlan = kOffBar + 2 * kStages * 8;
+  static constexpr int kOffPlan = kOffBar + (2 * kStages + 2 * kPubSlots) * 8;
   static constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
   static constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
   static constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
@@ -139,18 +140,25 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* empty = full + kStages;
+  uint64_t* pub_full = empty + kStages;    // consumer warps → publisher: a phase-0 job's h is stored
+  uint64_t* pub_empty = pub_full + kPubSlots;
   Entry* plan = reinterpret_cast<Entry*>(smem + L::kOffPlan);
   int* row_out = reinterpret_cast<int*>(smem + L::kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + L::kOffRowW);
   int* misc = reinterpret_cast<int*>(smem + L::kOffMisc);  // [0..31] scan scratch
   volatile int* stage_job = misc + 32;                     // [kStages]
   volatile int* abort_flag = misc + 48;
+  volatile int* pub_entry = misc + 52;                     // [kPubSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kPubSlots; ++i) {
+      mbar_init(&pub_full[i], kConsumerWarps);
+      mbar_init(&pub_empty[i], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -175,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   const int nks0 = (a.d + KS - 1) / KS, nks1 = (a.I + KS - 1) / KS;
   int* job_counter = a.sync;
   int* done0 = a.sync + 1;
-  const int done_target = T0 * kConsumerWarps;
+  const int done_target = T0;  // one publication per phase-0 tile
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------ producer thread --
@@ -281,6 +289,26 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     return;
   }
 
+  if (warp == kConsumerWarps + 1) {
+    // ---------------------------------------------------- publisher thread --
+    // Publishes each finished phase-0 job to the group's phase-1 jobs in other
+    // CTAs with a GPU-scope release, so that the consumer warps only ever pay
+    // a CTA-scope arrive. The consumers' h stores are ordered before their
+    // arrive (release, CTA scope); this thread's wait acquires them and its
+    // release reduction makes them visible GPU-wide before the count.
+    if (lane == 0) {
+      for (int pn = 0;; ++pn) {
+        const int ps = pn % kPubSlots;
+        if (!mbar_wait(&pub_full[ps], (uint32_t)((pn / kPubSlots) & 1), a.err, 0x251)) break;
+        const int e = pub_entry[ps];
+        if (e < 0) break;
+        red_release_add(done0 + e, 1);
+        mbar_arrive(&pub_empty[ps]);
+      }
+    }
+    return;
+  }
+
   // --------------------------------------------------------- consumer warps --
   // Warp w owns two weight rows of every stage: in phase 0 gate row w and up
   // row w of the 16-row tile (so h for row w is finished inside the warp), in
@@ -289,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   constexpr int NP = LM::NP;
   int stage = 0;
   uint32_t phase = 0;
+  int pub_n = 0;  // phase-0 jobs handed to the publisher so far
   for (;;) {
     if (!mbar_wait(&full[stage], phase, a.err, 0x220)) {
       *abort_flag = 1;
@@ -296,7 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     }
     if (*abort_flag) return;
     const int job = stage_job[stage];
-    if (job < 0) break;
+    if (job < 0) {
+      // end marker for the publisher
+      if (lane == 0) {
+        const int ps = pub_n % kPubSlots;
+        if (mbar_wait(&pub_empty[ps], (uint32_t)(((pub_n / kPubSlots) & 1) ^ 1), a.err, 0x252)) {
+          if (warp == 0) pub_entry[ps] = -1;
+          mbar_arrive(&pub_full[ps]);
+        }
+      }
+      break;
+    }
     const int ph = job < J0 ? 0 : 1;
     const int jj = ph == 0 ? job : job - J0;
     int g, tile;
@@ -352,10 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
 #pragma unroll
         for (int t = 0; t < kMaxM; ++t)
           if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(r[0][t]) * r[1][t];
-        // publish: a release reduction orders the h stores above before the
-        // count; the reader acquires the count and fences the async proxy
-        // before its TMA reads h.
-        red_release_add(done0 + g, 1);
+        // hand the finished job to the publisher thread (see above)
+        const int ps = pub_n % kPubSlots;
+        if (!mbar_wait(&pub_empty[ps], (uint32_t)(((pub_n / kPubSlots) & 1) ^ 1), a.err, 0x250)) {
+          *abort_flag = 1;
+        } else {
+          pub_entry[ps] = g;
+          mbar_arrive(&pub_full[ps]);
+        }
       } else {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -370,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         }
       }
     }
+    if (ph == 0) ++pub_n;
   }
 }
 
