@@ -57,7 +57,8 @@ static_assert(1 + kMaxEntries == kMmaSyncInts, "tensor-core kernel scratch size"
 static_assert(kSub == 32, "the epilogue and the TMEM slots assume at most 32 tokens");
 
 constexpr int kOffBar = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 4 + 1;       // full, empty, tfull[2], tempty[2], drain
+constexpr int kPubSlots = 8;                        // ring of finished phase-0 jobs
+constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots;  // full, empty, tfull, tempty, drain, pub
 constexpr int kOffPlan = kOffBar + kNumBars * 8;
 constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
 constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
@@ -87,6 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
+  uint64_t* pub_full = drain + 1;  // epilogue warps → publisher: a phase-0 job's h is stored
+  uint64_t* pub_empty = pub_full + kPubSlots;
   Entry* plan = reinterpret_cast<Entry*>(smem + kOffPlan);
   int* row_out = reinterpret_cast<int*>(smem + kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + kOffRowW);
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   volatile int* acc_job = misc + 24;                    // [2]
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(misc + 28);
   volatile int* abort_flag = misc + 32;
+  volatile int* pub_entry = misc + 36;                  // [kPubSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -107,6 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       mbar_init(&tempty[i], 4);
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < kPubSlots; ++i) {
+      mbar_init(&pub_full[i], 4);
+      mbar_init(&pub_empty[i], 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   const int nks0 = a.d / 64, nks1 = (a.I + 127) / 128;
   int* job_counter = a.sync_mma;
   int* done0 = a.sync_mma + 1;
-  const int done_target = T0 * 128;
+  const int done_target = T0;  // one publication per phase-0 tile
 
   if (warp == 0) {
     // ------------------------------------------------------ producer thread --
@@ -297,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     const int r_in = quad * 32 + lane;
     int slot = 0;
     uint32_t sphase = 0;
+    int pub_n = 0;  // phase-0 jobs handed to the publisher so far
     for (;;) {
       if (!mbar_wait(&tfull[slot], sphase, a.err, 0x330)) {
         *abort_flag = 1;
@@ -304,7 +313,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       }
       umma::fence_after_sync();
       const int job = acc_job[slot];
-      if (job < 0) break;
+      if (job < 0) {
+        // end marker for the publisher
+        if (lane == 0) {
+          const int ps = pub_n % kPubSlots;
+          if (mbar_wait(&pub_empty[ps], (uint32_t)(((pub_n / kPubSlots) & 1) ^ 1), a.err, 0x352)) {
+            if (warp == 2) pub_entry[ps] = -1;
+            mbar_arrive(&pub_full[ps]);
+          }
+        }
+        break;
+      }
       const int ph = job < J0 ? 0 : 1;
       const int jj = ph == 0 ? job : job - J0;
       int g, tile;
@@ -339,8 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             }
           }
         }
-        // publish this thread's h values to the group's phase-1 jobs
-        red_release_add(done0 + g, 1);
+        // hand the finished job to the publisher thread: __syncwarp orders the
+        // warp's h stores before lane 0's arrive (release, CTA scope)
+        __syncwarp();
+        if (lane == 0) {
+          const int ps = pub_n % kPubSlots;
+          if (!mbar_wait(&pub_empty[ps], (uint32_t)(((pub_n / kPubSlots) & 1) ^ 1), a.err, 0x350)) {
+            *abort_flag = 1;
+          } else {
+            if (warp == 2) pub_entry[ps] = g;
+            mbar_arrive(&pub_full[ps]);
+          }
+        }
+        ++pub_n;
       } else if (row < a.d) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -354,6 +384,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       if (++slot == 2) {
         slot = 0;
         sphase ^= 1u;
+      }
+    }
+  } else if (warp == 6) {
+    // ---------------------------------------------------- publisher thread --
+    // Publishes each finished phase-0 job to the group's phase-1 jobs with a
+    // GPU-scope release, so that the epilogue warps only pay a CTA-scope
+    // arrive; this thread's wait acquires their h stores and its release
+    // reduction makes them visible GPU-wide before the count.
+    if (lane == 0) {
+      for (int pn = 0;; ++pn) {
+        const int ps = pn % kPubSlots;
+        if (!mbar_wait(&pub_full[ps], (uint32_t)((pn / kPubSlots) & 1), a.err, 0x351)) break;
+        const int e = pub_entry[ps];
+        if (e < 0) break;
+        red_release_add(done0 + e, 1);
+        mbar_arrive(&pub_empty[ps]);
       }
     }
   }
