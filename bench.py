@@ -51,6 +51,9 @@ def parse_args():
                    help="profiling case WORKLOAD:ENGINE:N (e.g. v2lite:perslot:1): runs "
                         "--passes passes of one layer and prints their mean time")
     p.add_argument("--passes", type=int, default=4)
+    p.add_argument("--stack", action="store_true",
+                   help="26-layer V2-Lite stack: fit the step-time model on one layer run "
+                        "alone, predict the stack's passes and compare with measured ones")
     return p.parse_args()
 
 
@@ -113,6 +116,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ----------------------------------------------------------- across ranks --
+def max_over_ranks(x: float, dev) -> float:
+    """The largest of every rank's x (all ranks call it; one process: x)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_value(world: int, tokens_per_step: int, ms_step: float) -> float:
+    """Whole-job tokens/s: every rank processes tokens_per_step per step, and
+    the job's step takes the slowest rank's time."""
+    return world * tokens_per_step / (ms_step * 1e-3)
+
+
 # -------------------------------------------------------------- our engine --
 def build_workload(dev):
     import torch
@@ -147,7 +169,10 @@ def enqueue_step(w, runners, xs, step_idx, stream):
 
 
 def kernels_per_pass():
-    # moe_route: gate GEMV + top-k; moe_build_union: 1; engine: 2 phases; combine: 1
+    # moe_route: gate GEMV + top-k; moe_build_union: 1; expert call: prep + the
+    # CUDA-core kernel (the tensor-core kernel is not launched for this shape:
+    # 27 row tiles per expert and n <= 9 put every group below its threshold);
+    # moe_combine: 1
     return 2 + 1 + 2 + 1
 
 
@@ -228,24 +253,37 @@ def e2e_measure(w, runners, xs, steps, warmup):
     return ms, h2d, d2h
 
 
-def load_traffic(kernel_key: str):
-    """DRAM traffic per launch from a committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+TRAFFIC_SOURCES = ("expert_stream.cu", "engine.cu", "plan.cuh", "common.cuh", "launch.h")
+
+
+def kernel_source_hash() -> str:
+    """sha256 (first 16 hex digits) over the sources of the CUDA-core expert
+    kernel and its prep kernel."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        h.update(open(os.path.join(ROOT, "moe_expert_layer_warp_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(name: str):
+    """DRAM bytes per launch from a committed ncu summary (``key: value``
+    lines), if its counters were taken on the current kernel sources; else
+    None."""
+    path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
+    rec = {}
+    for line in open(path):
+        if ":" in line and not line.startswith((" ", "#")):
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("sources_sha256_16") != kernel_source_hash():
+        return None
     try:
-        rec = json.load(open(path)).get(kernel_key)
-    except ValueError:
+        return int(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
         return None
-    if not rec:
-        return None
-    src = os.path.join(ROOT, "moe_expert_layer_warp_gb300", "csrc", rec.get("source", ""))
-    if not os.path.exists(src):
-        return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return rec.get("bytes_per_launch") if h == rec.get("source_sha") else None
 
 
 def peaks():
@@ -346,14 +384,8 @@ def run_ours(args):
     e1.synchronize()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms_step = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-        dist.barrier()
-    value = world * tokens_per_step / (ms_step * 1e-3)
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    value = job_value(world, tokens_per_step, ms_step)
 
     st = api.moe_last_device_error()
     if st != api.MOE_OK:
@@ -363,6 +395,7 @@ def run_ours(args):
     samples, t_fix, pass_ms, alg_b, eng_ms = measure_breakdown(w, runners, xs)
     rep = stepmodel.build_report(samples, t_fix)
     e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     if rank != 0:
         return
@@ -396,12 +429,13 @@ def run_ours(args):
                          "consecutive passes read different replicas" % REPLICAS,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "timing": "CUDA-graph replay of each step, CUDA events on the stream"},
-        "roofline": {"kernel": "expert engine call (phase-0 up/gate + phase-1 down launches)",
+        "roofline": {"kernel": "expert_engine_kernel with its prep kernel (one expert call: "
+                               "up/gate and down of every group)",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": load_traffic("expert_engine_v2lite")},
+                     "traffic": load_traffic("traffic_expert_engine_v2lite_bench.txt")},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * tokens_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": round(job_value(world, tokens_per_step, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * 2 * len(w.pass_sizes) * kernels_per_pass(),
         "clocks": clk,
@@ -466,6 +500,125 @@ def run_reference(args):
     }), flush=True)
 
 
+STACK_DRAFT_COST_RATIO = 0.1601   # draft/verify cost ratio c the pages derive from FLOPs
+STACK_FIT_REPS = 4
+STACK_REPS = 3
+
+
+def run_stack(args):
+    """26 V2-Lite-shaped layers (~30 GB), each fed the same pass, at n = 1..9
+    and rho in {0, 0.5, 0.9, 0.99}. The bandwidths are fitted on layer 0's
+    expert call run alone (L2 flushed before each pass); the stack's pass time
+    is predicted from every layer's requested bytes over those bandwidths plus
+    the fixed time, and compared with the measured stack pass. Prints one
+    JSON line."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    from moe_expert_layer_warp_gb300 import api, configs, stepmodel, synth
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    w = configs.V2_LITE_STACK
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    layers = [synth.make_layer(w.shape, w.weight_seed + l, dev) for l in range(w.layers)]
+    runners = [PassRunner(L, max(w.pass_sizes)) for L in layers]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    xs = {(ri, n): torch.from_numpy(synth.make_pass(w.shape.d, n, rho,
+                                                    [w.x_seed_base + 100 * ri + n])).to(dev)
+          for ri, rho in enumerate(w.rhos) for n in w.pass_sizes}
+    engines = ("perslot", "dedup")
+
+    def req_bytes(R, eng):
+        b = [int(v) for v in R.bytes.cpu().tolist()]
+        return (b[0] if eng == "perslot" else b[1]) + b[2]
+
+    for (ri, n), x in xs.items():          # warm-up: every pass once through the stack
+        for eng in engines:
+            for R in runners:
+                R.forward(x, eng, stream)
+    torch.cuda.synchronize()
+    if api.moe_last_device_error() != api.MOE_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # fit on layer 0 run alone
+    R0 = runners[0]
+    samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
+    tfix = {n: [] for n in w.pass_sizes}
+    for rep in range(STACK_FIT_REPS):
+        for (ri, n), x in xs.items():
+            for eng in engines:
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                flush.zero_()
+                torch.cuda._sleep(SPIN_CYCLES)
+                ev[0].record(stream)
+                R0.route(x, stream)
+                R0.build_union(n, stream)
+                ev[1].record(stream)
+                R0.experts(x, eng, stream)
+                ev[2].record(stream)
+                R0.combine(n, stream)
+                ev[3].record(stream)
+                torch.cuda.synchronize()
+                t_exp = ev[1].elapsed_time(ev[2]) * 1e-3
+                samples[eng][n].append((req_bytes(R0, eng), t_exp))
+                tfix[n].append(ev[0].elapsed_time(ev[3]) * 1e-3 - t_exp)
+    t_fix = {n: statistics.median(v) for n, v in tfix.items()}
+    fits = {e: stepmodel.EngineFit({n: stepmodel.effective_bandwidth(
+        [b for b, _ in samples[e][n]], [t for _, t in samples[e][n]]) for n in w.pass_sizes},
+        t_fix) for e in engines}
+    eps = {e: {n: stepmodel.bandwidth_spread(samples[e][n]) for n in w.pass_sizes}
+           for e in engines}
+
+    # the stack: measured passes and their per-layer requested bytes
+    per_rho = []
+    for ri, rho in enumerate(w.rhos):
+        meas = {e: {} for e in engines}
+        pred = {e: {} for e in engines}
+        bound = {}
+        for n in w.pass_sizes:
+            x = xs[(ri, n)]
+            lb = {}
+            for eng in engines:
+                ts = []
+                for rep in range(STACK_REPS):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    torch.cuda._sleep(8 * SPIN_CYCLES)   # host queues the whole stack meanwhile
+                    e0.record(stream)
+                    for R in runners:
+                        R.forward(x, eng, stream)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e-3)
+                meas[eng][n] = statistics.median(ts)
+                lb[eng] = [req_bytes(R, eng) for R in runners]
+                pred[eng][n] = stepmodel.step_time(fits[eng], n, lb[eng])
+            bound[n] = stepmodel.saving_bound(sum(lb["perslot"]), fits["perslot"].bw[n],
+                                              eps["perslot"][n], sum(lb["dedup"]),
+                                              fits["dedup"].bw[n], eps["dedup"][n])
+        chk = stepmodel.StackCheck(list(w.pass_sizes), meas, pred, bound,
+                                   stepmodel.acceptance_grid(), STACK_DRAFT_COST_RATIO)
+        d = chk.as_dict()
+        d["rho"] = rho
+        per_rho.append(d)
+    if api.moe_last_device_error() != api.MOE_OK:
+        raise RuntimeError("device error in the stack passes")
+    print(json.dumps({
+        "stack": "deepseek-v2-lite-shaped 26-layer MoE stack (expert layers only, each fed "
+                 "the same pass), bf16 weights, %.1f GB of expert weights" % (
+                     w.layers * (w.shape.n_experts + w.shape.n_shared) * EXPERT_BYTES / 1e9),
+        "fit": {"layer": 0, "passes_per_point": STACK_FIT_REPS * len(w.rhos),
+                "l2": "flushed (256 MB write) before each fitted pass",
+                "bw_perslot_GBs": [round(fits["perslot"].bw[n] / 1e9, 1) for n in w.pass_sizes],
+                "bw_dedup_GBs": [round(fits["dedup"].bw[n] / 1e9, 1) for n in w.pass_sizes],
+                "eps_perslot": [round(eps["perslot"][n], 4) for n in w.pass_sizes],
+                "eps_dedup": [round(eps["dedup"][n], 4) for n in w.pass_sizes],
+                "t_fix_us": [round(t_fix[n] * 1e6, 2) for n in w.pass_sizes]},
+        "per_rho": per_rho,
+    }), flush=True)
+
+
 CASES = {"tiny": "TINY", "v2lite": "V2_LITE", "mixtral": "MIXTRAL", "v3": "V3"}
 
 
@@ -511,6 +664,8 @@ def main():
     args = parse_args()
     if args.case:
         run_case(args)
+    elif args.stack:
+        run_stack(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -183,6 +183,15 @@ moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_
 /* Size in bytes of the static scratch array of moe_verify_dedup_noalloc. */
 size_t moe_noalloc_scratch_limit(void);
 
+/* Failure-detection self-test (not part of the method): launches one kernel
+ * that waits on a shared-memory mbarrier nothing ever arrives on, through the
+ * same bounded wait every expert kernel uses, with a limit of limit_us
+ * microseconds (1 .. 1,000,000) instead of the kernels' 0.4 s. The wait
+ * expires, the kernel records a timeout in the device error word and
+ * returns; the context stays usable. A following moe_last_device_error on
+ * the same stream returns MOE_ETIMEOUT. MOE_EINVAL for a limit out of range. */
+moe_status moe_diag_bounded_wait(int32_t limit_us, void* stream);
+
 /* Synchronises `stream`, then reads and clears the library's device error
  * word: MOE_ETIMEOUT if a bounded device-side wait expired, MOE_EDEVICE if a
  * kernel recorded a failed check, MOE_ECUDA if the stream reports an error,

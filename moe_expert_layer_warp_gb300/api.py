@@ -23,7 +23,8 @@ MOE_MAX_TOKENS, MOE_MAX_PAIRS, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_MAX_SHARED = 1
 
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_build_union", "moe_verify_perslot",
             "moe_verify_dedup", "moe_combine", "moe_last_device_error", "moe_status_str",
-            "moe_last_cuda_error_string", "moe_verify_dedup_noalloc", "moe_noalloc_scratch_limit")
+            "moe_last_cuda_error_string", "moe_verify_dedup_noalloc", "moe_noalloc_scratch_limit",
+            "moe_diag_bounded_wait")
 
 
 class MoeError(RuntimeError):
@@ -77,12 +78,14 @@ def load(path: str = LIB_PATH):
     lib.moe_noalloc_scratch_limit.argtypes = []
     lib.moe_noalloc_scratch_limit.restype = SZ
     lib.moe_last_device_error.argtypes = [P]
+    lib.moe_diag_bounded_wait.argtypes = [I32, P]
     lib.moe_status_str.argtypes = [ctypes.c_int]
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_last_cuda_error_string.argtypes = []
     lib.moe_last_cuda_error_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_build_union", "moe_verify_perslot", "moe_verify_dedup",
-              "moe_combine", "moe_last_device_error", "moe_verify_dedup_noalloc"):
+              "moe_combine", "moe_last_device_error", "moe_verify_dedup_noalloc",
+              "moe_diag_bounded_wait"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -172,6 +175,10 @@ def moe_noalloc_scratch_limit() -> int:
 def moe_combine(desc, y_slot, n, y, stream=None):
     _check(load().moe_combine(ctypes.byref(desc), _ptr(y_slot), n, _ptr(y), _stream(stream)),
            "moe_combine")
+
+
+def moe_diag_bounded_wait(limit_us: int, stream=None):
+    _check(load().moe_diag_bounded_wait(limit_us, _stream(stream)), "moe_diag_bounded_wait")
 
 
 def moe_last_device_error(stream=None) -> int:

@@ -354,6 +354,15 @@ moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
 }
 
+moe_status moe_diag_bounded_wait(int32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return MOE_EINVAL;
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  cudaError_t e = moe::launch_diag_wait((unsigned long long)limit_us * 1000ull, di->err,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_diag_bounded_wait launch");
+}
+
 moe_status moe_last_device_error(void* stream) {
   DeviceInfo* di;
   MOE_TRY(device_info(&di));

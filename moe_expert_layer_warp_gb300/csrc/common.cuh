@@ -71,16 +71,21 @@ MOE_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed. Returns false
-// (and records ERR_TIMEOUT at `site`) if it did not complete within the limit.
-MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err, unsigned int site) {
+// (and records ERR_TIMEOUT at `site`) if it did not complete within limit_ns.
+MOE_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned int* err, unsigned int site,
+                           unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (unsigned int i = 0; i < kWaitLimitIters; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && global_ns() - t0 > kWaitLimitNs) break;
+    if ((i & 63u) == 63u && global_ns() - t0 > limit_ns) break;
   }
   report_error(err, ERR_TIMEOUT, site);
   return false;
+}
+
+MOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err, unsigned int site) {
+  return mbar_wait_for(bar, parity, err, site, kWaitLimitNs);
 }
 
 // ----------------------------------------------------------- bulk copies --

@@ -94,6 +94,9 @@ constexpr int kMmaSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKE
 // Tensor-core expert kernel (tcgen05 + TMEM) for groups of ≥ mma_min_m tokens.
 cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t stream);
 
+// Failure-detection self-test: a bounded mbarrier wait that expires.
+cudaError_t launch_diag_wait(unsigned long long limit_ns, unsigned int* err, cudaStream_t stream);
+
 // y[t] = Σ_j y_slot[t][j] over the k+s slots, in slot order.
 cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,
                            cudaStream_t stream);

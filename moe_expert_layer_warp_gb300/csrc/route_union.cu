@@ -278,7 +278,26 @@ __global__ void __launch_bounds__(256)
   reinterpret_cast<float4*>(y + (size_t)t * d)[c4] = acc;
 }
 
+// ------------------------------------------------------------ diagnostic --
+// Waits on an mbarrier that nothing arrives on, with the same bounded wait as
+// the expert kernels but a short limit: it records ERR_TIMEOUT and returns.
+__global__ void diag_wait_kernel(unsigned long long limit_ns, unsigned int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_for(&bar, 0, err, 0x900, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_diag_wait(unsigned long long limit_ns, unsigned int* err, cudaStream_t stream) {
+  diag_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
                          float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {

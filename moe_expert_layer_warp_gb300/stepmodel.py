@@ -232,3 +232,81 @@ def build_report(samples: Dict[str, Dict[int, List[tuple]]], t_fix: Dict[int, fl
         gamma_star_dd=staircase(al, interpolated(T_dd), t_draft, gmax),
         gamma_star_best=staircase(al, interpolated(T_best), t_draft, gmax),
         t_draft=t_draft)
+
+
+# ------------------------------------------------------------ stack check --
+def bandwidth_spread(samples: Sequence[tuple]) -> float:
+    """Relative spread ε of a fit: max over the fitted passes of
+    |b_i/s_i ÷ BW − 1|, BW = Σb/Σs. Used as the fit's bandwidth error."""
+    bw = effective_bandwidth([b for b, _ in samples], [s for _, s in samples])
+    return max(abs(b / s / bw - 1.0) for b, s in samples)
+
+
+def saving_bound(bytes_ps: float, bw_ps: float, eps_ps: float, bytes_dd: float, bw_dd: float,
+                 eps_dd: float) -> float:
+    """[A] how far a bandwidth error moves the predicted saving T_ps − T_dd.
+
+    Reading: if the true bandwidth of an engine lies in BW·[1−ε, 1+ε], its
+    byte time B/BW_true lies within B/BW · ε/(1−ε) of the prediction; the
+    fixed time is common to both engines and cancels in the saving, so the
+    saving moves by at most the sum of the two engines' moves."""
+    if not (0.0 <= eps_ps < 1.0 and 0.0 <= eps_dd < 1.0):
+        raise ValueError("bandwidth error must lie in [0, 1)")
+    return bytes_ps / bw_ps * eps_ps / (1.0 - eps_ps) + bytes_dd / bw_dd * eps_dd / (1.0 - eps_dd)
+
+
+def crossover_from_times(ns: Sequence[int], t_ps: Dict[int, float],
+                         t_dd: Dict[int, float]) -> Optional[int]:
+    """[A] the first pass size n ≥ 2 at which the dedup pass takes less time."""
+    for n in sorted(ns):
+        if n >= 2 and t_dd[n] < t_ps[n]:
+            return n
+    return None
+
+
+@dataclass
+class StackCheck:
+    """Predicted against measured stack passes at one hidden-state correlation."""
+    ns: List[int]
+    measured: Dict[str, Dict[int, float]]     # engine -> n -> seconds
+    predicted: Dict[str, Dict[int, float]]
+    bound: Dict[int, float]                   # n -> saving bound (seconds)
+    alphas: List[float]
+    draft_cost_ratio: float
+
+    def saving(self, which: str) -> Dict[int, float]:
+        t = self.measured if which == "measured" else self.predicted
+        return {n: t["perslot"][n] - t["dedup"][n] for n in self.ns}
+
+    def inside_bound(self) -> Dict[int, bool]:
+        sm_, sp = self.saving("measured"), self.saving("predicted")
+        return {n: abs(sm_[n] - sp[n]) <= self.bound[n] for n in self.ns}
+
+    def gamma_star(self, which: str) -> List[int]:
+        """γ*(α) over the grid with the faster engine at each n; a drafted
+        token costs draft_cost_ratio × the n = 1 pass."""
+        t = self.measured if which == "measured" else self.predicted
+        best = {n: min(t["perslot"][n], t["dedup"][n]) for n in self.ns}
+        return staircase(self.alphas, interpolated(best), self.draft_cost_ratio * best[1],
+                         max(self.ns) - 1)
+
+    def as_dict(self) -> dict:
+        gm, gp = self.gamma_star("measured"), self.gamma_star("predicted")
+        ins = self.inside_bound()
+        us = lambda d: [round(d[n] * 1e6, 2) for n in self.ns]  # noqa: E731
+        return {
+            "n": self.ns,
+            "measured_us": {e: us(self.measured[e]) for e in ("perslot", "dedup")},
+            "predicted_us": {e: us(self.predicted[e]) for e in ("perslot", "dedup")},
+            "saving_measured_us": us(self.saving("measured")),
+            "saving_predicted_us": us(self.saving("predicted")),
+            "saving_bound_us": us(self.bound),
+            "saving_inside_bound": sum(ins.values()), "points": len(self.ns),
+            "crossover_measured": crossover_from_times(self.ns, self.measured["perslot"],
+                                                       self.measured["dedup"]),
+            "crossover_predicted": crossover_from_times(self.ns, self.predicted["perslot"],
+                                                        self.predicted["dedup"]),
+            "draft_cost_ratio": self.draft_cost_ratio,
+            "gamma_star_measured": gm, "gamma_star_predicted": gp,
+            "gamma_star_within_one": sum(abs(a - b) <= 1 for a, b in zip(gm, gp)),
+        }

@@ -11,6 +11,7 @@ import json
 import os
 import random
 
+import numpy as np
 import pytest
 
 from moe_expert_layer_warp_gb300 import stepmodel as sm
@@ -123,3 +124,56 @@ def test_build_report_end_to_end():
     assert rep.u_bar[n_star] < rep.r[n_star]
     assert all(not (rep.u_bar[n] < rep.r[n]) for n in range(2, n_star))
     assert len(rep.gamma_star_best) == 22
+
+
+def test_bandwidth_spread():
+    assert sm.bandwidth_spread([(5.0, 1.0), (10.0, 2.0)]) == 0.0
+    # rates 100 and 300 over equal time: BW = 200, spread 0.5
+    assert sm.bandwidth_spread([(100.0, 1.0), (300.0, 1.0)]) == pytest.approx(0.5)
+
+
+def test_saving_bound_holds_for_every_bandwidth_in_range():
+    """Brute force over true bandwidths inside BW·[1−ε, 1+ε]: the saving's
+    move never exceeds the bound, and the worst corner reaches most of it."""
+    B_ps, bw_ps, e_ps = 3.0e9, 6.0e12, 0.08
+    B_dd, bw_dd, e_dd = 1.2e9, 4.5e12, 0.15
+    bound = sm.saving_bound(B_ps, bw_ps, e_ps, B_dd, bw_dd, e_dd)
+    pred = B_ps / bw_ps - B_dd / bw_dd
+    worst = 0.0
+    for a in np.linspace(1 - e_ps, 1 + e_ps, 41):
+        for b in np.linspace(1 - e_dd, 1 + e_dd, 41):
+            worst = max(worst, abs(B_ps / (bw_ps * a) - B_dd / (bw_dd * b) - pred))
+    assert worst <= bound * (1 + 1e-12)
+    assert worst >= 0.75 * bound
+    assert sm.saving_bound(B_ps, bw_ps, 0.0, B_dd, bw_dd, 0.0) == 0.0
+    with pytest.raises(ValueError):
+        sm.saving_bound(B_ps, bw_ps, 1.0, B_dd, bw_dd, 0.0)
+
+
+def test_crossover_from_times():
+    ns = list(range(1, 6))
+    t_ps = {n: 10.0 * n for n in ns}
+    t_dd = {n: 30.0 + 4.0 * n for n in ns}       # equal at n = 5: never strictly faster
+    assert sm.crossover_from_times(ns, t_ps, t_dd) is None
+    t_dd = {n: 12.0 + 5.0 * n for n in ns}       # n = 2: 22 > 20; n = 3: 27 < 30
+    assert sm.crossover_from_times(ns, t_ps, t_dd) == 3
+    # n = 1 never counts, even when dedup is faster there
+    assert sm.crossover_from_times([1, 2], {1: 2.0, 2: 1.0}, {1: 1.0, 2: 3.0}) is None
+
+
+def test_stack_check_agrees_with_itself_and_counts_misses():
+    ns = list(range(1, 10))
+    meas = {"perslot": {n: 100e-6 + 50e-6 * n for n in ns},
+            "dedup": {n: 110e-6 + 30e-6 * n for n in ns}}
+    bound = {n: 2e-6 for n in ns}
+    chk = sm.StackCheck(ns, meas, meas, bound, sm.acceptance_grid(), 0.1601)
+    d = chk.as_dict()
+    assert d["saving_inside_bound"] == 9
+    assert d["crossover_measured"] == d["crossover_predicted"] == 2
+    assert d["gamma_star_within_one"] == 22
+    assert d["gamma_star_measured"] == sorted(d["gamma_star_measured"])
+    # predictions off by 5 µs on dedup at n = 4: that point leaves the bound
+    pred = {"perslot": dict(meas["perslot"]), "dedup": dict(meas["dedup"])}
+    pred["dedup"][4] += 5e-6
+    chk = sm.StackCheck(ns, meas, pred, bound, sm.acceptance_grid(), 0.1601)
+    assert chk.as_dict()["saving_inside_bound"] == 8
