@@ -102,7 +102,10 @@ typedef struct {
  * for passes of up to n_max tokens. 0 on invalid arguments. The workspace is
  * caller-owned, 256-byte aligned, needs no initialisation, and may be reused
  * by consecutive calls on one stream; two calls that overlap on the device
- * must not share one.                                                       */
+ * must not share one. For bf16 layers it includes a fixed 24 MiB region of
+ * partial sums: when a pass has too few weight tiles to keep every SM busy,
+ * the engine cuts each tile's reduction into pieces and adds the pieces'
+ * partial sums in a fixed order (results do not depend on scheduling).     */
 size_t moe_workspace_bytes(const moe_layer_desc* desc, int32_t n_max);
 
 /* Gate GEMV, top-k and renormalised softmax
@@ -164,7 +167,7 @@ moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t 
  * memory and hands it only input and output buffers, or a latency-critical
  * serving loop where a device allocation, with its implicit synchronisation,
  * is not allowed after start-up. This entry point takes no workspace: its
- * scratch is a fixed array of moe_noalloc_scratch_limit() bytes (8 MiB)
+ * scratch is a fixed array of moe_noalloc_scratch_limit() bytes (32 MiB)
  * inside the library, which every GPU that loads the library keeps until the
  * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - Same arguments, outputs and numerics as moe_verify_dedup, minus the

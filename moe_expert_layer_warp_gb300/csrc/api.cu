@@ -82,9 +82,10 @@ moe_status check_n(const moe_layer_desc* d, int32_t n) {
 //   xg16     [2][n_max·k][d] bf16     their hi and lo bf16 halves
 //   x16      [2][n_max][d] bf16       hi and lo bf16 halves of x
 //   sync     [kCcSyncInts] int32      CUDA-core kernel job counter, group counts
-//   sync_mma [kMmaSyncInts] int32     tensor-core kernel job counter, group counts
+//   sync_mma [kMmaSyncInts] int32     tensor-core kernel job counter, group counts, piece counts
+//   part     [kMmaPartBytes]           tensor-core kernel partial sums of K pieces (bf16 layers)
 struct WsLayout {
-  size_t logits, h, h16, xg, xg16, x16, sync, sync_mma, total;
+  size_t logits, h, h16, xg, xg16, x16, sync, sync_mma, part, part_bytes, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -110,27 +111,26 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   off = align256(off + (size_t)moe::kCcSyncInts * 4);
   L.sync_mma = off;
   off = align256(off + (size_t)moe::kMmaSyncInts * 4);
+  L.part = off;
+  L.part_bytes = d->wdtype == MOE_W_BF16 ? moe::kMmaPartBytes : 0;
+  off = align256(off + L.part_bytes);
   L.total = off;
   return L;
 }
 
 // Smallest group (tokens) that runs on the tensor-core kernel (bf16 weights).
-// That kernel works in 128-row tiles of an expert (one job each, gate/up and
-// down); it pays off when its jobs fill the GPU. An expert with at least 64
-// such tiles (Mixtral- or DeepSeek-V3-shaped) gives enough work from groups of
-// 3 tokens; smaller experts (DeepSeek-V2-Lite-shaped: 27 tiles) stay on the
-// CUDA-core kernel, which reads a group's sub-groups tile by tile so that L2
-// serves the repeats, up to 16 tokens. MOE_MMA_MIN_M in the environment
-// overrides the choice (read once; for tuning).
-int mma_min_m(const moe_layer_desc* d) {
+// Every bf16 group goes there: its weights pass from HBM through shared
+// memory into the tensor cores with no per-element instruction, and its jobs
+// are cut along K until they fill the GPU, so it streams at the same rate
+// for one token as for 32. MOE_MMA_MIN_M in the environment (read once; for
+// tuning) sends groups below that size to the CUDA-core kernel instead.
+int mma_min_m(const moe_layer_desc*) {
   static const int forced = [] {
     const char* e = getenv("MOE_MMA_MIN_M");
     const int x = e ? atoi(e) : 0;
-    return x >= 2 ? x : 0;
+    return x >= 1 ? x : 0;
   }();
-  if (forced) return forced;
-  const int tiles = (d->inter + 127) / 128 + (d->d + 127) / 128;
-  return tiles >= 64 ? 3 : 17;
+  return forced ? forced : 1;
 }
 
 moe_status check_ws(const moe_layer_desc* d, int32_t n, const void* ws, size_t ws_bytes) {
@@ -251,6 +251,8 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.x16lo = a.x16 + (size_t)n * desc->d;
   a.sync = reinterpret_cast<int*>(ws + L.sync);
   a.sync_mma = reinterpret_cast<int*>(ws + L.sync_mma);
+  a.part = reinterpret_cast<float*>(ws + L.part);
+  a.part_bytes = L.part_bytes;
   // fp32 weights never go to the tensor cores (a tf32 product would miss the
   // fp32 tolerance), so every fp32 group stays on the CUDA-core kernel.
   a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m(desc) : 0x7fffffff;
@@ -291,7 +293,7 @@ moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights*
 }  // extern "C"
 
 namespace {
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 struct NoAllocSlot {

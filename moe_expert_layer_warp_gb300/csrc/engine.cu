@@ -17,7 +17,7 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
 
 // Runs right before the expert kernels and lets them launch as soon as it
 // starts (programmatic dependent launch); they wait for it before touching
-// its outputs. Block 0 zeroes both kernels' job counters and group counts.
+// its outputs. The grid zeroes both kernels' job counters and group counts.
 // Blocks [0, gather_rows): xg[r] = x[pair_tok[r]] (fp32) and its bf16 hi/lo
 // halves (dedup, union order). Blocks [gather_rows, gather_rows + n): the
 // bf16 hi/lo halves of x. hi = bf16(v), lo = bf16(v − hi).
@@ -29,9 +29,11 @@ __global__ void __launch_bounds__(256)
                        int* __restrict__ sync_cc, int* __restrict__ sync_mma) {
   pdl_wait();     // the union (dedup) or routing that precedes it
   pdl_trigger();
-  if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < kCcSyncInts; i += blockDim.x) sync_cc[i] = 0;
-    for (int i = threadIdx.x; i < kMmaSyncInts; i += blockDim.x) sync_mma[i] = 0;
+  {  // counters, spread over the grid (int4 stores; both regions are 256-byte aligned)
+    const int nt = gridDim.x * blockDim.x, t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int4 z = make_int4(0, 0, 0, 0);
+    for (int i = t; i < (kCcSyncInts + 3) / 4; i += nt) reinterpret_cast<int4*>(sync_cc)[i] = z;
+    for (int i = t; i < (kMmaSyncInts + 3) / 4; i += nt) reinterpret_cast<int4*>(sync_mma)[i] = z;
   }
   const int b = blockIdx.x;
   const float* src;
@@ -65,19 +67,22 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   const int gather = a.engine == 1 ? a.n * a.k : 0;
   const int convert = a.wdtype == 1 ? a.n : 0;
-  cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + convert, 1)), dim3(256), 0,
+  cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + convert, 4)), dim3(256), 0,
                              stream, a.d, convert, gather, a.x, a.pair_tok, a.xg, a.xg16,
                              a.xg16lo, a.x16, a.x16lo, a.sync, a.sync_mma);
   if (e != cudaSuccess) return e;
   // The tensor-core kernel runs only where a group can reach mma_min_m
   // tokens: a group never holds more than the pass's n tokens, and per-slot
-  // routed groups hold one, so per-slot needs shared experts for it.
-  const bool mma = a.wdtype == 1 && a.n >= a.mma_min_m && (a.engine == 1 || a.s > 0);
+  // routed groups hold one. The CUDA-core kernel runs unless every group
+  // goes to the tensor cores (mma_min_m ≤ 1).
+  const bool mma = a.wdtype == 1 && a.n >= a.mma_min_m &&
+                   (a.engine == 1 || a.s > 0 || a.mma_min_m <= 1);
+  const bool cc = !(mma && a.mma_min_m <= 1);
   ExpertArgs b = a;
   b.cc_waits_prep = mma ? 0 : 1;
   if (mma) {
     e = launch_expert_mma(b, num_sms, stream);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || !cc) return e;
   }
   return launch_expert_cc(b, num_sms, stream);
 }

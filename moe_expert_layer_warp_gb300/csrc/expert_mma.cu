@@ -1,33 +1,47 @@
-// expert_mma.cu — the expert FFNs of groups that many tokens share, on the
-// 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM), weights
-// streamed from HBM by TMA once per group.
+// expert_mma.cu — the expert FFNs of a verification pass on the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM), every
+// weight tile streamed from HBM by TMA once per group.
 //
 // Sources: "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
-// Kernel Bandwidth and the Best Draft Length", abstract — the deduplicating
-// engine reads each selected expert once per pass for all the tokens that
-// chose it; "Deep Dive into Mixture of Experts: From 1991 to DeepSeek-V3", §2
-// and §5 (weighted routed experts, unweighted shared experts). Each expert is
-// W_down(silu(W_gate x) ⊙ W_up x).
+// Kernel Bandwidth and the Best Draft Length", abstract — the per-slot engine
+// reads a selected expert once per token, the deduplicating engine reads it
+// once per pass for all the tokens that chose it; "Deep Dive into Mixture of
+// Experts: From 1991 to DeepSeek-V3", §2 and §5 (weighted routed experts,
+// unweighted shared experts). Each expert is W_down(silu(W_gate x) ⊙ W_up x).
 //
-// Once a group holds several tokens, its FFN is a dense contraction
+// A group's FFN is a contraction over its tokens
 //   H[tokens][I] = silu(X·W_gateᵀ) ⊙ (X·W_upᵀ),   Y[tokens][d] = H·W_downᵀ,
-// computed here as D = W·Xᵀ with the weights as the A operand (M = 128 weight
-// rows per tile) and the group's tokens as B (N = 16 or 32, sub-groups of at
-// most 32 tokens), fp32 accumulation. The weights are bf16 exactly; each fp32
+// computed as D = W·Xᵀ with the weights as the A operand (M = 128 weight rows
+// per tile) and the group's tokens as B, fp32 accumulation. With one to a few
+// tokens the tensor cores idle most of the time; what matters is that the
+// weights flow from HBM to shared memory to the tensor core with no
+// per-element instruction. The weights are bf16 exactly; each fp32
 // activation is split as hi + lo, both bf16 (hi = bf16(v), lo = bf16(v − hi)),
-// and both halves are multiplied into the same accumulator, so activations
-// keep ~16 more mantissa bits than a single bf16 rounding would. Phase 0
-// (gate and up, a 64-column K-step per stage, two accumulators) writes h as
-// its hi/lo halves; phase 1 (down, two K-steps per stage) writes the weighted
-// slot outputs. A phase-1
-// job loads its group's h only after every phase-0 tile of the group is
-// stored (counted in scratch, bounded acquire wait).
+// so activations keep ~16 more mantissa bits than one bf16 rounding. The two
+// halves are separate columns of one B tile — rows [0, h) the tokens' hi
+// halves, rows [h, 2h) their lo halves, h = 8, 16 or 32 ≥ the group's tokens,
+// N = 2h — so one MMA per K-step covers both, and the epilogue adds column t
+// and column h + t. Phase 0 (gate and up, one 64-column K-step per stage, two
+// accumulators) writes h as its hi/lo halves; phase 1 (down, two K-steps per
+// stage) writes the weighted slot outputs.
+//
+// Jobs. A job is (entry, 128-row tile, piece of K). When a phase has fewer
+// tiles than a few per CTA, each tile is cut into S ≤ 8 pieces along K so
+// that every SM streams. Every piece stores its fp32 partial sums and counts
+// itself with a release reduction (nothing waits for it); the CTA that runs
+// a tile's last piece hands the tile to its finisher warp, which waits
+// (bounded) until all pieces are counted, adds them in piece order — a fixed
+// order, so results are reproducible — and finishes the tile off the tensor
+// pipeline's path. A phase-1 job loads its group's h only after every
+// phase-0 tile of the group is stored (a count in scratch, bounded acquire
+// wait).
 //
 // Warp roles (one CTA per SM, persistent, jobs from a global counter):
 //   warp 0    TMA producer (one thread),
 //   warp 1    TMEM owner and MMA issuer (one thread), two accumulator slots,
-//   warps 2-5 epilogue: TMEM → registers → SwiGLU or weighting → global,
-//   warps 6-7 only help build the group table.
+//   warps 2-5 epilogue: TMEM → registers → partials / SwiGLU / weighting → global,
+//   warp 6    publisher of phase-0 tiles finished by the epilogue (GPU-scope release),
+//   warp 7    finisher of tiles cut into pieces.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -46,35 +60,66 @@ constexpr int kSub = kMmaSub;                       // tokens per entry (≤ MMA
 constexpr int kStages = 4;
 constexpr int kThreads = 256;
 constexpr int kTileBytes = kM * 128;                // [128 rows][64 bf16]
-constexpr int kBTileBytes = kSub * 128;             // [32 rows][64 bf16]
-// stage: two weight tiles, then up to four token tiles (hi/lo × one or two K-steps)
-constexpr int kStageBytes = 2 * kTileBytes + 4 * kBTileBytes;
+constexpr int kBStepBytes = 2 * kSub * 128;         // one K-step of tokens: [2h ≤ 64 rows][64 bf16]
+// stage: two weight tiles, then the token tiles of one or two K-steps
+constexpr int kStageBytes = 2 * kTileBytes + 2 * kBStepBytes;
 constexpr int kMaxEntries = max_entries(kSub);
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
-constexpr int kSlotCols = 64;                       // TMEM columns per accumulator slot
+constexpr int kSlotCols = 128;                      // TMEM columns per accumulator slot (gate, up)
 constexpr int kTmemCols = 2 * kSlotCols;
-static_assert(1 + kMaxEntries == kMmaSyncInts, "tensor-core kernel scratch size");
+constexpr int kJobsPerCta = 4;                      // pieces are cut until a phase has this many jobs per CTA
+constexpr int kMaxPieces = 8;
+static_assert(kMaxEntries == kMmaEntries, "tensor-core kernel entry count");
 static_assert(kSub == 32, "the epilogue and the TMEM slots assume at most 32 tokens");
 
 constexpr int kOffBar = kStages * kStageBytes;
 constexpr int kPubSlots = 8;                        // ring of finished phase-0 jobs
-constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots;  // full, empty, tfull, tempty, drain, pub
+constexpr int kFinSlots = 32;                       // ring of tiles to finish
+constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots + 2 * kFinSlots;
 constexpr int kOffPlan = kOffBar + kNumBars * 8;
 constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
 constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
 constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
-constexpr int kSmemBytes = kOffMisc + 64 * 4 + 1024;  // + slack to align the base to 1024
+constexpr int kSmemBytes = kOffMisc + 128 * 4 + 1024;  // + slack to align the base to 1024
+
+// Token tensors read as B, each with boxes of 64 columns × h rows for
+// h = 8, 16, 32: routed-group inputs (x gathered in union order, or x for
+// per-slot), shared-expert inputs (x), phase-1 inputs (h), hi and lo halves.
+enum { kXA, kXALo, kXS, kXSLo, kHH, kHLo, kNumB };
 
 struct Maps {
   CUtensorMap wg, wu, wd, swg, swu, swd;  // [E or s][rows][K] bf16, box 64 × 128 × 1
-  CUtensorMap xa, xs, h;                  // hi halves [rows][K] bf16, box 64 × 32
-  CUtensorMap xa_lo, xs_lo, h_lo;         // lo halves, same shapes
+  CUtensorMap b[3][kNumB];                // [h = 8, 16, 32][tensor]
 };
+
+// Rows h of a group's B tile half for m tokens, and its index in Maps::b.
+MOE_DEV int b_rows(int m) { return m <= 8 ? 8 : (m <= 16 ? 16 : 32); }
+MOE_DEV int b_index(int h) { return h == 8 ? 0 : (h == 16 ? 1 : 2); }
 
 struct Params {
   Maps maps;
   ExpertArgs a;
 };
+
+// How one phase is cut: T tiles per entry, nks K-steps per tile, S pieces of
+// kc K-steps (the last may be shorter).
+struct Cut {
+  int T, nks, S, kc;
+};
+
+// Pieces per tile for `tiles` (entry, tile) pairs: enough for kJobsPerCta
+// jobs per CTA, at most one per K-step, within the partial-sum scratch and
+// the arrival counts; then every piece non-empty.
+MOE_DEV Cut make_cut(int T, int nks, int tiles, int target, size_t budget, size_t slab_bytes) {
+  Cut c{T, nks, 1, nks};
+  if (tiles <= 0 || tiles >= target || 4 * tiles > kMmaCntInts) return c;
+  int S = min(min((target + tiles - 1) / tiles, nks), kMaxPieces);
+  while (S > 1 && (size_t)tiles * S * slab_bytes > budget) --S;
+  if (S <= 1) return c;
+  c.kc = (nks + S - 1) / S;
+  c.S = (nks + c.kc - 1) / c.kc;
+  return c;
+}
 
 MOE_DEV uint16_t to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
@@ -88,8 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint64_t* pub_full = drain + 1;  // epilogue warps → publisher: a phase-0 job's h is stored
+  uint64_t* pub_full = drain + 1;  // epilogue warps → publisher: a phase-0 job's quarters
   uint64_t* pub_empty = pub_full + kPubSlots;
+  uint64_t* fin_full = pub_empty + kPubSlots;  // epilogue → finisher: a tile's last piece is stored
+  uint64_t* fin_empty = fin_full + kFinSlots;
   Entry* plan = reinterpret_cast<Entry*>(smem + kOffPlan);
   int* row_out = reinterpret_cast<int*>(smem + kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + kOffRowW);
@@ -99,6 +146,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(misc + 28);
   volatile int* abort_flag = misc + 32;
   volatile int* pub_entry = misc + 36;                  // [kPubSlots]
+  int* pub_cnt = misc + 44;                             // [kPubSlots] quarters finished
+  int* max_m = misc + 52;
+  volatile int* fin_job = misc + 64;                    // [kFinSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -114,8 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     for (int i = 0; i < kPubSlots; ++i) {
       mbar_init(&pub_full[i], 4);
       mbar_init(&pub_empty[i], 1);
+      pub_cnt[i] = 0;
+    }
+    for (int i = 0; i < kFinSlots; ++i) {
+      mbar_init(&fin_full[i], 1);
+      mbar_init(&fin_empty[i], 1);
     }
     *abort_flag = 0;
+    *max_m = 0;
     fence_mbar_init();
   }
   if (warp == 1) umma::tmem_alloc(tmem_base, kTmemCols);
@@ -123,25 +179,44 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     prefetch_tmap(&prm.maps.wg);
     prefetch_tmap(&prm.maps.wu);
     prefetch_tmap(&prm.maps.wd);
-    prefetch_tmap(&prm.maps.xa);
-    prefetch_tmap(&prm.maps.h);
+    prefetch_tmap(&prm.maps.b[0][kXA]);
+    prefetch_tmap(&prm.maps.b[0][kHH]);
   }
   const int n_groups = build_plan<kSub, true>(a, plan, row_out, row_w, misc);
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_groups; i += blockDim.x) atomicMax(max_m, plan[i].m);
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
   pdl_wait();     // prep kernel's outputs
-  // The CUDA-core kernel may start now, on SMs this kernel leaves free: it
-  // needs nothing from this kernel, and the prep kernel is complete.
+  // The CUDA-core kernel, if it runs, may start now on SMs this kernel leaves
+  // free: it needs nothing from this kernel, and the prep kernel is complete.
   pdl_trigger();
   const uint32_t tmem = *tmem_base;
 
-  const int T0 = (a.I + kM - 1) / kM, T1 = (a.d + kM - 1) / kM;
-  const int J0 = n_groups * T0, J = J0 + n_groups * T1;
-  const int nks0 = a.d / 64, nks1 = (a.I + 127) / 128;
+  // Partial sums: slabs of [2 (gate, up) or 1][npad tokens][128 rows] fp32.
+  const int npad = *max_m <= 16 ? 16 : 32;
+  const size_t slab0 = (size_t)2 * npad * kM, slab1 = (size_t)npad * kM;  // floats
+  const size_t budget0 = a.part_bytes / 3 * 2, budget1 = a.part_bytes - budget0;
+  float* part0 = a.part;
+  float* part1 = a.part + budget0 / 4;
+  const int target = kJobsPerCta * (int)gridDim.x;
+  const Cut c0 = make_cut((a.I + kM - 1) / kM, a.d / 64, n_groups * ((a.I + kM - 1) / kM), target,
+                          budget0, slab0 * 4);
+  const Cut c1 = make_cut((a.d + kM - 1) / kM, (a.I + 127) / 128,
+                          n_groups * ((a.d + kM - 1) / kM), target, budget1, slab1 * 4);
+  const int J0 = n_groups * c0.T * c0.S, J = J0 + n_groups * c1.T * c1.S;
   int* job_counter = a.sync_mma;
   int* done0 = a.sync_mma + 1;
-  const int done_target = T0;  // one publication per phase-0 tile
+  int* cnt0 = a.sync_mma + 1 + kMmaEntries;
+  int* cnt1 = cnt0 + kMmaCntInts;
+  const int done_target = 4 * c0.T;  // four per phase-0 tile (one per quarter, or 4 at once)
+
+  auto decode = [&](int job, int* ph, int* g, int* tile, int* piece) {
+    *ph = job < J0 ? 0 : 1;
+    const Cut& c = *ph == 0 ? c0 : c1;
+    job_decode(plan, *ph == 0 ? job : job - J0, c.T, c.S, g, tile, piece);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------ producer thread --
@@ -162,15 +237,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           }
           break;
         }
-        const int ph = job < J0 ? 0 : 1;
-        const int jj = ph == 0 ? job : job - J0;
-        int g, tile;
-        job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile);
+        int ph, g, tile, piece;
+        decode(job, &ph, &g, &tile, &piece);
         const Entry en = plan[g];
         const bool sh = en.src < 0;
         const int ec = sh ? -en.src - 1 : en.src;
-        const int nks = ph == 0 ? nks0 : nks1;
-        for (int ks = 0; ks < nks && ok; ++ks) {
+        const int hb = b_rows(en.m);
+        const CUtensorMap* bm = prm.maps.b[b_index(hb)];
+        const uint32_t bbytes = hb * 128;  // one half (hi or lo) of one K-step
+        const Cut& c = ph == 0 ? c0 : c1;
+        const int ks_end = min(c.nks, (piece + 1) * c.kc);
+        for (int ks = piece * c.kc; ks < ks_end && ok; ++ks) {
           if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x300)) {
             *abort_flag = 1;
             ok = false;
@@ -178,32 +255,34 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           }
           unsigned char* st = smem + stage * kStageBytes;
           unsigned char* bt = st + 2 * kTileBytes;
-          if (ks == 0) stage_job[stage] = job;
+          if (ks == piece * c.kc) stage_job[stage] = job;
           if (ph == 0) {
             const int k0 = ks * 64;
-            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * kBTileBytes);
+            const CUtensorMap* xh = &bm[sh ? kXS : kXA];
+            const CUtensorMap* xl = &bm[sh ? kXSLo : kXALo];
+            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * bbytes);
             tma_load_3d(st, sh ? &prm.maps.swg : &prm.maps.wg, k0, tile * kM, ec, &full[stage], pol_w);
             tma_load_3d(st + kTileBytes, sh ? &prm.maps.swu : &prm.maps.wu, k0, tile * kM, ec,
                         &full[stage], pol_w);
-            tma_load_2d(bt, sh ? &prm.maps.xs : &prm.maps.xa, k0, en.arow, &full[stage], pol_x);
-            tma_load_2d(bt + kBTileBytes, sh ? &prm.maps.xs_lo : &prm.maps.xa_lo, k0, en.arow,
-                        &full[stage], pol_x);
+            tma_load_2d(bt, xh, k0, en.arow, &full[stage], pol_x);
+            tma_load_2d(bt + bbytes, xl, k0, en.arow, &full[stage], pol_x);
           } else {
             const int k0 = ks * 128;
             const CUtensorMap* wd = sh ? &prm.maps.swd : &prm.maps.wd;
-            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 4 * kBTileBytes);
+            const CUtensorMap* hh = &bm[kHH];
+            const CUtensorMap* hl = &bm[kHLo];
+            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 4 * bbytes);
             tma_load_3d(st, wd, k0, tile * kM, ec, &full[stage], pol_w);
             tma_load_3d(st + kTileBytes, wd, k0 + 64, tile * kM, ec, &full[stage], pol_w);
-            if (ks == 0) {
+            if (ks == piece * c.kc) {
               // the group's h rows must all be stored before they are read
               if (!wait_count(done0 + g, done_target, a.err, 0x340)) *abort_flag = 1;
               fence_proxy_async_global();
             }
-            tma_load_2d(bt, &prm.maps.h, k0, en.row0, &full[stage], pol_x);
-            tma_load_2d(bt + kBTileBytes, &prm.maps.h_lo, k0, en.row0, &full[stage], pol_x);
-            tma_load_2d(bt + 2 * kBTileBytes, &prm.maps.h, k0 + 64, en.row0, &full[stage], pol_x);
-            tma_load_2d(bt + 3 * kBTileBytes, &prm.maps.h_lo, k0 + 64, en.row0, &full[stage],
-                        pol_x);
+            tma_load_2d(bt, hh, k0, en.row0, &full[stage], pol_x);
+            tma_load_2d(bt + bbytes, hl, k0, en.row0, &full[stage], pol_x);
+            tma_load_2d(bt + kBStepBytes, hh, k0 + 64, en.row0, &full[stage], pol_x);
+            tma_load_2d(bt + kBStepBytes + bbytes, hl, k0 + 64, en.row0, &full[stage], pol_x);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -235,17 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           mbar_arrive(&tfull[slot]);
           break;
         }
-        const int ph = job < J0 ? 0 : 1;
-        const int jj = ph == 0 ? job : job - J0;
-        int g, tile_unused;
-        job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile_unused);
+        int ph, g, tile, piece;
+        decode(job, &ph, &g, &tile, &piece);
         const int m = plan[g].m;
-        const uint32_t idesc = umma::idesc_bf16(kM, m <= 16 ? 16 : 32);
+        const uint32_t idesc = umma::idesc_bf16(kM, 2 * b_rows(m));
         const uint32_t dacc = tmem + slot * kSlotCols;
-        const int nks = ph == 0 ? nks0 : nks1;
+        const Cut& c = ph == 0 ? c0 : c1;
+        const int ks0 = piece * c.kc, ks_end = min(c.nks, ks0 + c.kc);
         bool ok = true;
-        for (int ks = 0; ks < nks; ++ks) {
-          if (ks > 0 && !mbar_wait(&full[stage], phase, a.err, 0x322)) {
+        for (int ks = ks0; ks < ks_end; ++ks) {
+          if (ks > ks0 && !mbar_wait(&full[stage], phase, a.err, 0x322)) {
             *abort_flag = 1;
             ok = false;
             break;
@@ -254,30 +332,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           const uint64_t a0 = umma::desc_sw128(st);
           const uint64_t a1 = umma::desc_sw128(st + kTileBytes);
           const uint32_t bt = st + 2 * kTileBytes;
-          const uint64_t b0 = umma::desc_sw128(bt);                   // hi, K-step 0
-          const uint64_t b0l = umma::desc_sw128(bt + kBTileBytes);    // lo, K-step 0
+          const uint64_t b0 = umma::desc_sw128(bt);                   // K-step 0: hi | lo rows
+          const bool first = ks == ks0;
           if (ph == 0) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const uint32_t acc = (ks | j) != 0;
-              umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, acc);        // gate · x_hi
-              umma::mma_bf16(dacc, a0 + 2 * j, b0l + 2 * j, idesc, 1u);        // gate · x_lo
-              umma::mma_bf16(dacc + 32, a1 + 2 * j, b0 + 2 * j, idesc, acc);   // up · x_hi
-              umma::mma_bf16(dacc + 32, a1 + 2 * j, b0l + 2 * j, idesc, 1u);   // up · x_lo
+              const uint32_t acc = (!first || j != 0) ? 1u : 0u;
+              umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, acc);        // gate · [x_hi | x_lo]
+              umma::mma_bf16(dacc + 64, a1 + 2 * j, b0 + 2 * j, idesc, acc);   // up · [x_hi | x_lo]
             }
           } else {
-            const uint64_t b1 = umma::desc_sw128(bt + 2 * kBTileBytes);   // hi, K-step 1
-            const uint64_t b1l = umma::desc_sw128(bt + 3 * kBTileBytes);  // lo, K-step 1
+            const uint64_t b1 = umma::desc_sw128(bt + kBStepBytes);        // K-step 1
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, (ks | j) != 0);
-              umma::mma_bf16(dacc, a0 + 2 * j, b0l + 2 * j, idesc, 1u);
-            }
+            for (int j = 0; j < 4; ++j)
+              umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, (!first || j != 0) ? 1u : 0u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              umma::mma_bf16(dacc, a1 + 2 * j, b1 + 2 * j, idesc, 1u);
-              umma::mma_bf16(dacc, a1 + 2 * j, b1l + 2 * j, idesc, 1u);
-            }
+            for (int j = 0; j < 4; ++j) umma::mma_bf16(dacc, a1 + 2 * j, b1 + 2 * j, idesc, 1u);
           }
           issued_any = true;
           umma::commit(&empty[stage]);  // frees the stage once these MMAs have read it
@@ -301,11 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     }
   } else if (warp >= 2 && warp < 6) {
     // ----------------------------------------------------------- epilogue --
+    // Warp w handles rows 32·(w mod 4) .. +31 of every tile (its TMEM lanes).
     const int quad = warp & 3;
     const int r_in = quad * 32 + lane;
     int slot = 0;
     uint32_t sphase = 0;
     int pub_n = 0;  // phase-0 jobs handed to the publisher so far
+    int fin_n = 0;  // tiles handed to the finisher so far (warp 2)
     for (;;) {
       if (!mbar_wait(&tfull[slot], sphase, a.err, 0x330)) {
         *abort_flag = 1;
@@ -321,36 +393,98 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             if (warp == 2) pub_entry[ps] = -1;
             mbar_arrive(&pub_full[ps]);
           }
+          if (warp == 2) {  // and for the finisher
+            const int fs = fin_n % kFinSlots;
+            if (mbar_wait(&fin_empty[fs], (uint32_t)(((fin_n / kFinSlots) & 1) ^ 1), a.err, 0x353)) {
+              fin_job[fs] = -1;
+              mbar_arrive(&fin_full[fs]);
+            }
+          }
         }
         break;
       }
-      const int ph = job < J0 ? 0 : 1;
-      const int jj = ph == 0 ? job : job - J0;
-      int g, tile;
-      job_entry(plan, jj, ph == 0 ? T0 : T1, &g, &tile);
+      int ph, g, tile, piece;
+      decode(job, &ph, &g, &tile, &piece);
       const Entry en = plan[g];
       const int m = en.m;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + slot * kSlotCols;
-      uint32_t v0[16], v1[16], u0[16], u1[16];
-      umma::ld_x16(taddr, v0);
-      if (m > 16) umma::ld_x16(taddr + 16, v1);
-      if (ph == 0) {
-        umma::ld_x16(taddr + 32, u0);
-        if (m > 16) umma::ld_x16(taddr + 48, u1);
+      // Token c's sum is column c (hi half) plus column hb + c (lo half).
+      const int hb = b_rows(m);
+      uint32_t gr[32], ur[32];  // gate (phase 0) or down (phase 1) sums, up sums
+#pragma unroll
+      for (int c = 0; c < 32; ++c) gr[c] = ur[c] = 0u;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // q = 0: gate or down, q = 1: up
+        if (q == 1 && ph != 0) break;
+        uint32_t* r = q == 0 ? gr : ur;
+        const uint32_t tq = taddr + q * 64;
+        uint32_t t0[16], t1[16];
+        if (hb == 8) {
+          umma::ld_x16(tq, t0);
+          umma::wait_ld();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            r[c] = __float_as_uint(__uint_as_float(t0[c]) + __uint_as_float(t0[8 + c]));
+        } else {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            if (half * 16 < hb) {
+              umma::ld_x16(tq + 16 * half, t0);
+              umma::ld_x16(tq + hb + 16 * half, t1);
+              umma::wait_ld();
+#pragma unroll
+              for (int c = 0; c < 16; ++c)
+                r[16 * half + c] = __float_as_uint(__uint_as_float(t0[c]) + __uint_as_float(t1[c]));
+            }
+          }
+        }
       }
-      umma::wait_ld();
       umma::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[slot]);  // accumulator slot free again
+      float* gv = reinterpret_cast<float*>(gr);
+      float* uv = reinterpret_cast<float*>(ur);
+      const Cut& cut = ph == 0 ? c0 : c1;
+      if (cut.S > 1) {
+        // A piece: store the partial sums of the warp's 32 rows and count
+        // them (release, no wait). The CTA that runs the tile's last piece
+        // hands the tile to its finisher warp.
+        const size_t sfl = ph == 0 ? slab0 : slab1;
+        float* mine = (ph == 0 ? part0 : part1) +
+                      ((size_t)(g * cut.T + tile) * cut.S + piece) * sfl;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < m) {
+            mine[c * kM + r_in] = gv[c];
+            if (ph == 0) mine[(npad + c) * kM + r_in] = uv[c];
+          }
+        }
+        __syncwarp();  // the warp's partials before lane 0's release
+        if (lane == 0) red_release_add((ph == 0 ? cnt0 : cnt1) + g * cut.T + tile, 1);
+        if (warp == 2 && lane == 0 && piece == cut.S - 1) {
+          const int fs = fin_n % kFinSlots;
+          if (!mbar_wait(&fin_empty[fs], (uint32_t)(((fin_n / kFinSlots) & 1) ^ 1), a.err, 0x354)) {
+            *abort_flag = 1;
+          } else {
+            fin_job[fs] = job;
+            mbar_arrive(&fin_full[fs]);
+          }
+          ++fin_n;
+        }
+        if (++slot == 2) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+        continue;
+      }
+      // One piece: the epilogue finishes the tile's quarter itself.
       const int row = tile * kM + r_in;
       if (ph == 0) {
         if (row < a.I) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             if (c < m) {
-              const float gv = __uint_as_float(c < 16 ? v0[c & 15] : v1[c & 15]);
-              const float uv = __uint_as_float(c < 16 ? u0[c & 15] : u1[c & 15]);
-              const float hv = silu(gv) * uv;
+              const float hv = silu(gv[c]) * uv[c];
               const uint16_t hi = to_bf16(hv);
               const size_t at = (size_t)(en.row0 + c) * a.I + row;
               a.h16[at] = hi;
@@ -358,14 +492,15 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             }
           }
         }
-        // hand the finished job to the publisher thread: __syncwarp orders the
-        // warp's h stores before lane 0's arrive (release, CTA scope)
+        // Hand the quarter to the publisher thread: __syncwarp orders the
+        // warp's h stores before lane 0's arrive (release, CTA scope).
         __syncwarp();
         if (lane == 0) {
           const int ps = pub_n % kPubSlots;
           if (!mbar_wait(&pub_empty[ps], (uint32_t)(((pub_n / kPubSlots) & 1) ^ 1), a.err, 0x350)) {
             *abort_flag = 1;
           } else {
+            atomicAdd(&pub_cnt[ps], 1);
             if (warp == 2) pub_entry[ps] = g;
             mbar_arrive(&pub_full[ps]);
           }
@@ -376,8 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
         for (int c = 0; c < 32; ++c) {
           if (c < m) {
             const int rr = en.row0 + c;
-            const float yv = __uint_as_float(c < 16 ? v0[c & 15] : v1[c & 15]);
-            a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * yv;
+            a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * gv[c];
           }
         }
       }
@@ -388,18 +522,86 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     }
   } else if (warp == 6) {
     // ---------------------------------------------------- publisher thread --
-    // Publishes each finished phase-0 job to the group's phase-1 jobs with a
-    // GPU-scope release, so that the epilogue warps only pay a CTA-scope
-    // arrive; this thread's wait acquires their h stores and its release
-    // reduction makes them visible GPU-wide before the count.
+    // Publishes each phase-0 job's finished quarters to the group's phase-1
+    // jobs with a GPU-scope release, so that the epilogue warps only pay a
+    // CTA-scope arrive; this thread's wait acquires their h stores and its
+    // release reduction makes them visible GPU-wide before the count.
     if (lane == 0) {
       for (int pn = 0;; ++pn) {
         const int ps = pn % kPubSlots;
         if (!mbar_wait(&pub_full[ps], (uint32_t)((pn / kPubSlots) & 1), a.err, 0x351)) break;
         const int e = pub_entry[ps];
         if (e < 0) break;
-        red_release_add(done0 + e, 1);
+        const int q = pub_cnt[ps];
+        pub_cnt[ps] = 0;
+        if (q > 0) red_release_add(done0 + e, q);
         mbar_arrive(&pub_empty[ps]);
+      }
+    }
+  } else if (warp == 7) {
+    // ----------------------------------------------------- finisher warp --
+    // For each tile whose last piece ran here: wait (bounded) until all 4·S
+    // piece-quarters are counted, add the pieces in piece order, finish the
+    // tile's 128 rows (lane l: rows l, 32+l, 64+l, 96+l) and, in phase 0,
+    // publish the tile to the group's phase-1 jobs.
+    for (int fn = 0;; ++fn) {
+      const int fs = fn % kFinSlots;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&fin_full[fs], (uint32_t)((fn / kFinSlots) & 1), a.err, 0x360);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
+      if (!ok) break;
+      const int job = fin_job[fs];
+      if (job < 0) break;
+      int ph, g, tile, piece;
+      decode(job, &ph, &g, &tile, &piece);
+      const Cut& cut = ph == 0 ? c0 : c1;
+      if (lane == 0) {
+        ok = wait_count((ph == 0 ? cnt0 : cnt1) + g * cut.T + tile, 4 * cut.S, a.err, 0x361);
+        if (!ok) *abort_flag = 1;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();  // lane 0's acquire before every lane's reads
+      const Entry en = plan[g];
+      const int m = en.m;
+      const size_t sfl = ph == 0 ? slab0 : slab1;
+      const float* base = (ph == 0 ? part0 : part1) + (size_t)(g * cut.T + tile) * cut.S * sfl;
+      for (int c = 0; ok && c < m; ++c) {
+        float sg[4], su[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sg[i] = su[i] = 0.f;
+#pragma unroll
+        for (int p = 0; p < kMaxPieces; ++p) {
+          if (p < cut.S) {
+            const float* src = base + (size_t)p * sfl;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              sg[i] += __ldcg(src + c * kM + 32 * i + lane);
+              if (ph == 0) su[i] += __ldcg(src + (npad + c) * kM + 32 * i + lane);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = tile * kM + 32 * i + lane;
+          if (ph == 0) {
+            if (row < a.I) {
+              const float hv = silu(sg[i]) * su[i];
+              const uint16_t hi = to_bf16(hv);
+              const size_t at = (size_t)(en.row0 + c) * a.I + row;
+              a.h16[at] = hi;
+              a.h16lo[at] = to_bf16(hv - __uint_as_float((uint32_t)hi << 16));
+            }
+          } else if (row < a.d) {
+            const int rr = en.row0 + c;
+            a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * sg[i];
+          }
+        }
+      }
+      __syncwarp();  // every lane's stores before lane 0's release
+      if (lane == 0) {
+        if (ph == 0 && ok) red_release_add(done0 + g, 4);
+        mbar_arrive(&fin_empty[fs]);
       }
     }
   }
@@ -420,10 +622,10 @@ bool w_map(CUtensorMap* m, const void* p, int n_mat, int rows, int K) {
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool b_map(CUtensorMap* m, const void* p, int rows, int K) {
+bool b_map(CUtensorMap* m, const void* p, int rows, int K, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
   const uint64_t strides[1] = {(uint64_t)K * 2};
-  const uint32_t box[2] = {64, (uint32_t)kSub};
+  const uint32_t box[2] = {64, (uint32_t)box_rows};
   return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -454,16 +656,21 @@ cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t str
     ok &= w_map(&prm.maps.swu, a.ws_up, a.s, a.I, a.d);
     ok &= w_map(&prm.maps.swd, a.ws_down, a.s, a.d, a.I);
   }
-  if (a.engine == 1) {
-    ok &= b_map(&prm.maps.xa, a.xg16, P, a.d);
-    ok &= b_map(&prm.maps.xa_lo, a.xg16lo, P, a.d);
-  } else {  // per-slot routed groups (one token each) never run here
-    prm.maps.xa = prm.maps.xa_lo = prm.maps.wg;
+  // Phase-0 token rows: x gathered in union order (dedup) or x itself
+  // (per-slot: an entry's row is its token); shared experts read x.
+  const uint16_t* xa = a.engine == 1 ? a.xg16 : a.x16;
+  const uint16_t* xa_lo = a.engine == 1 ? a.xg16lo : a.x16lo;
+  const int xa_rows = a.engine == 1 ? P : a.n;
+  for (int si = 0; si < 3; ++si) {
+    const int br = 8 << si;
+    CUtensorMap* B = prm.maps.b[si];
+    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br);
+    ok &= b_map(&B[kXALo], xa_lo, xa_rows, a.d, br);
+    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br);
+    ok &= b_map(&B[kXSLo], a.x16lo, a.n, a.d, br);
+    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br);
+    ok &= b_map(&B[kHLo], a.h16lo, hrows, a.I, br);
   }
-  ok &= b_map(&prm.maps.xs, a.x16, a.n, a.d);
-  ok &= b_map(&prm.maps.xs_lo, a.x16lo, a.n, a.d);
-  ok &= b_map(&prm.maps.h, a.h16, hrows, a.I);
-  ok &= b_map(&prm.maps.h_lo, a.h16lo, hrows, a.I);
   if (!ok) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);

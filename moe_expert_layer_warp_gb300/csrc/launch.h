@@ -67,7 +67,10 @@ struct ExpertArgs {
   uint16_t* x16;        // [n][d] bf16 scratch: hi half of x
   uint16_t* x16lo;      //   and lo half
   int* sync;            // [kCcSyncInts] CUDA-core kernel's job counter and group counts
-  int* sync_mma;        // [kMmaSyncInts] tensor-core kernel's job counter and group counts
+  int* sync_mma;        // [kMmaSyncInts] tensor-core kernel's job counter, group counts and
+                        //   arrival counts of jobs cut along K
+  float* part;          // [part_bytes] tensor-core kernel's partial sums of jobs cut along K
+  size_t part_bytes;
   int mma_min_m;        // groups with at least this many tokens run on tensor cores
   int cc_waits_prep;    // 1: the CUDA-core kernel directly follows the prep kernel
   float* y_slot;
@@ -85,11 +88,18 @@ cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t 
 cudaError_t launch_expert_cc(const ExpertArgs& a, int num_sms, cudaStream_t stream);
 
 // Tokens per plan entry of the CUDA-core and tensor-core kernels, and the
-// ints of counter scratch each kernel uses (job counter + one per entry).
+// ints of counter scratch each kernel uses: a job counter and one count per
+// entry; the tensor-core kernel adds, per phase, kMmaCntInts arrival counts
+// of the pieces of jobs cut along K (one per (entry, tile, quarter of rows)).
 constexpr int kCcSub = 4;
 constexpr int kMmaSub = 32;
+constexpr int kMmaCntInts = 4096;
 constexpr int kCcSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kCcSub - 1) / kCcSub);
-constexpr int kMmaSyncInts = 1 + MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kMmaSub - 1) / kMmaSub);
+constexpr int kMmaEntries = MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + kMmaSub - 1) / kMmaSub);
+constexpr int kMmaSyncInts = 1 + kMmaEntries + 2 * kMmaCntInts;
+// Scratch for the partial sums of the tensor-core kernel's K pieces; it
+// bounds how finely a phase is cut (more pieces need more partials).
+constexpr size_t kMmaPartBytes = size_t(24) << 20;
 
 // Tensor-core expert kernel (tcgen05 + TMEM) for groups of ≥ mma_min_m tokens.
 cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t stream);

@@ -36,6 +36,21 @@ MOE_DEV void job_entry(const Entry* plan, int jj, int T, int* entry, int* tile) 
   *tile = local / eg.q;
 }
 
+// Job jj of a phase whose (entry, tile) pairs are each cut into S pieces
+// along K: the jobs of a group's q sub-groups are the q·T·S consecutive jobs
+// from first·T·S, ordered tile, then piece, then sub-group, so that the
+// sub-groups that read the same weights take consecutive jobs.
+MOE_DEV void job_decode(const Entry* plan, int jj, int T, int S, int* entry, int* tile,
+                        int* piece) {
+  const int TS = T * S;
+  const Entry& eg = plan[jj / TS];
+  const int local = jj - eg.first * TS;
+  *entry = eg.first + local % eg.q;
+  const int rest = local / eg.q;
+  *tile = rest / S;
+  *piece = rest - (rest / S) * S;
+}
+
 // Exclusive prefix sum over the block (one value per thread). Returns the
 // thread's offset; *total receives the sum. Uses scratch[0..warps].
 MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
@@ -133,6 +148,12 @@ MOE_DEV int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+MOE_DEV int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 MOE_DEV void red_release_add(int* p, int v) {

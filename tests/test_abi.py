@@ -11,7 +11,9 @@ from moe_expert_layer_warp_gb300 import api, build
 from moe_expert_layer_warp_gb300.configs import ALL, LayerShape, W_BF16
 
 CC_SYNC_INTS = 1 + 512 + 4 * 32   # CUDA-core kernel: job counter + per-entry tile counts
-MMA_SYNC_INTS = 1 + 512 + 4 * 4   # tensor-core kernel: job counter + per-entry tile counts
+MMA_SYNC_INTS = 1 + 528 + 2 * 4096   # tensor-core kernel: job counter, per-entry tile counts,
+                                     # per-phase arrival counts of K pieces
+MMA_PART_BYTES = 24 << 20            # tensor-core kernel partial sums (bf16 layers only)
 HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
@@ -49,7 +51,8 @@ def test_workspace_bytes_closed_form(lib):
         hrows = n * sh.top_k + sh.n_shared * n
         want = (a256(n * sh.n_experts * 4) + a256(hrows * sh.inter * 4) + a256(2 * hrows * sh.inter * 2)
                 + a256(n * sh.top_k * sh.d * 4) + a256(2 * n * sh.top_k * sh.d * 2)
-                + a256(2 * n * sh.d * 2) + a256(CC_SYNC_INTS * 4) + a256(MMA_SYNC_INTS * 4))
+                + a256(2 * n * sh.d * 2) + a256(CC_SYNC_INTS * 4) + a256(MMA_SYNC_INTS * 4)
+                + (MMA_PART_BYTES if sh.wdtype == W_BF16 else 0))
         assert got == want, w.name
 
 

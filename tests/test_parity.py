@@ -173,3 +173,19 @@ def test_v2_lite_stack_layers_full_size():
         check_pass(L, x, tokens=[4])
         del L
         torch.cuda.empty_cache()
+
+
+def test_small_layers_on_the_cuda_core_kernel():
+    """bf16 layers normally run on the tensor-core kernel alone; with
+    MOE_MMA_MIN_M above every group's size (read once per process, hence a
+    child process) the same small layers run on the CUDA-core kernel."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, MOE_MMA_MIN_M="1000")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "tests/test_parity.py::test_small_layers_every_element",
+                        "tests/test_parity.py::test_repeated_runs_are_bitwise_identical"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
