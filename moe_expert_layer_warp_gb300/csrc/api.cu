@@ -7,6 +7,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include <mutex>
 
 #include "moe_warp.h"
@@ -118,19 +120,32 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   return L;
 }
 
-// Smallest group (tokens) that runs on the tensor-core kernel (bf16 weights).
-// Every bf16 group goes there: its weights pass from HBM through shared
-// memory into the tensor cores with no per-element instruction, and its jobs
-// are cut along K until they fill the GPU, so it streams at the same rate
-// for one token as for 32. MOE_MMA_MIN_M in the environment (read once; for
-// tuning) sends groups below that size to the CUDA-core kernel instead.
-int mma_min_m(const moe_layer_desc*) {
+// Which expert kernel a bf16 call runs on; the two never share a call (run
+// side by side they slow each other). The tensor-core kernel streams each
+// weight tile through shared memory into the tensor cores with no
+// per-element instruction, but it needs about four 128-row tiles per SM;
+// with fewer it cuts tiles along K, and adding the pieces across CTAs costs
+// a few microseconds of synchronisation behind the CTAs' own streams. The
+// CUDA-core kernel works in 16- and 32-row tiles and needs no such step. So
+// a call goes to the tensor cores once its groups hold at least
+// kMmaMinTiles tiles (gate/up plus down tiles per group). The groups of a
+// dedup call are known only on the device; the estimate takes half of
+// min(E, n·k) distinct experts, the middle of the range the union spans for
+// correlated hidden states. MOE_MMA_MIN_M in the environment (read once; for
+// tuning) fixes instead the smallest group that runs on the tensor cores.
+constexpr int kMmaMinTiles = 360;
+
+int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   static const int forced = [] {
     const char* e = getenv("MOE_MMA_MIN_M");
     const int x = e ? atoi(e) : 0;
     return x >= 1 ? x : 0;
   }();
-  return forced ? forced : 1;
+  if (forced) return forced;
+  const int tiles = (d->inter + 127) / 128 + (d->d + 127) / 128;
+  const int routed = engine == 0 ? n * d->top_k : std::min(d->n_experts, n * d->top_k) / 2;
+  const int groups = routed + d->n_shared * ((n + moe::kMmaSub - 1) / moe::kMmaSub);
+  return groups * tiles >= kMmaMinTiles ? 1 : 0x7fffffff;
 }
 
 moe_status check_ws(const moe_layer_desc* d, int32_t n, const void* ws, size_t ws_bytes) {
@@ -255,7 +270,7 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.part_bytes = L.part_bytes;
   // fp32 weights never go to the tensor cores (a tf32 product would miss the
   // fp32 tolerance), so every fp32 group stays on the CUDA-core kernel.
-  a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m(desc) : 0x7fffffff;
+  a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m(desc, engine, n) : 0x7fffffff;
   a.y_slot = y_slot;
   a.err = di->err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

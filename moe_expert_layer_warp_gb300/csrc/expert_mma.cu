@@ -28,11 +28,11 @@
 // Jobs. A job is (entry, 128-row tile, piece of K). When a phase has fewer
 // tiles than a few per CTA, each tile is cut into S ≤ 8 pieces along K so
 // that every SM streams. Every piece stores its fp32 partial sums and counts
-// itself with a release reduction (nothing waits for it); the CTA that runs
-// a tile's last piece hands the tile to its finisher warp, which waits
-// (bounded) until all pieces are counted, adds them in piece order — a fixed
-// order, so results are reproducible — and finishes the tile off the tensor
-// pipeline's path. A phase-1 job loads its group's h only after every
+// itself per 32-row quarter with a release reduction (nothing waits for
+// it); the CTA that runs a tile's last piece hands each quarter to one of its
+// four finisher warps, which waits (bounded) until all pieces of the quarter
+// are counted, adds them in piece order — a fixed order, so results are
+// reproducible — and finishes the quarter off the tensor pipeline's path. A phase-1 job loads its group's h only after every
 // phase-0 tile of the group is stored (a count in scratch, bounded acquire
 // wait).
 //
@@ -41,7 +41,8 @@
 //   warp 1    TMEM owner and MMA issuer (one thread), two accumulator slots,
 //   warps 2-5 epilogue: TMEM → registers → partials / SwiGLU / weighting → global,
 //   warp 6    publisher of phase-0 tiles finished by the epilogue (GPU-scope release),
-//   warp 7    finisher of tiles cut into pieces.
+//   warp 7    only helps build the group table,
+//   warps 8-11 finishers of tiles cut into pieces (warp 8+q: rows 32q..32q+31).
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -58,7 +59,7 @@ namespace {
 constexpr int kM = 128;                             // weight rows per tile
 constexpr int kSub = kMmaSub;                       // tokens per entry (≤ MMA N)
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kTileBytes = kM * 128;                // [128 rows][64 bf16]
 constexpr int kBStepBytes = 2 * kSub * 128;         // one K-step of tokens: [2h ≤ 64 rows][64 bf16]
 // stage: two weight tiles, then the token tiles of one or two K-steps
@@ -74,8 +75,8 @@ static_assert(kSub == 32, "the epilogue and the TMEM slots assume at most 32 tok
 
 constexpr int kOffBar = kStages * kStageBytes;
 constexpr int kPubSlots = 8;                        // ring of finished phase-0 jobs
-constexpr int kFinSlots = 32;                       // ring of tiles to finish
-constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots + 2 * kFinSlots;
+constexpr int kFinSlots = 16;                       // per finisher: ring of quarters to finish
+constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots + 2 * 4 * kFinSlots;
 constexpr int kOffPlan = kOffBar + kNumBars * 8;
 constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
 constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
@@ -135,8 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   uint64_t* drain = tempty + 2;
   uint64_t* pub_full = drain + 1;  // epilogue warps → publisher: a phase-0 job's quarters
   uint64_t* pub_empty = pub_full + kPubSlots;
-  uint64_t* fin_full = pub_empty + kPubSlots;  // epilogue → finisher: a tile's last piece is stored
-  uint64_t* fin_empty = fin_full + kFinSlots;
+  uint64_t* fin_full = pub_empty + kPubSlots;  // [4][kFinSlots] epilogue warp q → finisher q
+  uint64_t* fin_empty = fin_full + 4 * kFinSlots;
   Entry* plan = reinterpret_cast<Entry*>(smem + kOffPlan);
   int* row_out = reinterpret_cast<int*>(smem + kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + kOffRowW);
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   volatile int* pub_entry = misc + 36;                  // [kPubSlots]
   int* pub_cnt = misc + 44;                             // [kPubSlots] quarters finished
   int* max_m = misc + 52;
-  volatile int* fin_job = misc + 64;                    // [kFinSlots]
+  volatile int* fin_job = misc + 64;                    // [4][kFinSlots]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       mbar_init(&pub_empty[i], 1);
       pub_cnt[i] = 0;
     }
-    for (int i = 0; i < kFinSlots; ++i) {
+    for (int i = 0; i < 4 * kFinSlots; ++i) {
       mbar_init(&fin_full[i], 1);
       mbar_init(&fin_empty[i], 1);
     }
@@ -377,7 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     int slot = 0;
     uint32_t sphase = 0;
     int pub_n = 0;  // phase-0 jobs handed to the publisher so far
-    int fin_n = 0;  // tiles handed to the finisher so far (warp 2)
+    int fin_n = 0;  // quarters handed to finisher `quad` so far (lane 0)
+    uint64_t* my_fin_full = fin_full + quad * kFinSlots;
+    uint64_t* my_fin_empty = fin_empty + quad * kFinSlots;
+    volatile int* my_fin_job = fin_job + quad * kFinSlots;
     for (;;) {
       if (!mbar_wait(&tfull[slot], sphase, a.err, 0x330)) {
         *abort_flag = 1;
@@ -393,11 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             if (warp == 2) pub_entry[ps] = -1;
             mbar_arrive(&pub_full[ps]);
           }
-          if (warp == 2) {  // and for the finisher
+          {  // and for this quarter's finisher
             const int fs = fin_n % kFinSlots;
-            if (mbar_wait(&fin_empty[fs], (uint32_t)(((fin_n / kFinSlots) & 1) ^ 1), a.err, 0x353)) {
-              fin_job[fs] = -1;
-              mbar_arrive(&fin_full[fs]);
+            if (mbar_wait(&my_fin_empty[fs], (uint32_t)(((fin_n / kFinSlots) & 1) ^ 1), a.err, 0x353)) {
+              my_fin_job[fs] = -1;
+              mbar_arrive(&my_fin_full[fs]);
             }
           }
         }
@@ -448,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       if (cut.S > 1) {
         // A piece: store the partial sums of the warp's 32 rows and count
         // them (release, no wait). The CTA that runs the tile's last piece
-        // hands the tile to its finisher warp.
+        // hands each quarter to that quarter's finisher warp.
         const size_t sfl = ph == 0 ? slab0 : slab1;
         float* mine = (ph == 0 ? part0 : part1) +
                       ((size_t)(g * cut.T + tile) * cut.S + piece) * sfl;
@@ -460,14 +464,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           }
         }
         __syncwarp();  // the warp's partials before lane 0's release
-        if (lane == 0) red_release_add((ph == 0 ? cnt0 : cnt1) + g * cut.T + tile, 1);
-        if (warp == 2 && lane == 0 && piece == cut.S - 1) {
+        if (lane == 0) red_release_add((ph == 0 ? cnt0 : cnt1) + (g * cut.T + tile) * 4 + quad, 1);
+        if (lane == 0 && piece == cut.S - 1) {
           const int fs = fin_n % kFinSlots;
-          if (!mbar_wait(&fin_empty[fs], (uint32_t)(((fin_n / kFinSlots) & 1) ^ 1), a.err, 0x354)) {
+          if (!mbar_wait(&my_fin_empty[fs], (uint32_t)(((fin_n / kFinSlots) & 1) ^ 1), a.err, 0x354)) {
             *abort_flag = 1;
           } else {
-            fin_job[fs] = job;
-            mbar_arrive(&fin_full[fs]);
+            my_fin_job[fs] = job;
+            mbar_arrive(&my_fin_full[fs]);
           }
           ++fin_n;
         }
@@ -538,26 +542,32 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
         mbar_arrive(&pub_empty[ps]);
       }
     }
-  } else if (warp == 7) {
-    // ----------------------------------------------------- finisher warp --
-    // For each tile whose last piece ran here: wait (bounded) until all 4·S
-    // piece-quarters are counted, add the pieces in piece order, finish the
-    // tile's 128 rows (lane l: rows l, 32+l, 64+l, 96+l) and, in phase 0,
-    // publish the tile to the group's phase-1 jobs.
+  } else if (warp >= 8) {
+    // ---------------------------------------------------- finisher warps --
+    // Finisher q, for each quarter q of a tile whose last piece ran here:
+    // wait (bounded) until the S pieces of the quarter are counted, add the
+    // pieces in piece order (lane l: row 32q + l; four tokens per round of
+    // loads), finish the rows and, in phase 0, publish the quarter to the
+    // group's phase-1 jobs.
+    const int q = warp - 8;
+    const int row_in = q * 32 + lane;
+    uint64_t* my_full = fin_full + q * kFinSlots;
+    uint64_t* my_empty = fin_empty + q * kFinSlots;
+    volatile int* my_job = fin_job + q * kFinSlots;
     for (int fn = 0;; ++fn) {
       const int fs = fn % kFinSlots;
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&fin_full[fs], (uint32_t)((fn / kFinSlots) & 1), a.err, 0x360);
+      if (lane == 0) ok = mbar_wait(&my_full[fs], (uint32_t)((fn / kFinSlots) & 1), a.err, 0x360);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       __syncwarp();
       if (!ok) break;
-      const int job = fin_job[fs];
+      const int job = my_job[fs];
       if (job < 0) break;
       int ph, g, tile, piece;
       decode(job, &ph, &g, &tile, &piece);
       const Cut& cut = ph == 0 ? c0 : c1;
       if (lane == 0) {
-        ok = wait_count((ph == 0 ? cnt0 : cnt1) + g * cut.T + tile, 4 * cut.S, a.err, 0x361);
+        ok = wait_count((ph == 0 ? cnt0 : cnt1) + (g * cut.T + tile) * 4 + q, cut.S, a.err, 0x361);
         if (!ok) *abort_flag = 1;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -566,42 +576,47 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       const int m = en.m;
       const size_t sfl = ph == 0 ? slab0 : slab1;
       const float* base = (ph == 0 ? part0 : part1) + (size_t)(g * cut.T + tile) * cut.S * sfl;
-      for (int c = 0; ok && c < m; ++c) {
+      const int row = tile * kM + row_in;
+      for (int cb = 0; ok && cb < m; cb += 4) {
         float sg[4], su[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sg[i] = su[i] = 0.f;
+        for (int u = 0; u < 4; ++u) sg[u] = su[u] = 0.f;
 #pragma unroll
         for (int p = 0; p < kMaxPieces; ++p) {
           if (p < cut.S) {
             const float* src = base + (size_t)p * sfl;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              sg[i] += __ldcg(src + c * kM + 32 * i + lane);
-              if (ph == 0) su[i] += __ldcg(src + (npad + c) * kM + 32 * i + lane);
+            for (int u = 0; u < 4; ++u) {
+              if (cb + u < m) {
+                sg[u] += __ldcg(src + (cb + u) * kM + row_in);
+                if (ph == 0) su[u] += __ldcg(src + (npad + cb + u) * kM + row_in);
+              }
             }
           }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = tile * kM + 32 * i + lane;
-          if (ph == 0) {
-            if (row < a.I) {
-              const float hv = silu(sg[i]) * su[i];
-              const uint16_t hi = to_bf16(hv);
-              const size_t at = (size_t)(en.row0 + c) * a.I + row;
-              a.h16[at] = hi;
-              a.h16lo[at] = to_bf16(hv - __uint_as_float((uint32_t)hi << 16));
+        for (int u = 0; u < 4; ++u) {
+          const int c = cb + u;
+          if (c < m) {
+            if (ph == 0) {
+              if (row < a.I) {
+                const float hv = silu(sg[u]) * su[u];
+                const uint16_t hi = to_bf16(hv);
+                const size_t at = (size_t)(en.row0 + c) * a.I + row;
+                a.h16[at] = hi;
+                a.h16lo[at] = to_bf16(hv - __uint_as_float((uint32_t)hi << 16));
+              }
+            } else if (row < a.d) {
+              const int rr = en.row0 + c;
+              a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * sg[u];
             }
-          } else if (row < a.d) {
-            const int rr = en.row0 + c;
-            a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * sg[i];
           }
         }
       }
       __syncwarp();  // every lane's stores before lane 0's release
       if (lane == 0) {
-        if (ph == 0 && ok) red_release_add(done0 + g, 4);
-        mbar_arrive(&fin_empty[fs]);
+        if (ph == 0 && ok) red_release_add(done0 + g, 1);
+        mbar_arrive(&my_empty[fs]);
       }
     }
   }

@@ -175,17 +175,20 @@ def test_v2_lite_stack_layers_full_size():
         torch.cuda.empty_cache()
 
 
-def test_small_layers_on_the_cuda_core_kernel():
-    """bf16 layers normally run on the tensor-core kernel alone; with
-    MOE_MMA_MIN_M above every group's size (read once per process, hence a
-    child process) the same small layers run on the CUDA-core kernel."""
+@pytest.mark.parametrize("min_m", ["1000", "1"], ids=["cuda-core-only", "tensor-core-only"])
+def test_small_layers_on_each_expert_kernel(min_m):
+    """bf16 calls pick one expert kernel by size; MOE_MMA_MIN_M (read once per
+    process, hence a child process) forces every group of the same small
+    layers onto the CUDA-core kernel (1000) or the tensor-core kernel (1),
+    cutting tiles along K wherever they are few."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, MOE_MMA_MIN_M="1000")
+    env = dict(os.environ, MOE_MMA_MIN_M=min_m)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_parity.py::test_small_layers_every_element",
+                        "tests/test_parity.py::test_identical_tokens_select_k_experts",
                         "tests/test_parity.py::test_repeated_runs_are_bitwise_identical"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
