@@ -169,10 +169,8 @@ def enqueue_step(w, runners, xs, step_idx, stream):
 
 
 def kernels_per_pass():
-    # moe_route: gate GEMV + top-k; moe_build_union: 1; expert call: prep + the
-    # CUDA-core kernel (the tensor-core kernel is not launched for this shape:
-    # 27 row tiles per expert and n <= 9 put every group below its threshold);
-    # moe_combine: 1
+    # moe_route: gate GEMV + top-k; moe_build_union: 1; expert call: prep + one
+    # expert kernel (tensor-core or CUDA-core, chosen per call); moe_combine: 1
     return 2 + 1 + 2 + 1
 
 
@@ -219,25 +217,110 @@ def measure_breakdown(w, runners, xs, reps=3):
 
 
 def e2e_measure(w, runners, xs, steps, warmup):
-    """End to end through the public API with host buffers: every pass copies
-    its hidden states from pinned host memory and reads y back to pinned host
-    memory, inside the timed region."""
+    """End to end through the public API with host buffers, as a serving loop
+    runs it: each step uploads all its passes' hidden states from pinned host
+    memory in one copy, runs the passes (PassRunner.forward writing each y
+    into the step's output block) and reads the block back to pinned host
+    memory in one copy. One CUDA graph per step variant holds the upload, the
+    passes and the read-back; every step replays one, so every copy runs every
+    step inside the timed region."""
     import torch
     stream = torch.cuda.current_stream()
+    dev = xs[w.pass_sizes[0]][0].device
+    d = w.shape.d
+    n_variants = REPLICAS * N_PASSES_PER_N // math.gcd(REPLICAS, N_PASSES_PER_N)
+    plans = [step_plan(w, v) for v in range(n_variants)]
+    rows = sum(n for _, n, _, _ in plans[0])
+    hx = []
+    for v in range(n_variants):
+        blk = torch.empty((rows, d), dtype=torch.float32).pin_memory()
+        r = 0
+        for _, n, _, q in plans[v]:
+            blk[r:r + n].copy_(xs[n][q].cpu())
+            r += n
+        hx.append(blk)
+    hy = [torch.empty((rows, d), dtype=torch.float32).pin_memory() for _ in range(n_variants)]
+    dx = torch.empty((rows, d), dtype=torch.float32, device=dev)
+    dy = torch.empty((rows, d), dtype=torch.float32, device=dev)
+    h2d = d2h = rows * d * 4
+
+    def capture_step(v, cap):
+        dx.copy_(hx[v], non_blocking=True)
+        r = 0
+        for rep, n, eng, q in plans[v]:
+            runners[rep].forward(dx[r:r + n], eng, cap, out=dy[r:r + n])
+            r += n
+        hy[v].copy_(dy, non_blocking=True)
+
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    graphs = []
+    with torch.cuda.stream(cap):
+        for v in range(n_variants):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                capture_step(v, cap)
+            graphs.append(g)
+    stream.wait_stream(cap)
+    for i in range(max(warmup, n_variants)):
+        graphs[i % n_variants].replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        graphs[i % n_variants].replay()
+    t1.record(stream)
+    t1.synchronize()
+    return t0.elapsed_time(t1) / steps, h2d, d2h
+
+
+def e2e_measure_eager(w, runners, xs, steps, warmup):
+    """End to end through the public API called pass by pass from Python, with
+    host buffers: every pass copies its hidden states from pinned host memory
+    and reads y back to pinned host memory, inside the timed region. The
+    copies run on a copy stream, ordered against the compute stream by events,
+    so that a pass's upload overlaps the previous pass and its read-back
+    overlaps the next (double-buffered device and host buffers). Returns the
+    device time per step and the host's issue time per step."""
+    import torch
+    stream = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    dev = xs[w.pass_sizes[0]][0].device
     hx = {n: [x.cpu().pin_memory() for x in xs[n]] for n in xs}
-    hy = {n: torch.empty((n, w.shape.d), dtype=torch.float32).pin_memory() for n in xs}
-    dx = {n: torch.empty((n, w.shape.d), dtype=torch.float32, device=xs[n][0].device)
+    hy = {n: [torch.empty((n, w.shape.d), dtype=torch.float32).pin_memory() for _ in range(2)]
+          for n in xs}
+    dx = {n: [torch.empty((n, w.shape.d), dtype=torch.float32, device=dev) for _ in range(2)]
           for n in xs}
     h2d = d2h = 0
     for n in w.pass_sizes:
         h2d += 2 * n * w.shape.d * 4
         d2h += 2 * n * w.shape.d * 4
+    state = {"i": 0, "done": [None, None], "read": {}}
 
     def one(step_idx):
         for rep, n, eng, q in step_plan(w, step_idx):
-            dx[n].copy_(hx[n][q], non_blocking=True)
-            y = runners[rep].forward(dx[n], eng, stream)
-            hy[n].copy_(y, non_blocking=True)
+            b = state["i"] & 1
+            state["i"] += 1
+            with torch.cuda.stream(copy):
+                if state["done"][b] is not None:
+                    copy.wait_event(state["done"][b])   # buffer b's previous pass is done
+                dx[n][b].copy_(hx[n][q], non_blocking=True)
+                up = torch.cuda.Event()
+                up.record(copy)
+            stream.wait_event(up)
+            if rep in state["read"]:
+                stream.wait_event(state["read"][rep])   # this runner's last y has been read
+            y = runners[rep].forward(dx[n][b], eng, stream)
+            fin = torch.cuda.Event()
+            fin.record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(fin)
+                hy[n][b].copy_(y, non_blocking=True)
+                rd = torch.cuda.Event()
+                rd.record(copy)
+            state["done"][b] = rd
+            state["read"][rep] = rd
 
     for i in range(warmup):
         one(i)
@@ -245,20 +328,25 @@ def e2e_measure(w, runners, xs, steps, warmup):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
+    copy.wait_event(t0)
+    h0 = time.perf_counter()
     for i in range(steps):
         one(i)
+    host_ms = (time.perf_counter() - h0) * 1e3 / steps
+    stream.wait_stream(copy)
     t1.record(stream)
     t1.synchronize()
     ms = t0.elapsed_time(t1) / steps
-    return ms, h2d, d2h
+    return ms, h2d, d2h, host_ms
 
 
-TRAFFIC_SOURCES = ("expert_stream.cu", "engine.cu", "plan.cuh", "common.cuh", "launch.h")
+TRAFFIC_SOURCES = ("expert_stream.cu", "expert_mma.cu", "engine.cu", "plan.cuh", "common.cuh",
+                   "launch.h", "tcgen05.cuh", "tmap.h", "api.cu")
 
 
 def kernel_source_hash() -> str:
-    """sha256 (first 16 hex digits) over the sources of the CUDA-core expert
-    kernel and its prep kernel."""
+    """sha256 (first 16 hex digits) over the sources of the expert call: the
+    prep kernel, both expert kernels and the choice between them."""
     import hashlib
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES:
@@ -396,6 +484,8 @@ def run_ours(args):
     rep = stepmodel.build_report(samples, t_fix)
     e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
     e2e_ms = max_over_ranks(e2e_ms, dev)
+    eager_ms, _, _, eager_host_ms = e2e_measure_eager(w, runners, xs, max(3, args.steps // 2), 3)
+    eager_ms = max_over_ranks(eager_ms, dev)
 
     if rank != 0:
         return
@@ -429,15 +519,19 @@ def run_ours(args):
                          "consecutive passes read different replicas" % REPLICAS,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "timing": "CUDA-graph replay of each step, CUDA events on the stream"},
-        "roofline": {"kernel": "expert_engine_kernel with its prep kernel (one expert call: "
-                               "up/gate and down of every group)",
+        "roofline": {"kernel": "expert call: prep kernel + expert_mma_kernel (tensor cores) or "
+                               "expert_engine_kernel (CUDA cores), chosen per call; up/gate and "
+                               "down of every group",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": load_traffic("traffic_expert_engine_v2lite_bench.txt")},
+                     "traffic": load_traffic("traffic_expert_call_v2lite_bench.txt")},
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_value(world, tokens_per_step, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * 2 * len(w.pass_sizes) * kernels_per_pass(),
+        "e2e_eager": {"value": round(job_value(world, tokens_per_step, eager_ms), 1),
+                      "unit": UNIT, "host_issue_ms_per_step": round(eager_host_ms, 4),
+                      "note": "the same passes and copies issued call by call from Python"},
         "clocks": clk,
         "engines": per_engine,
         "stepmodel": rep.as_dict(),

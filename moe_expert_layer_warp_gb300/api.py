@@ -112,6 +112,8 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def _stream(stream) -> ctypes.c_void_p:
+    if isinstance(stream, ctypes.c_void_p):
+        return stream
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))

@@ -645,6 +645,38 @@ bool b_map(CUtensorMap* m, const void* p, int rows, int K, int box_rows) {
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// Every tensor map of one launch.
+bool build_maps(const ExpertArgs& a, Maps* M) {
+  memset(M, 0, sizeof *M);
+  const int P = a.n * a.k;
+  const int hrows = P + a.s * a.n;
+  bool ok = true;
+  ok &= w_map(&M->wg, a.w_gate, a.E, a.I, a.d);
+  ok &= w_map(&M->wu, a.w_up, a.E, a.I, a.d);
+  ok &= w_map(&M->wd, a.w_down, a.E, a.d, a.I);
+  if (a.s > 0) {
+    ok &= w_map(&M->swg, a.ws_gate, a.s, a.I, a.d);
+    ok &= w_map(&M->swu, a.ws_up, a.s, a.I, a.d);
+    ok &= w_map(&M->swd, a.ws_down, a.s, a.d, a.I);
+  }
+  // Phase-0 token rows: x gathered in union order (dedup) or x itself
+  // (per-slot: an entry's row is its token); shared experts read x.
+  const uint16_t* xa = a.engine == 1 ? a.xg16 : a.x16;
+  const uint16_t* xa_lo = a.engine == 1 ? a.xg16lo : a.x16lo;
+  const int xa_rows = a.engine == 1 ? P : a.n;
+  for (int si = 0; si < 3; ++si) {
+    const int br = 8 << si;
+    CUtensorMap* B = M->b[si];
+    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br);
+    ok &= b_map(&B[kXALo], xa_lo, xa_rows, a.d, br);
+    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br);
+    ok &= b_map(&B[kXSLo], a.x16lo, a.n, a.d, br);
+    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br);
+    ok &= b_map(&B[kHLo], a.h16lo, hrows, a.I, br);
+  }
+  return ok;
+}
+
 }  // namespace
 
 cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
@@ -660,33 +692,23 @@ cudaError_t launch_expert_mma(const ExpertArgs& a, int num_sms, cudaStream_t str
   Params prm;
   memset(&prm, 0, sizeof prm);
   prm.a = a;
-  const int P = a.n * a.k;
-  const int hrows = P + a.s * a.n;
-  bool ok = true;
-  ok &= w_map(&prm.maps.wg, a.w_gate, a.E, a.I, a.d);
-  ok &= w_map(&prm.maps.wu, a.w_up, a.E, a.I, a.d);
-  ok &= w_map(&prm.maps.wd, a.w_down, a.E, a.d, a.I);
-  if (a.s > 0) {
-    ok &= w_map(&prm.maps.swg, a.ws_gate, a.s, a.I, a.d);
-    ok &= w_map(&prm.maps.swu, a.ws_up, a.s, a.I, a.d);
-    ok &= w_map(&prm.maps.swd, a.ws_down, a.s, a.d, a.I);
+  // Everything the tensor maps depend on; a recent call with the same key
+  // reuses its maps.
+  struct Key {
+    const void* p[13];
+    int v[8];
+  } key;
+  memset(&key, 0, sizeof key);
+  const void* kp[13] = {a.w_gate, a.w_up, a.w_down, a.ws_gate, a.ws_up, a.ws_down, a.xg16,
+                        a.xg16lo, a.x16, a.x16lo, a.h16, a.h16lo, nullptr};
+  memcpy(key.p, kp, sizeof kp);
+  const int kv[8] = {a.d, a.I, a.E, a.k, a.s, a.n, a.engine, dev};
+  memcpy(key.v, kv, sizeof kv);
+  static RecentCache<Key, Maps> cache;
+  if (!cache.get(key, &prm.maps)) {
+    if (!build_maps(a, &prm.maps)) return cudaErrorInvalidValue;
+    cache.put(key, prm.maps);
   }
-  // Phase-0 token rows: x gathered in union order (dedup) or x itself
-  // (per-slot: an entry's row is its token); shared experts read x.
-  const uint16_t* xa = a.engine == 1 ? a.xg16 : a.x16;
-  const uint16_t* xa_lo = a.engine == 1 ? a.xg16lo : a.x16lo;
-  const int xa_rows = a.engine == 1 ? P : a.n;
-  for (int si = 0; si < 3; ++si) {
-    const int br = 8 << si;
-    CUtensorMap* B = prm.maps.b[si];
-    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br);
-    ok &= b_map(&B[kXALo], xa_lo, xa_rows, a.d, br);
-    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br);
-    ok &= b_map(&B[kXSLo], a.x16lo, a.n, a.d, br);
-    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br);
-    ok &= b_map(&B[kHLo], a.h16lo, hrows, a.I, br);
-  }
-  if (!ok) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(num_sms);

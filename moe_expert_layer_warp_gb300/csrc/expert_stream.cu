@@ -434,11 +434,37 @@ bool act_map(CUtensorMap* m, const float* p, int rows, int K, int ks, int box_ro
   return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dims, strides, box);
 }
 
+// Every tensor map of one launch.
+template <int WB>
+bool build_maps(const ExpertArgs& a, Maps* M) {
+  memset(M, 0, sizeof *M);
+  constexpr int ks = Layout<WB>::KS;
+  const int P = a.n * a.k;
+  const int hrows = P + a.s * a.n;
+  bool ok = true;
+  ok &= weight_map(&M->w0, a.w_gate, WB, a.E, a.I, a.d, kRowsPhase0);
+  ok &= weight_map(&M->w1, a.w_up, WB, a.E, a.I, a.d, kRowsPhase0);
+  ok &= weight_map(&M->w2, a.w_down, WB, a.E, a.d, a.I, kRowsPhase1);
+  if (a.s > 0) {
+    ok &= weight_map(&M->sw0, a.ws_gate, WB, a.s, a.I, a.d, kRowsPhase0);
+    ok &= weight_map(&M->sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
+    ok &= weight_map(&M->sw2, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
+  }
+  const float* xa = a.engine == 0 ? a.x : a.xg;
+  const int xa_rows = a.engine == 0 ? a.n : P;
+  ok &= act_map(&M->a1, xa, xa_rows, a.d, ks, 1);
+  ok &= act_map(&M->aM, xa, xa_rows, a.d, ks, kMaxM);
+  ok &= act_map(&M->s1, a.x, a.n, a.d, ks, 1);
+  ok &= act_map(&M->sM, a.x, a.n, a.d, ks, kMaxM);
+  ok &= act_map(&M->h1, a.h, hrows, a.I, ks, 1);
+  ok &= act_map(&M->hM, a.h, hrows, a.I, ks, kMaxM);
+  return ok;
+}
+
 template <int WB>
 cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   auto kern = expert_engine_kernel<WB>;
   constexpr int bytes = Layout<WB>::kBytes;
-  constexpr int ks = Layout<WB>::KS;
   static int configured_device = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -450,26 +476,22 @@ cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream)
   Params prm;
   memset(&prm, 0, sizeof prm);
   prm.a = a;
-  const int P = a.n * a.k;
-  const int hrows = P + a.s * a.n;
-  bool ok = true;
-  ok &= weight_map(&prm.maps.w0, a.w_gate, WB, a.E, a.I, a.d, kRowsPhase0);
-  ok &= weight_map(&prm.maps.w1, a.w_up, WB, a.E, a.I, a.d, kRowsPhase0);
-  ok &= weight_map(&prm.maps.w2, a.w_down, WB, a.E, a.d, a.I, kRowsPhase1);
-  if (a.s > 0) {
-    ok &= weight_map(&prm.maps.sw0, a.ws_gate, WB, a.s, a.I, a.d, kRowsPhase0);
-    ok &= weight_map(&prm.maps.sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
-    ok &= weight_map(&prm.maps.sw2, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
+  // Everything the tensor maps depend on; an earlier call with the same key
+  // reuses its maps.
+  struct Key {
+    const void* p[9];
+    int v[8];
+  } key;
+  memset(&key, 0, sizeof key);
+  const void* kp[9] = {a.w_gate, a.w_up, a.w_down, a.ws_gate, a.ws_up, a.ws_down, a.x, a.xg, a.h};
+  memcpy(key.p, kp, sizeof kp);
+  const int kv[8] = {a.d, a.I, a.E, a.k, a.s, a.n, a.engine, dev};
+  memcpy(key.v, kv, sizeof kv);
+  static RecentCache<Key, Maps> cache;
+  if (!cache.get(key, &prm.maps)) {
+    if (!build_maps<WB>(a, &prm.maps)) return cudaErrorInvalidValue;
+    cache.put(key, prm.maps);
   }
-  const float* xa = a.engine == 0 ? a.x : a.xg;
-  const int xa_rows = a.engine == 0 ? a.n : P;
-  ok &= act_map(&prm.maps.a1, xa, xa_rows, a.d, ks, 1);
-  ok &= act_map(&prm.maps.aM, xa, xa_rows, a.d, ks, kMaxM);
-  ok &= act_map(&prm.maps.s1, a.x, a.n, a.d, ks, 1);
-  ok &= act_map(&prm.maps.sM, a.x, a.n, a.d, ks, kMaxM);
-  ok &= act_map(&prm.maps.h1, a.h, hrows, a.I, ks, 1);
-  ok &= act_map(&prm.maps.hM, a.h, hrows, a.I, ks, kMaxM);
-  if (!ok) return cudaErrorInvalidValue;
   // Programmatic dependent launch: the engine's prologue overlaps the prep
   // kernel; its griddepcontrol.wait orders every use of the prep's outputs.
   cudaLaunchConfig_t cfg;

@@ -86,4 +86,35 @@ inline bool make_tmap(CUtensorMap* out, const void* ptr, CUtensorMapDataType dty
   return true;
 }
 
+// Values computed for recent keys, compared bytewise (Key must be a POD:
+// zero it before filling it, so padding compares equal). A launcher keeps its
+// whole set of tensor maps here, so that a call with the same pointers and
+// sizes as an earlier one reuses them with one lookup. Bounded: cleared when
+// it passes 1024 entries.
+template <class Key, class Val>
+class RecentCache {
+ public:
+  bool get(const Key& k, Val* v) {
+    std::lock_guard<std::mutex> lock(mu_);
+    auto it = map_.find(Bytes(k));
+    if (it == map_.end()) return false;
+    *v = it->second;
+    return true;
+  }
+  void put(const Key& k, const Val& v) {
+    std::lock_guard<std::mutex> lock(mu_);
+    if (map_.size() >= 1024) map_.clear();
+    map_[Bytes(k)] = v;
+  }
+
+ private:
+  struct Bytes {
+    Key k;
+    explicit Bytes(const Key& key) : k(key) {}
+    bool operator<(const Bytes& o) const { return memcmp(&k, &o.k, sizeof(Key)) < 0; }
+  };
+  std::mutex mu_;
+  std::map<Bytes, Val> map_;
+};
+
 }  // namespace moe

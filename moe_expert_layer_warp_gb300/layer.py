@@ -4,9 +4,12 @@
 union, slot outputs, output) for passes of up to ``n_max`` tokens and calls
 the library's entry points in order: moe_route → moe_build_union →
 moe_verify_perslot or moe_verify_dedup → moe_combine. Buffers are allocated
-once, through torch, at construction.
+once, through torch, at construction, and so are the C arguments that point
+at them: a call only marshals x and the stream.
 """
 from __future__ import annotations
+
+import ctypes
 
 import torch
 
@@ -48,41 +51,82 @@ class PassRunner:
                                                      self.pair_slot, self.bytes)))
         self.y_slot = torch.empty(n_max * (k + s) * d, **f32)
         self.y = torch.empty(n_max * d, **f32)
+        # C arguments fixed for the runner's lifetime
+        V = ctypes.c_void_p
+        self._lib = api.load()
+        self._desc = ctypes.byref(self.desc)
+        self._wref = ctypes.byref(self.wc)
+        self._uref = ctypes.byref(self.u)
+        self._ws = V(self.workspace.data_ptr())
+        self._ws_bytes = nbytes
+        self._router = V(weights.w_router.data_ptr())
+        self._idx = V(self.topk_idx.data_ptr())
+        self._tw = V(self.topk_w.data_ptr())
+        self._yslot = V(self.y_slot.data_ptr())
+        self._y = V(self.y.data_ptr())
+
+    def _x(self, x: torch.Tensor) -> ctypes.c_void_p:
+        n = x.shape[0]
+        if (x.dtype != torch.float32 or x.dim() != 2 or x.shape[1] != self.shape.d or
+                n > self.n_max or n < 1 or x.device != self.weights.device or
+                not x.is_contiguous()):
+            raise ValueError("x must be a contiguous float32 [1..%d][%d] tensor on %s"
+                             % (self.n_max, self.shape.d, self.weights.device))
+        return ctypes.c_void_p(x.data_ptr())
 
     # -- single steps ---------------------------------------------------------
-    def route(self, x: torch.Tensor, stream=None):
-        n = x.shape[0]
-        api.moe_route(self.desc, self.weights.w_router, x, n, self.topk_idx, self.topk_w,
-                      self.workspace, stream)
+    def route(self, x: torch.Tensor, stream=None, _xp=None):
+        xp = _xp or self._x(x)
+        api._check(self._lib.moe_route(self._desc, self._router, xp, x.shape[0], self._idx,
+                                       self._tw, self._ws, self._ws_bytes, api._stream(stream)),
+                   "moe_route")
 
     def build_union(self, n: int, stream=None):
-        api.moe_build_union(self.desc, self.topk_idx, n, self.u, stream)
+        api._check(self._lib.moe_build_union(self._desc, self._idx, n, self._uref,
+                                             api._stream(stream)), "moe_build_union")
 
-    def experts(self, x: torch.Tensor, engine: str, stream=None):
+    def experts(self, x: torch.Tensor, engine: str, stream=None, _xp=None):
+        xp = _xp or self._x(x)
         n = x.shape[0]
+        st = api._stream(stream)
         if engine == PERSLOT:
-            api.moe_verify_perslot(self.desc, self.wc, x, n, self.topk_idx, self.topk_w,
-                                   self.workspace, self.y_slot, stream)
+            api._check(self._lib.moe_verify_perslot(self._desc, self._wref, xp, n, self._idx,
+                                                    self._tw, self._ws, self._ws_bytes,
+                                                    self._yslot, st), "moe_verify_perslot")
         elif engine == DEDUP:
-            api.moe_verify_dedup(self.desc, self.wc, x, n, self.u, self.topk_w, self.workspace,
-                                 self.y_slot, stream)
+            api._check(self._lib.moe_verify_dedup(self._desc, self._wref, xp, n, self._uref,
+                                                  self._tw, self._ws, self._ws_bytes,
+                                                  self._yslot, st), "moe_verify_dedup")
         else:
             raise ValueError("engine must be %r or %r" % (PERSLOT, DEDUP))
 
-    def combine(self, n: int, stream=None):
-        api.moe_combine(self.desc, self.y_slot, n, self.y, stream)
+    def combine(self, n: int, stream=None, out: torch.Tensor = None):
+        y = self._y
+        if out is not None:
+            if (out.dtype != torch.float32 or out.numel() != n * self.shape.d or
+                    out.device != self.weights.device or not out.is_contiguous()):
+                raise ValueError("out must be a contiguous float32 [%d][%d] tensor on %s"
+                                 % (n, self.shape.d, self.weights.device))
+            y = ctypes.c_void_p(out.data_ptr())
+        api._check(self._lib.moe_combine(self._desc, self._yslot, n, y, api._stream(stream)),
+                   "moe_combine")
 
     # -- a whole pass ---------------------------------------------------------
-    def forward(self, x: torch.Tensor, engine: str = DEDUP, stream=None) -> torch.Tensor:
-        """y [n][d] for the pass x [n][d] (fp32, on the layer's device)."""
+    def forward(self, x: torch.Tensor, engine: str = DEDUP, stream=None,
+                out: torch.Tensor = None) -> torch.Tensor:
+        """y [n][d] for the pass x [n][d] (fp32, on the layer's device),
+        written to `out` if given (a contiguous fp32 [n][d] device tensor),
+        else to the runner's own buffer (overwritten by its next pass)."""
+        xp = self._x(x)
+        if engine not in (PERSLOT, DEDUP):
+            raise ValueError("engine must be %r or %r" % (PERSLOT, DEDUP))
         n = x.shape[0]
-        if x.dtype != torch.float32 or x.shape[1] != self.shape.d or n > self.n_max:
-            raise ValueError("x must be float32 [n<=%d][%d]" % (self.n_max, self.shape.d))
-        self.route(x, stream)
-        self.build_union(n, stream)
-        self.experts(x, engine, stream)
-        self.combine(n, stream)
-        return self.y[: n * self.shape.d].view(n, self.shape.d)
+        st = api._stream(stream)
+        self.route(x, st, xp)
+        self.build_union(n, st)
+        self.experts(x, engine, st, xp)
+        self.combine(n, st, out)
+        return out if out is not None else self.y[: n * self.shape.d].view(n, self.shape.d)
 
     # -- views ---------------------------------------------------------------
     def routing(self, n: int):
