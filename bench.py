@@ -595,17 +595,18 @@ def run_reference(args):
 
 
 STACK_DRAFT_COST_RATIO = 0.1601   # draft/verify cost ratio c the pages derive from FLOPs
-STACK_FIT_REPS = 4
+STACK_FIT_PASSES = 4   # held-out passes (own seeds) per (rho, n) for the bandwidth fit
 STACK_REPS = 3
 
 
 def run_stack(args):
     """26 V2-Lite-shaped layers (~30 GB), each fed the same pass, at n = 1..9
-    and rho in {0, 0.5, 0.9, 0.99}. The bandwidths are fitted on layer 0's
-    expert call run alone (L2 flushed before each pass); the stack's pass time
-    is predicted from every layer's requested bytes over those bandwidths plus
-    the fixed time, and compared with the measured stack pass. Prints one
-    JSON line."""
+    and rho in {0, 0.5, 0.9, 0.99}. Per rho, the bandwidths are fitted on
+    layer 0's expert call run alone (L2 flushed before each pass) over
+    STACK_FIT_PASSES held-out passes (own seeds) at that rho; each stack pass
+    is predicted from every layer's requested bytes over those bandwidths
+    plus the fixed time, and compared with the measured stack pass. Prints
+    one JSON line."""
     import torch
     from __graft_entry__ import build
     build()
@@ -618,55 +619,68 @@ def run_stack(args):
     runners = [PassRunner(L, max(w.pass_sizes)) for L in layers]
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    xs = {(ri, n): torch.from_numpy(synth.make_pass(w.shape.d, n, rho,
-                                                    [w.x_seed_base + 100 * ri + n])).to(dev)
-          for ri, rho in enumerate(w.rhos) for n in w.pass_sizes}
     engines = ("perslot", "dedup")
+
+    def make_x(ri, rho, n, f):
+        return torch.from_numpy(synth.make_pass(w.shape.d, n, rho, [
+            w.x_seed_base + 100 * ri + 10000 * f + n])).to(dev)
+
+    xs = {(ri, n): make_x(ri, rho, n, 0) for ri, rho in enumerate(w.rhos) for n in w.pass_sizes}
+    fit_xs = {(ri, n): [make_x(ri, rho, n, 1 + f) for f in range(STACK_FIT_PASSES)]
+              for ri, rho in enumerate(w.rhos) for n in w.pass_sizes}
 
     def req_bytes(R, eng):
         b = [int(v) for v in R.bytes.cpu().tolist()]
         return (b[0] if eng == "perslot" else b[1]) + b[2]
 
-    for (ri, n), x in xs.items():          # warm-up: every pass once through the stack
-        for eng in engines:
+    for (ri, n), x in xs.items():          # warm-up: every pass once through the stack,
+        for eng in engines:                # every fitted pass once through layer 0
             for R in runners:
                 R.forward(x, eng, stream)
+            for xf in fit_xs[(ri, n)]:
+                runners[0].forward(xf, eng, stream)
     torch.cuda.synchronize()
     if api.moe_last_device_error() != api.MOE_OK:
         raise RuntimeError("device error during warm-up")
 
-    # fit on layer 0 run alone
     R0 = runners[0]
-    samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
-    tfix = {n: [] for n in w.pass_sizes}
-    for rep in range(STACK_FIT_REPS):
-        for (ri, n), x in xs.items():
-            for eng in engines:
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-                flush.zero_()
-                torch.cuda._sleep(SPIN_CYCLES)
-                ev[0].record(stream)
-                R0.route(x, stream)
-                R0.build_union(n, stream)
-                ev[1].record(stream)
-                R0.experts(x, eng, stream)
-                ev[2].record(stream)
-                R0.combine(n, stream)
-                ev[3].record(stream)
-                torch.cuda.synchronize()
-                t_exp = ev[1].elapsed_time(ev[2]) * 1e-3
-                samples[eng][n].append((req_bytes(R0, eng), t_exp))
-                tfix[n].append(ev[0].elapsed_time(ev[3]) * 1e-3 - t_exp)
-    t_fix = {n: statistics.median(v) for n, v in tfix.items()}
-    fits = {e: stepmodel.EngineFit({n: stepmodel.effective_bandwidth(
-        [b for b, _ in samples[e][n]], [t for _, t in samples[e][n]]) for n in w.pass_sizes},
-        t_fix) for e in engines}
-    eps = {e: {n: stepmodel.bandwidth_spread(samples[e][n]) for n in w.pass_sizes}
-           for e in engines}
-
-    # the stack: measured passes and their per-layer requested bytes
-    per_rho = []
+    per_rho, fits_out = [], []
     for ri, rho in enumerate(w.rhos):
+        # fit on layer 0 run alone, held-out passes at this rho
+        samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
+        tfix = {n: [] for n in w.pass_sizes}
+        for n in w.pass_sizes:
+            for x in fit_xs[(ri, n)]:
+                for eng in engines:
+                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                    flush.zero_()
+                    torch.cuda._sleep(SPIN_CYCLES)
+                    ev[0].record(stream)
+                    R0.route(x, stream)
+                    R0.build_union(n, stream)
+                    ev[1].record(stream)
+                    R0.experts(x, eng, stream)
+                    ev[2].record(stream)
+                    R0.combine(n, stream)
+                    ev[3].record(stream)
+                    torch.cuda.synchronize()
+                    t_exp = ev[1].elapsed_time(ev[2]) * 1e-3
+                    samples[eng][n].append((req_bytes(R0, eng), t_exp))
+                    tfix[n].append(ev[0].elapsed_time(ev[3]) * 1e-3 - t_exp)
+        t_fix = {n: statistics.median(v) for n, v in tfix.items()}
+        fits = {e: stepmodel.EngineFit({n: stepmodel.effective_bandwidth(
+            [b for b, _ in samples[e][n]], [t for _, t in samples[e][n]]) for n in w.pass_sizes},
+            t_fix) for e in engines}
+        eps = {e: {n: stepmodel.bandwidth_spread(samples[e][n]) for n in w.pass_sizes}
+               for e in engines}
+        fits_out.append({
+            "rho": rho,
+            "bw_perslot_GBs": [round(fits["perslot"].bw[n] / 1e9, 1) for n in w.pass_sizes],
+            "bw_dedup_GBs": [round(fits["dedup"].bw[n] / 1e9, 1) for n in w.pass_sizes],
+            "eps_perslot": [round(eps["perslot"][n], 4) for n in w.pass_sizes],
+            "eps_dedup": [round(eps["dedup"][n], 4) for n in w.pass_sizes],
+            "t_fix_us": [round(t_fix[n] * 1e6, 2) for n in w.pass_sizes]})
+        # the stack: measured passes and their per-layer requested bytes
         meas = {e: {} for e in engines}
         pred = {e: {} for e in engines}
         bound = {}
@@ -702,13 +716,8 @@ def run_stack(args):
         "stack": "deepseek-v2-lite-shaped 26-layer MoE stack (expert layers only, each fed "
                  "the same pass), bf16 weights, %.1f GB of expert weights" % (
                      w.layers * (w.shape.n_experts + w.shape.n_shared) * EXPERT_BYTES / 1e9),
-        "fit": {"layer": 0, "passes_per_point": STACK_FIT_REPS * len(w.rhos),
-                "l2": "flushed (256 MB write) before each fitted pass",
-                "bw_perslot_GBs": [round(fits["perslot"].bw[n] / 1e9, 1) for n in w.pass_sizes],
-                "bw_dedup_GBs": [round(fits["dedup"].bw[n] / 1e9, 1) for n in w.pass_sizes],
-                "eps_perslot": [round(eps["perslot"][n], 4) for n in w.pass_sizes],
-                "eps_dedup": [round(eps["dedup"][n], 4) for n in w.pass_sizes],
-                "t_fix_us": [round(t_fix[n] * 1e6, 2) for n in w.pass_sizes]},
+        "fit": {"layer": 0, "passes_per_point": STACK_FIT_PASSES,
+                "l2": "flushed (256 MB write) before each fitted pass", "per_rho": fits_out},
         "per_rho": per_rho,
     }), flush=True)
 

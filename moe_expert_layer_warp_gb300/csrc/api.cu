@@ -83,11 +83,12 @@ moe_status check_n(const moe_layer_desc* d, int32_t n) {
 //   xg       [n_max·k][d] fp32        x rows gathered in union order
 //   xg16     [2][n_max·k][d] bf16     their hi and lo bf16 halves
 //   x16      [2][n_max][d] bf16       hi and lo bf16 halves of x
+//   x32      [n_max][d] fp32          a copy of x (CUDA-core kernel input)
 //   sync     [kCcSyncInts] int32      CUDA-core kernel job counter, group counts
 //   sync_mma [kMmaSyncInts] int32     tensor-core kernel job counter, group counts, piece counts
 //   part     [kMmaPartBytes]           tensor-core kernel partial sums of K pieces (bf16 layers)
 struct WsLayout {
-  size_t logits, h, h16, xg, xg16, x16, sync, sync_mma, part, part_bytes, total;
+  size_t logits, h, h16, xg, xg16, x16, x32, sync, sync_mma, part, part_bytes, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -109,6 +110,8 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   off = align256(off + 2 * pairs * d->d * 2);
   L.x16 = off;
   off = align256(off + 2 * (size_t)n_max * d->d * 2);
+  L.x32 = off;
+  off = align256(off + (size_t)n_max * d->d * 4);
   L.sync = off;
   off = align256(off + (size_t)moe::kCcSyncInts * 4);
   L.sync_mma = off;
@@ -264,6 +267,7 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   a.xg16lo = a.xg16 + (size_t)n * desc->top_k * desc->d;
   a.x16 = reinterpret_cast<uint16_t*>(ws + L.x16);
   a.x16lo = a.x16 + (size_t)n * desc->d;
+  a.x32 = reinterpret_cast<float*>(ws + L.x32);
   a.sync = reinterpret_cast<int*>(ws + L.sync);
   a.sync_mma = reinterpret_cast<int*>(ws + L.sync_mma);
   a.part = reinterpret_cast<float*>(ws + L.part);

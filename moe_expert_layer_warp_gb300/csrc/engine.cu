@@ -19,14 +19,16 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
 // starts (programmatic dependent launch); they wait for it before touching
 // its outputs. The grid zeroes both kernels' job counters and group counts.
 // Blocks [0, gather_rows): xg[r] = x[pair_tok[r]] (fp32) and its bf16 hi/lo
-// halves (dedup, union order). Blocks [gather_rows, gather_rows + n): the
-// bf16 hi/lo halves of x. hi = bf16(v), lo = bf16(v − hi).
+// halves (dedup, union order). Blocks [gather_rows, gather_rows + n): x32 =
+// a copy of x and, for bf16 layers, the bf16 hi/lo halves of x.
+// hi = bf16(v), lo = bf16(v − hi).
 __global__ void __launch_bounds__(256)
-    engine_prep_kernel(int d, int n, int gather_rows, const float* __restrict__ x,
+    engine_prep_kernel(int d, int n, int gather_rows, int halves, const float* __restrict__ x,
                        const int32_t* __restrict__ pair_tok, float* __restrict__ xg,
                        uint16_t* __restrict__ xg16, uint16_t* __restrict__ xg16lo,
-                       uint16_t* __restrict__ x16, uint16_t* __restrict__ x16lo,
-                       int* __restrict__ sync_cc, int* __restrict__ sync_mma) {
+                       float* __restrict__ x32, uint16_t* __restrict__ x16,
+                       uint16_t* __restrict__ x16lo, int* __restrict__ sync_cc,
+                       int* __restrict__ sync_mma) {
   pdl_wait();     // the union (dedup) or routing that precedes it
   pdl_trigger();
   {  // counters, spread over the grid (int4 stores; both regions are 256-byte aligned)
@@ -46,14 +48,17 @@ __global__ void __launch_bounds__(256)
     lo = xg16lo + (size_t)b * d;
   } else if (b < gather_rows + n) {
     src = x + (size_t)(b - gather_rows) * d;
+    dst32 = x32 + (size_t)(b - gather_rows) * d;
     hi = x16 + (size_t)(b - gather_rows) * d;
     lo = x16lo + (size_t)(b - gather_rows) * d;
+    if (!halves) hi = lo = nullptr;
   } else {
     return;
   }
   for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
     const float4 v = __ldg(reinterpret_cast<const float4*>(src) + i);
-    if (dst32) reinterpret_cast<float4*>(dst32)[i] = v;
+    reinterpret_cast<float4*>(dst32)[i] = v;
+    if (!hi) continue;
     const uint2 h = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
     const uint2 l = make_uint2(pack_bf16x2(v.x - bf16lo(h.x), v.y - bf16hi(h.x)),
                                pack_bf16x2(v.z - bf16lo(h.y), v.w - bf16hi(h.y)));
@@ -66,10 +71,9 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
   const int gather = a.engine == 1 ? a.n * a.k : 0;
-  const int convert = a.wdtype == 1 ? a.n : 0;
-  cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + convert, 4)), dim3(256), 0,
-                             stream, a.d, convert, gather, a.x, a.pair_tok, a.xg, a.xg16,
-                             a.xg16lo, a.x16, a.x16lo, a.sync, a.sync_mma);
+  cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + a.n, 4)), dim3(256), 0, stream,
+                             a.d, a.n, gather, a.wdtype == 1 ? 1 : 0, a.x, a.pair_tok, a.xg,
+                             a.xg16, a.xg16lo, a.x32, a.x16, a.x16lo, a.sync, a.sync_mma);
   if (e != cudaSuccess) return e;
   // The tensor-core kernel runs only where a group can reach mma_min_m
   // tokens: a group never holds more than the pass's n tokens, and per-slot

@@ -450,12 +450,12 @@ bool build_maps(const ExpertArgs& a, Maps* M) {
     ok &= weight_map(&M->sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
     ok &= weight_map(&M->sw2, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
   }
-  const float* xa = a.engine == 0 ? a.x : a.xg;
+  const float* xa = a.engine == 0 ? a.x32 : a.xg;
   const int xa_rows = a.engine == 0 ? a.n : P;
   ok &= act_map(&M->a1, xa, xa_rows, a.d, ks, 1);
   ok &= act_map(&M->aM, xa, xa_rows, a.d, ks, kMaxM);
-  ok &= act_map(&M->s1, a.x, a.n, a.d, ks, 1);
-  ok &= act_map(&M->sM, a.x, a.n, a.d, ks, kMaxM);
+  ok &= act_map(&M->s1, a.x32, a.n, a.d, ks, 1);
+  ok &= act_map(&M->sM, a.x32, a.n, a.d, ks, kMaxM);
   ok &= act_map(&M->h1, a.h, hrows, a.I, ks, 1);
   ok &= act_map(&M->hM, a.h, hrows, a.I, ks, kMaxM);
   return ok;
@@ -483,7 +483,7 @@ cudaError_t launch_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream)
     int v[8];
   } key;
   memset(&key, 0, sizeof key);
-  const void* kp[9] = {a.w_gate, a.w_up, a.w_down, a.ws_gate, a.ws_up, a.ws_down, a.x, a.xg, a.h};
+  const void* kp[9] = {a.w_gate, a.w_up, a.w_down, a.ws_gate, a.ws_up, a.ws_down, a.x32, a.xg, a.h};
   memcpy(key.p, kp, sizeof kp);
   const int kv[8] = {a.d, a.I, a.E, a.k, a.s, a.n, a.engine, dev};
   memcpy(key.v, kv, sizeof kv);

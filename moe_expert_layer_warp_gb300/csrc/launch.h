@@ -60,6 +60,8 @@ struct ExpertArgs {
   const void* ws_down;
   float* h;             // [n·k + s·n][I] fp32 scratch (CUDA-core groups)
   float* xg;            // [n·k][d] fp32 scratch: x rows gathered in union order (dedup)
+  float* x32;           // [n][d] fp32 scratch: a copy of x, so that the CUDA-core kernel's
+                        //   tensor maps point into the workspace only
   uint16_t* h16;        // [n·k + s·n][I] bf16 scratch (tensor-core groups): hi half of h
   uint16_t* h16lo;      //   and lo half: h = hi + lo to ~16 extra mantissa bits
   uint16_t* xg16;       // [n·k][d] bf16 scratch: hi half of xg

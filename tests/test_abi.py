@@ -51,7 +51,8 @@ def test_workspace_bytes_closed_form(lib):
         hrows = n * sh.top_k + sh.n_shared * n
         want = (a256(n * sh.n_experts * 4) + a256(hrows * sh.inter * 4) + a256(2 * hrows * sh.inter * 2)
                 + a256(n * sh.top_k * sh.d * 4) + a256(2 * n * sh.top_k * sh.d * 2)
-                + a256(2 * n * sh.d * 2) + a256(CC_SYNC_INTS * 4) + a256(MMA_SYNC_INTS * 4)
+                + a256(2 * n * sh.d * 2) + a256(n * sh.d * 4) + a256(CC_SYNC_INTS * 4)
+                + a256(MMA_SYNC_INTS * 4)
                 + (MMA_PART_BYTES if sh.wdtype == W_BF16 else 0))
         assert got == want, w.name
 
