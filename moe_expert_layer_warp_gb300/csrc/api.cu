@@ -126,18 +126,20 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
 // Which expert kernel a bf16 call runs on; the two never share a call (run
 // side by side they slow each other). The tensor-core kernel streams each
 // weight tile through shared memory into the tensor cores with no
-// per-element instruction, but it needs about four 128-row tiles per SM;
-// with fewer it cuts tiles along K, and adding the pieces across CTAs costs
-// a few microseconds of synchronisation behind the CTAs' own streams. The
-// CUDA-core kernel works in 16- and 32-row tiles and needs no such step. So
-// a call goes to the tensor cores once its groups hold at least
-// kMmaMinTiles tiles (gate/up plus down tiles per group). The groups of a
-// dedup call are known only on the device; the estimate takes half of
-// min(E, n·k) distinct experts, the middle of the range the union spans for
-// correlated hidden states. MOE_MMA_MIN_M in the environment (read once; for
-// tuning) fixes instead the smallest group that runs on the tensor cores.
-constexpr int kMmaMinTiles = 360;
-
+// per-element instruction, so it keeps its rate however many tokens a group
+// holds; but it works in 128-row tiles, a group's down tiles wait for all of
+// its gate/up tiles, and with fewer tiles than SMs it must cut tiles along K
+// and add the pieces across CTAs. The CUDA-core kernel works in 16- and
+// 32-row tiles, so few groups still fill the GPU, but its arithmetic per
+// weight byte grows with the tokens per group. Measured on GB300
+// (DeepSeek-V2-Lite- and Mixtral-shaped layers): one-token groups
+// (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups; dedup
+// groups, which hold several tokens, go faster on the tensor cores from
+// ~350 tiles with 12 groups or more, or with 3 tokens or more per group.
+// The groups of a dedup call are known only on the device: the estimate
+// takes half of min(E, n·k) distinct experts. MOE_MMA_MIN_M in the
+// environment (read once; for tuning) fixes instead the smallest group
+// that runs on the tensor cores.
 int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   static const int forced = [] {
     const char* e = getenv("MOE_MMA_MIN_M");
@@ -145,10 +147,19 @@ int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
     return x >= 1 ? x : 0;
   }();
   if (forced) return forced;
-  const int tiles = (d->inter + 127) / 128 + (d->d + 127) / 128;
-  const int routed = engine == 0 ? n * d->top_k : std::min(d->n_experts, n * d->top_k) / 2;
-  const int groups = routed + d->n_shared * ((n + moe::kMmaSub - 1) / moe::kMmaSub);
-  return groups * tiles >= kMmaMinTiles ? 1 : 0x7fffffff;
+  const int tiles = (d->inter + 127) / 128 + (d->d + 127) / 128;  // per group
+  const int pairs = n * d->top_k;
+  const int shared = d->n_shared * ((n + moe::kMmaSub - 1) / moe::kMmaSub);
+  bool mma;
+  if (engine == 0) {
+    const int groups = pairs + shared;
+    mma = groups * tiles >= 400 && groups >= 12;
+  } else {
+    const int routed = std::max(1, std::min(d->n_experts, pairs) / 2);
+    const int groups = routed + shared;
+    mma = groups * tiles >= 350 && (groups >= 12 || pairs >= 3 * routed);
+  }
+  return mma ? 1 : 0x7fffffff;
 }
 
 moe_status check_ws(const moe_layer_desc* d, int32_t n, const void* ws, size_t ws_bytes) {

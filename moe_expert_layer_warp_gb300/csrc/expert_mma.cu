@@ -68,7 +68,7 @@ constexpr int kMaxEntries = max_entries(kSub);
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
 constexpr int kSlotCols = 128;                      // TMEM columns per accumulator slot (gate, up)
 constexpr int kTmemCols = 2 * kSlotCols;
-constexpr int kJobsPerCta = 4;                      // pieces are cut until a phase has this many jobs per CTA
+constexpr int kJobsPerCta = 1;                      // tiles are cut only while a phase has fewer than one per CTA
 constexpr int kMaxPieces = 8;
 static_assert(kMaxEntries == kMmaEntries, "tensor-core kernel entry count");
 static_assert(kSub == 32, "the epilogue and the TMEM slots assume at most 32 tokens");
