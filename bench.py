@@ -75,7 +75,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        import tempfile
+        self.path = os.environ.get("MOE_CLOCKS_LOG") or os.path.join(
+            tempfile.gettempdir(), "moe_clocks_rank%d.csv" % gpu_index)
 
     def start(self):
         try:

@@ -16,13 +16,16 @@
  *       Σ weight·expert(x).
  *   [S] same post, §5 "DeepSeek-V3 and the Current State of the Art", routing
  *       sketch: output starts from the sum of the always-on shared experts.
+ *   [G'] same post, §5, routing sketch: a per-expert bias added to the gate's
+ *       scores before the top-k; the sketch takes the softmax over the kept
+ *       biased scores.
  *   [D] same post, §1 "1991: Where It Started": the dense mixture, where every
  *       expert runs and the gate weights combine them.
  *   [B] "Speculative Decoding for Mixture-of-Experts Models: Expert Bytes,
  *       Kernel Bandwidth and the Best Draft Length", abstract: per-slot bytes
  *       (an expert read once per token) and dedup bytes (each selected expert
  *       read once per pass).
- * Readings where the sources are silent (each one also listed in the design doc):
+ * Readings where the sources are silent:
  *   - experts are SwiGLU FFNs without biases: W_down(silu(W_gate x) ⊙ W_up x),
  *     silu(z) = z/(1+exp(-z)); the sources never define the expert body.
  *   - equal logits are ordered by ascending expert index (ties select the
@@ -95,21 +98,45 @@ static int by_logit_then_index(const void* pa, const void* pb) {
  *              first expert left out; +inf when k == E and k == 1). A GPU
  *              evaluation whose logit error is below gap/2 orders these
  *              positions exactly as this function does.                    */
+int oracle_topk_biased(int E, int k, int n, const double* logits, const double* bias,
+                       int bias_in_weights, int32_t* idx, double* w, double* gap);
+
 int oracle_topk(int E, int k, int n, const double* logits, int32_t* idx, double* w, double* gap) {
+  return oracle_topk_biased(E, k, n, logits, NULL, 1, idx, w, gap);
+}
+
+/* [G'] the DeepSeek-style routing sketch: a per-expert bias b_e is added to
+ * the gate's scores and the top k of l_e + b_e are selected (ties -> lower
+ * index). bias_in_weights = 1 takes the softmax over the k kept biased
+ * scores, as the sketch writes it; 0 takes it over the kept experts'
+ * unbiased logits (bias for selection only). bias == NULL is no bias. gap is
+ * that of the biased scores (the values the selection compares).          */
+int oracle_topk_biased(int E, int k, int n, const double* logits, const double* bias,
+                       int bias_in_weights, int32_t* idx, double* w, double* gap) {
   if (E <= 0 || k <= 0 || k > E || n <= 0 || !logits || !idx || !w) return 1;
   scored* s = (scored*)malloc(sizeof(scored) * (size_t)E);
-  if (!s) return 2;
+  double* u = (double*)malloc(sizeof(double) * (size_t)k);
+  if (!s || !u) {
+    free(s);
+    free(u);
+    return 2;
+  }
   for (int t = 0; t < n; ++t) {
     for (int e = 0; e < E; ++e) {
-      s[e].v = logits[(size_t)t * E + e];
+      s[e].v = logits[(size_t)t * E + e] + (bias ? bias[e] : 0.0);
       s[e].e = e;
     }
     qsort(s, (size_t)E, sizeof(scored), by_logit_then_index);
-    double lmax = s[0].v, z = 0.0;
-    for (int j = 0; j < k; ++j) z += exp(s[j].v - lmax);
+    /* the values the softmax runs over, and their maximum */
+    double umax = -INFINITY, z = 0.0;
+    for (int j = 0; j < k; ++j) {
+      u[j] = (bias && !bias_in_weights) ? logits[(size_t)t * E + s[j].e] : s[j].v;
+      if (u[j] > umax) umax = u[j];
+    }
+    for (int j = 0; j < k; ++j) z += exp(u[j] - umax);
     for (int j = 0; j < k; ++j) {
       idx[(size_t)t * k + j] = s[j].e;
-      w[(size_t)t * k + j] = exp(s[j].v - lmax) / z;
+      w[(size_t)t * k + j] = exp(u[j] - umax) / z;
     }
     if (gap) {
       int last = (k < E) ? k : E - 1;
@@ -122,6 +149,7 @@ int oracle_topk(int E, int k, int n, const double* logits, int32_t* idx, double*
     }
   }
   free(s);
+  free(u);
   return 0;
 }
 

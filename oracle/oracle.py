@@ -47,12 +47,13 @@ def bind(path: str):
     I = ctypes.c_int
     lib.oracle_gate_logits.argtypes = [I, I, I, P, P, P, P]
     lib.oracle_topk.argtypes = [I, I, I, P, P, P, P]
+    lib.oracle_topk_biased.argtypes = [I, I, I, P, P, I, P, P, P]
     lib.oracle_expert_ffn.argtypes = [I, I, I, P, P, P, P, P]
     lib.oracle_moe_token.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_dense_token.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P]
     lib.oracle_union.argtypes = [I, I, I, P, P, P, P, P, P]
     lib.oracle_bytes.argtypes = [I, I, I, I, I, I, I, P]
-    for f in (lib.oracle_gate_logits, lib.oracle_topk, lib.oracle_expert_ffn,
+    for f in (lib.oracle_gate_logits, lib.oracle_topk, lib.oracle_topk_biased, lib.oracle_expert_ffn,
               lib.oracle_moe_token, lib.oracle_dense_token, lib.oracle_union,
               lib.oracle_bytes):
         f.restype = ctypes.c_int
@@ -101,24 +102,33 @@ def gate_logits(x, w_router):
     return logits, absdot
 
 
-def topk(logits, k):
-    """Top-k (descending logit, ties -> lower index), softmax over the k kept
-    logits, and the smallest gap between consecutive sorted logits at
-    positions 0..k per token."""
+def topk(logits, k, bias=None, bias_in_weights=True):
+    """Top-k (descending score, ties -> lower index), softmax over the k kept
+    scores, and the smallest gap between consecutive sorted scores at
+    positions 0..k per token. With a per-expert bias (DeepSeek-style routing
+    sketch) the score is logit + bias; bias_in_weights=False takes the softmax
+    over the kept experts' unbiased logits instead (bias for selection only)."""
     logits = _c(logits, np.float64)
     n, E = logits.shape
     idx = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float64)
     gap = np.empty((n,), np.float64)
-    _check(_load().oracle_topk(E, k, n, _p(logits), _p(idx), _p(w), _p(gap)), "topk")
+    if bias is None:
+        _check(_load().oracle_topk(E, k, n, _p(logits), _p(idx), _p(w), _p(gap)), "topk")
+    else:
+        b = _c(bias, np.float64)
+        assert b.shape == (E,)
+        _check(_load().oracle_topk_biased(E, k, n, _p(logits), _p(b), 1 if bias_in_weights else 0,
+                                          _p(idx), _p(w), _p(gap)), "topk_biased")
     return idx, w, gap
 
 
-def route(x, w_router, k):
-    """Gate GEMV + top-k + renormalised softmax. Returns a dict with idx, w,
-    logits, absdot and gap."""
+def route(x, w_router, k, bias=None, bias_in_weights=True):
+    """Gate GEMV + top-k + renormalised softmax (optionally with a per-expert
+    routing bias, see topk). Returns a dict with idx, w, logits, absdot and
+    gap (of the scores the selection compares)."""
     logits, absdot = gate_logits(x, w_router)
-    idx, w, gap = topk(logits, k)
+    idx, w, gap = topk(logits, k, bias, bias_in_weights)
     return {"idx": idx, "w": w, "logits": logits, "absdot": absdot, "gap": gap}
 
 

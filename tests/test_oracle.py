@@ -307,3 +307,75 @@ def test_union_size_for_independent_tokens_is_plausible():
         sizes.append(oracle.union(oracle.route(x, L["wr"], 6)["idx"], 64)["count"])
     expect = 64 * (1 - (1 - 6 / 64) ** 8)
     assert abs(np.mean(sizes) - expect) < 0.2 * expect
+
+
+# -- routing bias (DeepSeek-style routing sketch, §5) -------------------------
+def _brute_topk(scores, k):
+    """Indices of the k largest scores, ties to the lower index (plain sort)."""
+    return [int(e) for e in sorted(range(len(scores)), key=lambda e: (-scores[e], e))[:k]]
+
+
+def _softmax(v):
+    v = np.asarray(v, np.float64)
+    z = np.exp(v - v.max())
+    return z / z.sum()
+
+
+@pytest.mark.parametrize("bias_in_weights", [True, False])
+def test_biased_topk_brute_force(bias_in_weights):
+    """Selection on logit + bias; weights the softmax of the kept biased
+    scores (the sketch as written) or of the kept unbiased logits."""
+    rng = np.random.default_rng(11)
+    E, k, n = 12, 3, 40
+    # multiples of 1/8 so every sum is exact and ties occur
+    logits = rng.integers(-16, 16, size=(n, E)) / 8.0
+    bias = rng.integers(-8, 8, size=E) / 8.0
+    idx, w, gap = oracle.topk(logits, k, bias, bias_in_weights)
+    for t in range(n):
+        sc = logits[t] + bias
+        want = _brute_topk(sc, k)
+        assert idx[t].tolist() == want
+        vals = sc[want] if bias_in_weights else logits[t][want]
+        np.testing.assert_allclose(w[t], _softmax(vals), rtol=0, atol=1e-15)
+        srt = sorted(sc, reverse=True)
+        assert gap[t] == min(srt[j] - srt[j + 1] for j in range(k))
+
+
+def test_zero_bias_equals_unbiased_routing():
+    rng = np.random.default_rng(3)
+    logits = rng.standard_normal((30, 16))
+    a = oracle.topk(logits, 4)
+    for mode in (True, False):
+        b = oracle.topk(logits, 4, np.zeros(16), mode)
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_constant_bias_changes_nothing():
+    """A bias equal on every expert shifts all scores alike: the selection is
+    unchanged and so are the weights (softmax is shift invariant)."""
+    rng = np.random.default_rng(5)
+    logits = rng.integers(-40, 40, size=(25, 10)) / 4.0
+    a = oracle.topk(logits, 3)
+    for mode in (True, False):
+        b = oracle.topk(logits, 3, np.full(10, 2.5), mode)
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-15)
+
+
+def test_dominant_bias_forces_selection_and_modes_differ():
+    """A bias far above every logit puts its expert first in every token's
+    selection. With the bias in the weights that expert takes almost all
+    the weight; with selection-only bias its weight follows its own logit."""
+    rng = np.random.default_rng(9)
+    logits = rng.standard_normal((20, 8))
+    bias = np.zeros(8)
+    bias[5] = 100.0
+    idx_s, w_s, _ = oracle.topk(logits, 2, bias, True)
+    idx_o, w_o, _ = oracle.topk(logits, 2, bias, False)
+    assert (idx_s[:, 0] == 5).all() and (idx_o[:, 0] == 5).all()
+    np.testing.assert_array_equal(idx_s, idx_o)
+    assert (w_s[:, 1] < 1e-40).all()          # exp(-~100) relative to the first
+    for t in range(20):
+        np.testing.assert_allclose(w_o[t], _softmax(logits[t][idx_o[t]]), rtol=0, atol=1e-15)
+    assert np.abs(w_o[:, 0] - w_s[:, 0]).max() > 0.1

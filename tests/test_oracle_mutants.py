@@ -28,10 +28,19 @@ MUTANTS = [
      "return (a->e > b->e) ? -1 : (a->e < b->e);"),
     ("ascending instead of descending", "if (a->v > b->v) return -1;",
      "if (a->v > b->v) return 1;"),
-    ("softmax numerator not shifted", "w[(size_t)t * k + j] = exp(s[j].v - lmax) / z;",
-     "w[(size_t)t * k + j] = exp(s[j].v) / z;"),
-    ("softmax over one fewer logit", "for (int j = 0; j < k; ++j) z += exp(s[j].v - lmax);",
-     "for (int j = 0; j + 1 < k; ++j) z += exp(s[j].v - lmax);"),
+    ("softmax numerator not shifted", "w[(size_t)t * k + j] = exp(u[j] - umax) / z;",
+     "w[(size_t)t * k + j] = exp(u[j]) / z;"),
+    ("softmax over one fewer logit", "for (int j = 0; j < k; ++j) z += exp(u[j] - umax);",
+     "for (int j = 0; j + 1 < k; ++j) z += exp(u[j] - umax);"),
+    ("routing bias ignored in the selection",
+     "s[e].v = logits[(size_t)t * E + e] + (bias ? bias[e] : 0.0);",
+     "s[e].v = logits[(size_t)t * E + e];"),
+    ("selection-only bias also in the weights",
+     "u[j] = (bias && !bias_in_weights) ? logits[(size_t)t * E + s[j].e] : s[j].v;",
+     "u[j] = s[j].v;"),
+    ("sketch weights without the bias",
+     "u[j] = (bias && !bias_in_weights) ? logits[(size_t)t * E + s[j].e] : s[j].v;",
+     "u[j] = bias ? logits[(size_t)t * E + s[j].e] : s[j].v;"),
     ("shared expert weighted by the first gate weight",
      "      y[r] += o[r];\n      if (slot_out) slot_out[(size_t)(k + i) * d + r] = o[r];",
      "      y[r] += w_t[0] * o[r];\n      if (slot_out) slot_out[(size_t)(k + i) * d + r] = o[r];"),
@@ -56,6 +65,11 @@ ALL_PINS = [
     pins.test_topk_matches_torch_topk_without_ties,
     pins.test_duplicated_router_rows_tie_to_lower_index,
     pins.test_softmax_is_full_softmax_renormalised_over_selection,
+    lambda: pins.test_biased_topk_brute_force(True),
+    lambda: pins.test_biased_topk_brute_force(False),
+    pins.test_zero_bias_equals_unbiased_routing,
+    pins.test_constant_bias_changes_nothing,
+    pins.test_dominant_bias_forces_selection_and_modes_differ,
     pins.test_expert_ffn_closed_form,
     lambda: pins.test_expert_ffn_matches_torch_swiglu(W_F32),
     lambda: pins.test_expert_ffn_matches_torch_swiglu(W_BF16),
