@@ -123,6 +123,22 @@ moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const fl
                      int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* Gate GEMV and top-k with a per-expert routing bias ("Deep Dive into
+ * Mixture of Experts", §5, DeepSeek-style routing sketch: a bias, adjusted
+ * for load balance, is added to the gate's scores before the top-k).
+ *   bias     [E] fp32 device (4-byte aligned), or NULL for no bias (then the
+ *            call is moe_route).
+ *   bias_in_weights  1: topk_w is the softmax of the k kept biased scores,
+ *            as the sketch writes it; 0: the bias only selects, and topk_w is
+ *            the softmax of the kept experts' unbiased logits.
+ * Selection compares fl(logit + bias[e]) (fp32 add after the compensated
+ * dot); ties, order and every other argument as moe_route. MOE_EINVAL for a
+ * bias_in_weights other than 0 or 1 or a misaligned bias.                  */
+moe_status moe_route_biased(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                            int32_t bias_in_weights, const float* x, int32_t n,
+                            int32_t* topk_idx, float* topk_w, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* Union of the selected experts and the pairs grouped by expert
  * ("Speculative Decoding for Mixture-of-Experts Models", abstract: the
  * deduplicating engine reads each selected expert once per pass).

@@ -198,7 +198,17 @@ size_t moe_workspace_bytes(const moe_layer_desc* desc, int32_t n_max) {
 moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const float* x,
                      int32_t n, int32_t* topk_idx, float* topk_w, void* workspace,
                      size_t workspace_bytes, void* stream) {
+  return moe_route_biased(desc, w_router, nullptr, 1, x, n, topk_idx, topk_w, workspace,
+                          workspace_bytes, stream);
+}
+
+moe_status moe_route_biased(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                            int32_t bias_in_weights, const float* x, int32_t n,
+                            int32_t* topk_idx, float* topk_w, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   MOE_TRY(check_desc(desc));
+  if (bias_in_weights != 0 && bias_in_weights != 1) return MOE_EINVAL;
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u) != 0) return MOE_EINVAL;
   MOE_TRY(check_n(desc, n));
   if (!w_router || !x || !topk_idx || !topk_w) return MOE_EINVAL;
   if (!aligned16(w_router) || !aligned16(x)) return MOE_EINVAL;
@@ -207,8 +217,9 @@ moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const fl
   MOE_TRY(device_info(&di));
   WsLayout L = ws_layout(desc, n);
   float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.logits);
-  cudaError_t e = moe::launch_route(desc->d, desc->n_experts, desc->top_k, n, x, w_router, logits,
-                                    topk_idx, topk_w, static_cast<cudaStream_t>(stream));
+  cudaError_t e = moe::launch_route(desc->d, desc->n_experts, desc->top_k, n, x, w_router, bias,
+                                    bias_in_weights, logits, topk_idx, topk_w,
+                                    static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route launch");
 }
 

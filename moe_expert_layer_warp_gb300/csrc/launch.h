@@ -28,9 +28,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Routing: gate GEMV with compensated fp32 dots (writes logits[n][E] into
-// scratch), then warp-per-token top-k + softmax over the k kept logits.
+// scratch), then warp-per-token top-k + softmax over the k kept scores;
+// bias (nullable) [E] is added to the logits for the selection, and to the
+// softmax's inputs too when bias_in_weights.
 cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
-                         float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t stream);
+                         const float* bias, int bias_in_weights, float* logits, int32_t* topk_idx,
+                         float* topk_w, cudaStream_t stream);
 
 // Union of selected experts, pairs grouped by (expert, token), byte counts.
 cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,

@@ -109,12 +109,17 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 
 // ------------------------------------------------------------------ top-k --
 // One warp per token. Expert e lives in lane e%32, register e/32. k rounds of
-// warp argmax; the larger logit wins, equal logits go to the lower index.
+// warp argmax; the larger score wins, equal scores go to the lower index.
+// The score is the logit, or fl(logit + bias[e]) with a routing bias
+// ("Deep Dive into Mixture of Experts", §5, DeepSeek-style routing sketch);
+// the softmax then runs over the kept biased scores (bias_in_weights) or the
+// kept experts' unbiased logits.
 constexpr int kTopkWarps = 8;
 constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
 
 __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_kernel(int E, int k, int n, const float* __restrict__ logits,
+                const float* __restrict__ bias, int bias_in_weights,
                 int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   pdl_wait();
   pdl_trigger();
@@ -127,7 +132,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   for (int r = 0; r < kPerLane; ++r) {
     const int e = lane + 32 * r;
     if (e < E) {
-      v[r] = logits[(size_t)t * E + e];
+      v[r] = bias ? __fadd_rn(logits[(size_t)t * E + e], bias[e]) : logits[(size_t)t * E + e];
     } else {
       v[r] = -INFINITY;
       taken |= 1u << r;
@@ -163,6 +168,13 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
       my_v = bv;
       my_e = be;
     }
+  }
+  if (bias && !bias_in_weights) {
+    // selection only: the softmax runs over the kept experts' own logits
+    my_v = (lane < k) ? logits[(size_t)t * E + my_e] : -INFINITY;
+    v0 = my_v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, o));
   }
   const float ej = (lane < k) ? expf(my_v - v0) : 0.f;
   const float z = warp_sum(ej);
@@ -300,14 +312,15 @@ cudaError_t launch_diag_wait(unsigned long long limit_ns, unsigned int* err, cud
 }
 
 cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float* w_router,
-                         float* logits, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
+                         const float* bias, int bias_in_weights, float* logits, int32_t* topk_idx,
+                         float* topk_w, cudaStream_t stream) {
   dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
   cudaError_t e = launch_pdl(gate_logits_kernel, g1, dim3(kGateWarps * 32), 0, stream, d, E, n, x,
                              w_router, logits);
   if (e != cudaSuccess) return e;
   dim3 g2((n + kTopkWarps - 1) / kTopkWarps);
   return launch_pdl(topk_kernel, g2, dim3(kTopkWarps * 32), 0, stream, E, k, n,
-                    static_cast<const float*>(logits), topk_idx, topk_w);
+                    static_cast<const float*>(logits), bias, bias_in_weights, topk_idx, topk_w);
 }
 
 cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,

@@ -21,7 +21,11 @@ DEDUP = "dedup"
 
 
 class PassRunner:
-    def __init__(self, weights: LayerWeights, n_max: int):
+    def __init__(self, weights: LayerWeights, n_max: int, bias: torch.Tensor = None,
+                 bias_in_weights: bool = True):
+        """bias: optional per-expert routing bias [E] fp32 on the layer's
+        device (DeepSeek-style routing); bias_in_weights: whether the kept
+        experts' softmax includes it (see moe_route_biased)."""
         sh = weights.shape
         self.shape = sh
         self.weights = weights
@@ -64,6 +68,14 @@ class PassRunner:
         self._tw = V(self.topk_w.data_ptr())
         self._yslot = V(self.y_slot.data_ptr())
         self._y = V(self.y.data_ptr())
+        self.bias = None
+        if bias is not None:
+            if (bias.dtype != torch.float32 or bias.numel() != E or bias.device != dev or
+                    not bias.is_contiguous()):
+                raise ValueError("bias must be a contiguous float32 [%d] tensor on %s" % (E, dev))
+            self.bias = bias
+        self._bias = V(bias.data_ptr()) if bias is not None else None
+        self._bias_w = 1 if bias_in_weights else 0
 
     def _x(self, x: torch.Tensor) -> ctypes.c_void_p:
         n = x.shape[0]
@@ -77,9 +89,15 @@ class PassRunner:
     # -- single steps ---------------------------------------------------------
     def route(self, x: torch.Tensor, stream=None, _xp=None):
         xp = _xp or self._x(x)
-        api._check(self._lib.moe_route(self._desc, self._router, xp, x.shape[0], self._idx,
-                                       self._tw, self._ws, self._ws_bytes, api._stream(stream)),
-                   "moe_route")
+        if self._bias is None:
+            api._check(self._lib.moe_route(self._desc, self._router, xp, x.shape[0], self._idx,
+                                           self._tw, self._ws, self._ws_bytes,
+                                           api._stream(stream)), "moe_route")
+        else:
+            api._check(self._lib.moe_route_biased(self._desc, self._router, self._bias,
+                                                  self._bias_w, xp, x.shape[0], self._idx,
+                                                  self._tw, self._ws, self._ws_bytes,
+                                                  api._stream(stream)), "moe_route_biased")
 
     def build_union(self, n: int, stream=None):
         api._check(self._lib.moe_build_union(self._desc, self._idx, n, self._uref,

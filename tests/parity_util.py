@@ -21,31 +21,36 @@ def y_tol(shape) -> float:
     return 1e-5 if shape.wdtype == W_F32 else 2e-2
 
 
-def logit_error_bound(orc_route: dict, d: int) -> np.ndarray:
+def logit_error_bound(orc_route: dict, d: int, bias=None) -> np.ndarray:
     """Upper bound on |fp32 compensated-dot logit − exact logit| per (t, e):
     rounding of the result (u·|l|) plus the compensated-dot remainder
     γ_d²·Σ|x_i·w_i| (Ogita, Rump and Oishi 2005, accurate dot product), with
-    a factor 2 of slack for the lane-then-tree order of the partial sums."""
+    a factor 2 of slack for the lane-then-tree order of the partial sums.
+    With a routing bias the score is fl(logit + bias): its rounding,
+    u·(|l| + |b|), is added (again with a factor 2)."""
     gamma = d * U32 / (1.0 - d * U32)
-    return 2.0 * (U32 * np.abs(orc_route["logits"]) + gamma * gamma * orc_route["absdot"])
+    b = 2.0 * (U32 * np.abs(orc_route["logits"]) + gamma * gamma * orc_route["absdot"])
+    if bias is not None:
+        b = b + 2.0 * U32 * (np.abs(orc_route["logits"]) + np.abs(bias)[None, :])
+    return b
 
 
-def certified_tokens(orc_route: dict, d: int) -> np.ndarray:
-    """Tokens whose sorted logits at positions 0..k are separated by more than
+def certified_tokens(orc_route: dict, d: int, bias=None) -> np.ndarray:
+    """Tokens whose sorted scores at positions 0..k are separated by more than
     twice the GPU's error bound: for these the GPU's selection and order must
     equal the oracle's exactly."""
-    b = logit_error_bound(orc_route, d).max(axis=1)
+    b = logit_error_bound(orc_route, d, bias).max(axis=1)
     return orc_route["gap"] > 2.0 * b
 
 
-def check_routing(gpu_idx: np.ndarray, gpu_w: np.ndarray, orc_route: dict, d: int):
+def check_routing(gpu_idx: np.ndarray, gpu_w: np.ndarray, orc_route: dict, d: int, bias=None):
     """Bit-exact indices on certified tokens; on the others (near-ties within
     the error bound) the GPU's choice must be one an exact computation could
     make within that bound. Weights within 1e-5 absolute where indices agree.
     Returns the number of tie-ambiguous tokens."""
-    cert = certified_tokens(orc_route, d)
-    bound = logit_error_bound(orc_route, d)
-    lg = orc_route["logits"]
+    cert = certified_tokens(orc_route, d, bias)
+    bound = logit_error_bound(orc_route, d, bias)
+    lg = orc_route["logits"] + (0.0 if bias is None else np.asarray(bias, np.float64)[None, :])
     amb = 0
     for t in range(gpu_idx.shape[0]):
         if cert[t]:

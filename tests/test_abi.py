@@ -100,3 +100,14 @@ def test_null_and_misaligned_pointers_return_einval(lib):
 def test_status_strings(lib):
     for s in range(6):
         assert api.status_str(s).startswith("MOE_")
+
+
+def test_biased_route_rejects_bad_mode_and_misaligned_bias(lib):
+    desc = api.make_desc(LayerShape(256, 8, 2, 512, 0, W_BF16))
+    one = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    big = 1 << 30
+    f = lib.moe_route_biased
+    assert f(ctypes.byref(desc), one, one, 2, one, 4, one, one, ws, big, None) == api.MOE_EINVAL
+    assert f(ctypes.byref(desc), one, ctypes.c_void_p(4098), 1, one, 4, one, one, ws, big,
+             None) == api.MOE_EINVAL

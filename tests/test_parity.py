@@ -109,6 +109,34 @@ def test_tiny_workload_every_element():
     check_pass(L, x)
 
 
+@pytest.mark.parametrize("bias_in_weights", [True, False], ids=["bias-in-weights", "selection-only"])
+def test_biased_routing_and_layer(bias_in_weights):
+    """moe_route_biased (DeepSeek-style routing bias) against the oracle:
+    certified tokens bit-exact, weights to 1e-5, and the layer output of both
+    engines with that routing within the bf16 tolerance."""
+    shape = LayerShape(512, 32, 4, 256, 1, W_BF16)
+    L = synth.make_layer(shape, 41, "cuda")
+    n = 17
+    x = synth.make_pass(shape.d, n, 0.5, [91])
+    wr = L.w_router.cpu().numpy()
+    spread = float(np.std(oracle.gate_logits(x, wr)[0]))
+    bias = (np.random.default_rng(7).standard_normal(shape.n_experts) * spread).astype(np.float32)
+    R = PassRunner(L, n, bias=torch.from_numpy(bias).cuda(), bias_in_weights=bias_in_weights)
+    xt = torch.from_numpy(x).cuda()
+    y_ps = R.forward(xt, PERSLOT).cpu().numpy()
+    idx, w = (t.cpu().numpy() for t in R.routing(n))
+    y_dd = R.forward(xt, DEDUP).cpu().numpy()
+    from moe_expert_layer_warp_gb300 import api
+    assert api.moe_last_device_error() == api.MOE_OK
+    orc = oracle.route(x, wr, shape.top_k, bias.astype(np.float64), bias_in_weights)
+    amb = pu.check_routing(idx, w, orc, shape.d, bias.astype(np.float64))
+    assert amb <= 1
+    toks = [t for t in range(n) if np.array_equal(idx[t], orc["idx"][t])]
+    y_o, _ = pu.oracle_outputs(L, x, orc, toks)
+    pu.assert_close_rms(y_ps[toks], y_o, pu.y_tol(shape), "biased per-slot y")
+    pu.assert_close_rms(y_dd[toks], y_o, pu.y_tol(shape), "biased dedup y")
+
+
 def test_identical_tokens_select_k_experts():
     shape = LayerShape(512, 32, 4, 256, 1, W_BF16)
     L = synth.make_layer(shape, 5, "cuda")
