@@ -598,6 +598,8 @@ def run_reference(args):
 
 STACK_DRAFT_COST_RATIO = 0.1601   # draft/verify cost ratio c the pages derive from FLOPs
 STACK_FIT_PASSES = 4   # held-out passes (own seeds) per (rho, n) for the bandwidth fit
+STACK_DEPTHS = (1, 4, 13, 26)     # partial stacks whose crossover is predicted and measured
+STACK_AUTOCORR = 0.155   # within-stream acceptance autocorrelation p11 - p10 (pooled, overdisp)
 STACK_REPS = 3
 
 
@@ -682,28 +684,32 @@ def run_stack(args):
             "eps_perslot": [round(eps["perslot"][n], 4) for n in w.pass_sizes],
             "eps_dedup": [round(eps["dedup"][n], 4) for n in w.pass_sizes],
             "t_fix_us": [round(t_fix[n] * 1e6, 2) for n in w.pass_sizes]})
-        # the stack: measured passes and their per-layer requested bytes
-        meas = {e: {} for e in engines}
-        pred = {e: {} for e in engines}
+        # the stack (and its first-L-layer partial stacks): measured passes
+        # and their per-layer requested bytes
+        meas_d = {L: {e: {} for e in engines} for L in STACK_DEPTHS}
+        pred_d = {L: {e: {} for e in engines} for L in STACK_DEPTHS}
         bound = {}
         for n in w.pass_sizes:
             x = xs[(ri, n)]
             lb = {}
             for eng in engines:
-                ts = []
-                for rep in range(STACK_REPS):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    torch.cuda._sleep(8 * SPIN_CYCLES)   # host queues the whole stack meanwhile
-                    e0.record(stream)
-                    for R in runners:
-                        R.forward(x, eng, stream)
-                    e1.record(stream)
-                    torch.cuda.synchronize()
-                    ts.append(e0.elapsed_time(e1) * 1e-3)
-                meas[eng][n] = statistics.median(ts)
+                for L in STACK_DEPTHS:
+                    ts = []
+                    for rep in range(STACK_REPS):
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        torch.cuda._sleep(8 * SPIN_CYCLES)   # host queues the stack meanwhile
+                        e0.record(stream)
+                        for R in runners[:L]:
+                            R.forward(x, eng, stream)
+                        e1.record(stream)
+                        torch.cuda.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1e-3)
+                    meas_d[L][eng][n] = statistics.median(ts)
                 lb[eng] = [req_bytes(R, eng) for R in runners]
-                pred[eng][n] = stepmodel.step_time(fits[eng], n, lb[eng])
+                for L in STACK_DEPTHS:
+                    pred_d[L][eng][n] = stepmodel.step_time(fits[eng], n, lb[eng][:L])
+            meas, pred = meas_d[w.layers], pred_d[w.layers]
             bound[n] = stepmodel.saving_bound(sum(lb["perslot"]), fits["perslot"].bw[n],
                                               eps["perslot"][n], sum(lb["dedup"]),
                                               fits["dedup"].bw[n], eps["dedup"][n])
@@ -711,6 +717,31 @@ def run_stack(args):
                                    stepmodel.acceptance_grid(), STACK_DRAFT_COST_RATIO)
         d = chk.as_dict()
         d["rho"] = rho
+        ns = list(w.pass_sizes)
+        d["crossover_by_depth"] = [
+            {"layers": L,
+             "measured": stepmodel.crossover_from_times(ns, meas_d[L]["perslot"], meas_d[L]["dedup"]),
+             "predicted": stepmodel.crossover_from_times(ns, pred_d[L]["perslot"],
+                                                         pred_d[L]["dedup"])}
+            for L in STACK_DEPTHS]
+        # best draft length under i.i.d. and over-dispersed (two-state Markov)
+        # acceptance, on the measured stack's best-engine pass times
+        best = {n: min(meas["perslot"][n], meas["dedup"][n]) for n in ns}
+        T = stepmodel.interpolated(best)
+        td = STACK_DRAFT_COST_RATIO * best[1]
+        alphas = stepmodel.acceptance_grid()
+        g_iid = [stepmodel.best_draft_length_yield(
+            lambda g, a=a: stepmodel.expected_tokens(a, g), T, td, max(ns) - 1) for a in alphas]
+        g_mk = [stepmodel.best_draft_length_yield(
+            lambda g, a=a: stepmodel.markov_yield(a, STACK_AUTOCORR, g), T, td, max(ns) - 1)
+            for a in alphas]
+        d["non_geometric"] = {
+            "autocorr_p11_minus_p10": STACK_AUTOCORR,
+            "gamma_star_iid": g_iid, "gamma_star_markov": g_mk,
+            "shift": [b - a for a, b in zip(g_iid, g_mk)],
+            "yield_ratio_markov_over_iid_at_0.90": [
+                round(stepmodel.markov_yield(0.9, STACK_AUTOCORR, g) /
+                      stepmodel.expected_tokens(0.9, g), 4) for g in range(1, max(ns))]}
         per_rho.append(d)
     if api.moe_last_device_error() != api.MOE_OK:
         raise RuntimeError("device error in the stack passes")

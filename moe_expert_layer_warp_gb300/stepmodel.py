@@ -17,6 +17,13 @@ Sources:
   [L] "Is Speculative Decoding's Speedup a Hardware Problem or a Model
       Problem?", Hypothesis 1: Leviathan et al.'s expected speedup
       (1 − α^(γ+1)) / ((1 − α)(γ·c + 1)) for a draft/verify cost ratio c.
+  [W] overdisp README, method and results: a_t ∈ {0,1} says whether the
+      draft's token at position t is accepted; a block walk over that stream
+      gives, for a draft length g, the tokens each block advances (the
+      accepted run, capped at g, plus the verifier's token) and the blocks;
+      autocorrelation is p11 − p10 (accept after accept minus accept after
+      reject); over-dispersed streams yield fewer tokens per block than the
+      i.i.d. formula at the same α, and the best draft length moves down.
   [F] "Building a Terminal Based LLM Inference Internals Explorer - Part 3:
       Speculative Decoding", section "The Flow": one verification pass scores
       the γ drafts and the bonus position, n = γ + 1 tokens.
@@ -310,3 +317,78 @@ class StackCheck:
             "gamma_star_measured": gm, "gamma_star_predicted": gp,
             "gamma_star_within_one": sum(abs(a - b) <= 1 for a, b in zip(gm, gp)),
         }
+
+
+# ------------------------------------------------ non-geometric acceptance --
+def block_walk(a: Sequence[int], g: int):
+    """[W] Walks an accept stream with draft length g: a block starting at
+    position t advances r + 1 positions, r = the run of accepted drafts from
+    t capped at g (the verifier supplies the token at t + r); the next block
+    starts at t + r + 1. Returns (tokens, blocks, drafted) over the whole
+    blocks that fit in the stream."""
+    if g < 0:
+        raise ValueError("draft length must be >= 0")
+    n = len(a)
+    t = tokens = blocks = 0
+    while t + g < n:           # the block's drafts and the verifier's position fit
+        r = 0
+        while r < g and a[t + r]:
+            r += 1
+        tokens += r + 1
+        blocks += 1
+        t += r + 1
+    return tokens, blocks, blocks * g
+
+
+def markov_rates(alpha: float, autocorr: float):
+    """(p11, p10) of a two-state accept chain with stationary acceptance α
+    and autocorrelation p11 − p10 = autocorr: α = p10 / (1 − p11 + p10)."""
+    p10 = alpha * (1.0 - autocorr)
+    p11 = p10 + autocorr
+    if not (0.0 <= p10 <= 1.0 and 0.0 <= p11 <= 1.0):
+        raise ValueError("no chain with alpha=%g, autocorr=%g" % (alpha, autocorr))
+    return p11, p10
+
+
+def markov_stream(n: int, alpha: float, autocorr: float, rng) -> "np.ndarray":
+    """A seeded accept stream of length n from the two-state chain, started
+    in its stationary distribution."""
+    import numpy as np
+    p11, p10 = markov_rates(alpha, autocorr)
+    u = rng.random(n)
+    a = np.empty(n, np.int8)
+    prev = u[0] < alpha
+    a[0] = prev
+    for t in range(1, n):
+        prev = u[t] < (p11 if prev else p10)
+        a[t] = prev
+    return a
+
+
+def markov_yield(alpha: float, autocorr: float, g: int) -> float:
+    """Closed-form tokens per block of the block walk over the two-state
+    chain (renewal-reward over the block's start state s = the acceptance of
+    the position before it). From s the first draft is accepted with
+    r_s = p11 or p10 and each next one with p11, so E[k|s] = 1 + r_s·(1 −
+    p11^g)/(1 − p11); the next block starts in state 1 only when all g drafts
+    were accepted and the verifier's position was accepted too, P = r_s·p11^g.
+    With p11 = p10 = α this is (1 − α^(g+1))/(1 − α)."""
+    p, q = markov_rates(alpha, autocorr)
+    if g == 0:
+        return 1.0
+    run = g if p == 1.0 else (1.0 - p ** g) / (1.0 - p)
+    e1, e0 = 1.0 + p * run, 1.0 + q * run
+    pi1 = q * p ** g / (1.0 - p ** (g + 1) + q * p ** g)
+    return pi1 * e1 + (1.0 - pi1) * e0
+
+
+def best_draft_length_yield(yield_fn: Callable[[int], float], verify_time: Callable[[int], float],
+                            t_draft: float, gamma_max: int) -> int:
+    """γ* = argmax over γ ∈ {0..gamma_max} of yield(γ) / (γ·t_draft + T(γ+1)),
+    ties to the smaller γ, for any tokens-per-block function."""
+    best_g, best_v = 0, yield_fn(0) / verify_time(1)
+    for g in range(1, gamma_max + 1):
+        v = yield_fn(g) / (g * t_draft + verify_time(g + 1))
+        if v > best_v:
+            best_g, best_v = g, v
+    return best_g

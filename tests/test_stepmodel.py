@@ -177,3 +177,63 @@ def test_stack_check_agrees_with_itself_and_counts_misses():
     pred["dedup"][4] += 5e-6
     chk = sm.StackCheck(ns, meas, pred, bound, sm.acceptance_grid(), 0.1601)
     assert chk.as_dict()["saving_inside_bound"] == 8
+
+
+# -- non-geometric acceptance (overdisp README: block walk, p11 - p10) -------
+def test_block_walk_hand_cases():
+    a = [1, 1, 0, 1, 1, 1, 1, 0, 1]
+    # g = 2: t=0 run 2 -> 3 tokens (t=3); t=3 run 2 -> 3 (t=6); t=6 run 1 -> 2 (t=8); t=8: 8+2 > 8
+    assert sm.block_walk(a, 2) == (8, 3, 6)
+    # g = 0: every position is a block of one verifier token
+    assert sm.block_walk(a, 0) == (9, 9, 0)
+    # g = 4: t=0 run 2 -> 3 (t=3); t=3 run 4 -> 5 (t=8); t=8: 8+4 > 8
+    assert sm.block_walk(a, 4) == (8, 2, 8)
+    assert sm.block_walk([0, 0, 0], 1) == (2, 2, 2)
+
+
+def test_markov_yield_reduces_to_geometric_without_autocorrelation():
+    for alpha in (0.1, 0.5, 0.77, 0.95):
+        for g in range(0, 12):
+            assert sm.markov_yield(alpha, 0.0, g) == pytest.approx(sm.expected_tokens(alpha, g),
+                                                                   rel=1e-13)
+
+
+def test_markov_rates_define_the_chain():
+    p11, p10 = sm.markov_rates(0.9, 0.155)
+    assert p11 - p10 == pytest.approx(0.155)
+    assert p10 / (1 - p11 + p10) == pytest.approx(0.9)
+    with pytest.raises(ValueError):
+        sm.markov_rates(0.5, -1.5)           # p10 would exceed 1
+
+
+@pytest.mark.parametrize("alpha,autocorr", [(0.6, 0.2), (0.9, 0.155), (0.94, 0.233), (0.8, -0.1)])
+def test_block_walk_of_simulated_streams_matches_closed_form(alpha, autocorr):
+    rng = np.random.default_rng(123)
+    a = sm.markov_stream(300_000, alpha, autocorr, rng)
+    assert a.mean() == pytest.approx(alpha, abs=0.01)
+    prev = a[:-1].astype(bool)
+    p11 = a[1:][prev].mean()
+    p10 = a[1:][~prev].mean()
+    assert p11 - p10 == pytest.approx(autocorr, abs=0.01)
+    for g in (1, 3, 8):
+        tok, blocks, drafted = sm.block_walk(a, g)
+        assert drafted == g * blocks
+        assert tok / blocks == pytest.approx(sm.markov_yield(alpha, autocorr, g), rel=0.01)
+
+
+def test_positive_autocorrelation_lowers_the_yield_and_the_best_draft_length():
+    """Over-dispersed acceptance yields fewer tokens per block than the i.i.d.
+    formula at the same alpha (more so at longer drafts), and with a verify
+    time that grows with the pass the best draft length does not move up."""
+    for g in (2, 8, 16):
+        assert sm.markov_yield(0.9, 0.2, g) < sm.expected_tokens(0.9, g)
+    assert (sm.markov_yield(0.9, 0.2, 16) / sm.expected_tokens(0.9, 16) <
+            sm.markov_yield(0.9, 0.2, 2) / sm.expected_tokens(0.9, 2))
+    T = {n: 1.0 + 0.12 * (n - 1) for n in range(1, 17)}
+    for alpha in (0.6, 0.75, 0.9, 0.95):
+        g_iid = sm.best_draft_length_yield(lambda g: sm.expected_tokens(alpha, g),
+                                           sm.interpolated(T), 0.05, 15)
+        g_mk = sm.best_draft_length_yield(lambda g: sm.markov_yield(alpha, 0.2, g),
+                                          sm.interpolated(T), 0.05, 15)
+        assert g_mk <= g_iid
+        assert g_iid == sm.best_draft_length(alpha, sm.interpolated(T), 0.05, 15)
