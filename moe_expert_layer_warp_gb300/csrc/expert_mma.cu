@@ -26,15 +26,15 @@
 // stage) writes the weighted slot outputs.
 //
 // Jobs. A job is (entry, 128-row tile, piece of K). When a phase has fewer
-// tiles than a few per CTA, each tile is cut into S ≤ 8 pieces along K so
-// that every SM streams. Every piece stores its fp32 partial sums and counts
+// tiles than CTAs, each tile is cut into S ≤ 8 pieces along K so that every
+// SM streams. Every piece stores its fp32 partial sums and counts
 // itself per 32-row quarter with a release reduction (nothing waits for
 // it); the CTA that runs a tile's last piece hands each quarter to one of its
 // four finisher warps, which waits (bounded) until all pieces of the quarter
 // are counted, adds them in piece order — a fixed order, so results are
-// reproducible — and finishes the quarter off the tensor pipeline's path. A phase-1 job loads its group's h only after every
-// phase-0 tile of the group is stored (a count in scratch, bounded acquire
-// wait).
+// reproducible — and finishes the quarter off the tensor pipeline's path.
+// A phase-1 job loads its group's h only after every phase-0 tile of the
+// group is stored (a count in scratch, bounded acquire wait).
 //
 // Warp roles (one CTA per SM, persistent, jobs from a global counter):
 //   warp 0    TMA producer (one thread),

@@ -10,24 +10,28 @@
 // selected experts) and §5 (shared experts, unweighted). Each expert is
 // W_down(silu(W_gate x) ⊙ W_up x).
 //
-// Work decomposition. A "group" is one expert applied to a set of ≤ kMaxM
-// tokens; its activation rows live in h (one fp32 row of I per token):
+// Work decomposition. A "group" is one expert applied to a set of tokens
+// whose activation rows are consecutive rows of h (one fp32 row of I per
+// token), split into sub-groups of at most kMaxM = 4 tokens:
 //   per-slot: one group per (token, slot) pair, rows in pair order t·k + j;
-//   dedup:    one group per union expert (split into groups of ≤ kMaxM
-//             tokens), rows in the union's (expert, token) order;
+//   dedup:    one group per union expert, rows in the union's (expert, token)
+//             order;
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
 // Phase 0 computes h = silu(W_gate x) ⊙ (W_up x) in tiles of 16 rows of I;
 // phase 1 computes y_slot = w · (W_down h) in tiles of 32 rows of d. A job is
-// (group, tile); CTA b takes jobs b, b+G, b+2G, …
+// (sub-group, tile); the producer thread of each CTA takes the next job from
+// a global counter, and the sub-groups of one group take consecutive jobs
+// tile by tile, so that L2 serves their repeated weight tiles.
 //
 // Per stage the producer thread issues one TMA box per weight matrix (16 rows
 // of W_gate and 16 of W_up, or 32 rows of W_down, × K_s = 256 bf16 / 128 fp32
-// columns: 16 KB) and one box of the group's input rows (1 or 8 rows × K_s
-// fp32 columns of x, of x gathered per union expert, or of h). Each of the 8
-// consumer warps owns 4 weight rows: lane l holds 16 bytes of each and the
+// columns: 16 KB) and one box of the sub-group's input rows (1 or 4 rows × K_s
+// fp32 columns of x, of x gathered per union expert, or of h). Each of the 16
+// consumer warps owns 2 weight rows: lane l holds 16 bytes of each and the
 // same columns of every token, so every weight byte is read from shared
-// memory once and used for all tokens of the group. Columns beyond K arrive
-// zero-filled from the TMA and contribute nothing.
+// memory once and used for all tokens of the sub-group. Columns beyond K
+// arrive zero-filled from the TMA and contribute nothing. A publisher warp
+// makes finished phase-0 tiles visible to other CTAs' phase-1 jobs.
 #include <math.h>
 
 #include "moe_warp.h"

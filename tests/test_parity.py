@@ -3,7 +3,9 @@ the same seeded inputs.
 
 Small layers are compared on every output element; they span several row
 tiles and K stages with ragged K tails, groups split beyond 8 tokens, k = E,
-k = 1, the largest pass (n·k = 512), n = 1 and identical tokens. The five
+k = 1, the largest pass (n·k = 512), the most shared experts (4, split into
+sub-groups past 32 tokens), the most experts and largest top-k (256, 16),
+the smallest dimensions (d = I = 64), n = 1 and identical tokens. The five
 workload shapes run at full size in the launch configuration the benchmark
 times and are compared on sampled tokens (routing, union and bytes on every
 token). Both engines are checked, and against each other.
@@ -90,6 +92,9 @@ SMALL = [
     ("k-equals-E", LayerShape(128, 4, 4, 128, 0, W_BF16), [3]),
     ("top-1", LayerShape(128, 8, 1, 64, 2, W_F32), [5]),
     ("max-pairs", LayerShape(256, 32, 4, 128, 1, W_BF16), [128]),
+    ("max-shared", LayerShape(256, 16, 2, 192, 4, W_BF16), [1, 40]),
+    ("max-experts-top16", LayerShape(128, 256, 16, 64, 1, W_F32), [3, 32]),
+    ("min-dims", LayerShape(64, 8, 2, 64, 1, W_BF16), [1, 9]),
 ]
 
 
