@@ -37,7 +37,8 @@ WORKLOAD = "deepseek-v2-lite-shaped MoE layer: d=2048, 64 routed experts top-6 +
 REPLICAS = 4
 N_PASSES_PER_N = 2        # distinct hidden-state passes per n, alternated across steps
 EXPERT_BYTES = 3 * 2048 * 1408 * 2
-SPIN_CYCLES = 200_000     # ~0.1 ms of device spin before a timed pass (host queues meanwhile)
+SPIN_CYCLES = 2_000_000   # ~1 ms of device spin before a timed pass: the host queues the whole
+                          # pass meanwhile, so no launch waits on the host inside the timed span
 
 
 def parse_args():
@@ -663,7 +664,7 @@ STACK_REPS = 3
 def run_stack(args):
     """26 V2-Lite-shaped layers (~30 GB), each fed the same pass, at n = 1..9
     and rho in {0, 0.5, 0.9, 0.99}. Per rho, the bandwidths are fitted on
-    layer 0's expert call run alone (L2 flushed before each pass) over
+    layer 0's expert call run alone (L2 flushed by a 256 MB read before each pass) over
     STACK_FIT_PASSES held-out passes (own seeds) at that rho; each stack pass
     is predicted from every layer's requested bytes over those bandwidths
     plus the fixed time, and compared with the measured stack pass. Prints
@@ -679,7 +680,9 @@ def run_stack(args):
     layers = [synth.make_layer(w.shape, w.weight_seed + l, dev) for l in range(w.layers)]
     runners = [PassRunner(L, max(w.pass_sizes)) for L in layers]
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    # read (not written) to flush L2: the flush leaves clean lines behind, as
+    # the previous layer's weights do inside a stack pass
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device=dev)
     engines = ("perslot", "dedup")
 
     def make_x(ri, rho, n, f):
@@ -714,7 +717,7 @@ def run_stack(args):
             for x in fit_xs[(ri, n)]:
                 for eng in engines:
                     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-                    flush.zero_()
+                    flush.sum()
                     torch.cuda._sleep(SPIN_CYCLES)
                     ev[0].record(stream)
                     R0.route(x, stream)
@@ -807,7 +810,7 @@ def run_stack(args):
                  "the same pass), bf16 weights, %.1f GB of expert weights" % (
                      w.layers * (w.shape.n_experts + w.shape.n_shared) * EXPERT_BYTES / 1e9),
         "fit": {"layer": 0, "passes_per_point": STACK_FIT_PASSES,
-                "l2": "flushed (256 MB write) before each fitted pass", "per_rho": fits_out},
+                "l2": "flushed (256 MB read) before each fitted pass", "per_rho": fits_out},
         "per_rho": per_rho,
     }), flush=True)
 

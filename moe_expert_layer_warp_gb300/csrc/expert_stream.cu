@@ -17,21 +17,28 @@
 //   dedup:    one group per union expert, rows in the union's (expert, token)
 //             order;
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
-// Phase 0 computes h = silu(W_gate x) ⊙ (W_up x) in tiles of 16 rows of I;
-// phase 1 computes y_slot = w · (W_down h) in tiles of 32 rows of d. A job is
+// Phase 0 computes h = silu(W_gate x) ⊙ (W_up x) in tiles of 32 rows of I;
+// phase 1 computes y_slot = w · (W_down h) in tiles of 64 rows of d. A job is
 // (sub-group, tile); the producer thread of each CTA takes the next job from
 // a global counter, and the sub-groups of one group take consecutive jobs
 // tile by tile, so that L2 serves their repeated weight tiles.
 //
-// Per stage the producer thread issues one TMA box per weight matrix (16 rows
-// of W_gate and 16 of W_up, or 32 rows of W_down, × K_s = 256 bf16 / 128 fp32
-// columns: 16 KB) and one box of the sub-group's input rows (1 or 4 rows × K_s
-// fp32 columns of x, of x gathered per union expert, or of h). Each of the 16
-// consumer warps owns 2 weight rows: lane l holds 16 bytes of each and the
-// same columns of every token, so every weight byte is read from shared
-// memory once and used for all tokens of the sub-group. Columns beyond K
-// arrive zero-filled from the TMA and contribute nothing. A publisher warp
-// makes finished phase-0 tiles visible to other CTAs' phase-1 jobs.
+// A stage holds 32 KB of weights — 32 rows of W_gate and the same 32 rows of
+// W_up, or 64 rows of W_down, × K_s = 256 bf16 / 128 fp32 columns — and the
+// sub-group's input rows for those columns (1 or 4 rows of x, of x gathered
+// per union expert, or of h). The weights arrive as ONE tensor-map box where
+// possible: W_gate and W_up are read through one map whose outermost
+// dimension steps from one matrix to the other, so a phase-0 stage is a
+// single [2][32][K_s] box. An SM's TMA stream completes boxes at a roughly
+// fixed rate whatever their size, so fewer, larger boxes per stage raise
+// what one SM can pull from HBM (about 30 GB/s with two 8 KB boxes and an
+// input box per stage, about 65 GB/s with one 32 KB box and an input box;
+// the GPU-wide share of an SM is about 45 GB/s). Each of the 16 consumer
+// warps owns 4 weight rows: lane l holds 16 bytes of each and the same
+// columns of every token, so every weight byte is read from shared memory
+// once and used for all tokens of the sub-group. Columns beyond K arrive
+// zero-filled from the TMA and contribute nothing. A publisher warp makes
+// finished phase-0 tiles visible to other CTAs' phase-1 jobs.
 #include <math.h>
 
 #include "moe_warp.h"
@@ -46,23 +53,28 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + producer warp + publisher warp
 constexpr int kPubSlots = 8;                         // ring of finished phase-0 jobs
-constexpr int kRowChunks = 32;
-constexpr int kChunkBytes = 512;
+constexpr int kRowChunks = 64;                       // weight rows per stage
+constexpr int kChunkBytes = 512;                     // bytes of one weight row per stage
 constexpr int kMaxM = kCcSub;
-constexpr int kStages = 10;
+constexpr int kStages = 5;
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
 constexpr int kMaxEntries = max_entries(kMaxM);
-constexpr int kRowsPhase0 = 16;  // rows of I per phase-0 tile (gate and up)
-constexpr int kRowsPhase1 = 32;  // rows of d per phase-1 tile
+constexpr int kRowsPhase0 = 32;  // rows of I per phase-0 tile (gate and up)
+constexpr int kRowsPhase1 = 64;  // rows of d per phase-1 tile
+static_assert(2 * kRowsPhase0 == kRowChunks && kRowsPhase1 == kRowChunks, "stage rows");
+static_assert(kRowChunks == 4 * kConsumerWarps, "four weight rows per consumer warp");
 static_assert(1 + kMaxEntries == kCcSyncInts, "engine scratch size");
 
 // Tensor maps of one launch. w0/w1/w2: routed experts' W_gate, W_up, W_down
-// ([E][rows][K]); sw0/sw1/sw2: the shared experts'. a1/aM: phase-0 input rows
-// of routed groups (x, or x gathered in union order) with a box of 1 or 8
-// rows; s1/sM: phase-0 input rows of shared-expert groups (x); h1/hM: phase-1
-// input rows (h).
+// ([E][rows][K]); sw0/sw1/sw2: the shared experts'. gu/sgu: W_gate and W_up
+// as one [2][E][I][K] tensor (the outer stride is the distance between the
+// two arrays) when that distance is expressible (pair/spair); up_first when
+// W_up lies below W_gate. a1/aM: phase-0 input rows of routed groups (x, or
+// x gathered in union order) with a box of 1 or kMaxM rows; s1/sM: phase-0
+// input rows of shared-expert groups (x); h1/hM: phase-1 input rows (h).
 struct Maps {
-  CUtensorMap w0, w1, w2, sw0, sw1, sw2, a1, aM, s1, sM, h1, hM;
+  CUtensorMap w0, w1, w2, sw0, sw1, sw2, a1, aM, s1, sM, h1, hM, gu, sgu;
+  int pair, spair, up_first, sup_first;
 };
 
 struct Params {
@@ -168,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     fence_mbar_init();
   }
   if (threadIdx.x == kConsumerWarps * 32) {
-    prefetch_tmap(&prm.maps.w0);
-    prefetch_tmap(&prm.maps.w1);
+    prefetch_tmap(prm.maps.pair ? &prm.maps.gu : &prm.maps.w0);
     prefetch_tmap(&prm.maps.w2);
     prefetch_tmap(&prm.maps.a1);
   }
@@ -246,9 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
           mbar_arrive_expect_tx(&full[stage], kRowChunks * kChunkBytes + xbytes);
           const int k0 = ks * KS;
           if (ph == 0) {
-            tma_load_3d(st, m0, k0, tile * kRowsPhase0, ecoord, &full[stage], pol_w);
-            tma_load_3d(st + 16 * kChunkBytes, m1, k0, tile * kRowsPhase0, ecoord, &full[stage],
-                        pol_w);
+            if (shared_expert ? prm.maps.spair : prm.maps.pair) {
+              tma_load_4d(st, shared_expert ? &prm.maps.sgu : &prm.maps.gu, k0, tile * kRowsPhase0,
+                          ecoord, 0, &full[stage], pol_w);
+            } else {
+              tma_load_3d(st, m0, k0, tile * kRowsPhase0, ecoord, &full[stage], pol_w);
+              tma_load_3d(st + kRowsPhase0 * kChunkBytes, m1, k0, tile * kRowsPhase0, ecoord,
+                          &full[stage], pol_w);
+            }
           } else {
             tma_load_3d(st, m0, k0, tile * kRowsPhase1, ecoord, &full[stage], pol_w);
             if (ks == 0) {
@@ -314,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
 
   // --------------------------------------------------------- consumer warps --
-  // Warp w owns two weight rows of every stage: in phase 0 gate row w and up
-  // row w of the 16-row tile (so h for row w is finished inside the warp), in
-  // phase 1 rows 2w and 2w+1 of the 32-row tile.
+  // Warp w owns four weight rows of every stage: in phase 0 gate rows 2w and
+  // 2w+1 and the same up rows of the 32-row tile (so h for those rows is
+  // finished inside the warp), in phase 1 rows 4w .. 4w+3 of the 64-row tile.
   using LM = LaneMap<WB>;
   constexpr int NP = LM::NP;
   int stage = 0;
@@ -347,11 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     const Entry en = plan[g];
     const int m = en.m;
     const int nks = ph == 0 ? nks0 : nks1;
-    const int c0 = ph == 0 ? warp : 2 * warp;
-    const int c1 = ph == 0 ? 16 + warp : 2 * warp + 1;
-    float2 acc[2][kMaxM];
+    // stage rows of this warp: phase 0 gate 2w, gate 2w+1, up 2w, up 2w+1
+    // (the box holds one matrix's 32 rows, then the other's); phase 1 4w..4w+3
+    int wrow[4];
+    if (ph == 0) {
+      const int gate0 = (en.src < 0 ? prm.maps.sup_first : prm.maps.up_first) ? kRowsPhase0 : 0;
+      const int up0 = kRowsPhase0 - gate0;
+      wrow[0] = gate0 + 2 * warp;
+      wrow[1] = gate0 + 2 * warp + 1;
+      wrow[2] = up0 + 2 * warp;
+      wrow[3] = up0 + 2 * warp + 1;
+    } else {
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 4; ++q) wrow[q] = 4 * warp + q;
+    }
+    float2 acc[4][kMaxM];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t) acc[q][t] = make_float2(0.f, 0.f);
     for (int ks = 0; ks < nks; ++ks) {
@@ -361,19 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
       }
       const unsigned char* st = smem + stage * L::kStageBytes;
       const float* sx = reinterpret_cast<const float*>(st + L::kWBytes);
-      float2 w0[NP], w1[NP];
-      LM::load_w(st + c0 * kChunkBytes, lane, w0);
-      LM::load_w(st + c1 * kChunkBytes, lane, w1);
+      float2 wv[4][NP];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) LM::load_w(st + wrow[q] * kChunkBytes, lane, wv[q]);
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t) {
         if (t < m) {
           float2 xv[NP];
           LM::load_x(sx + t * KS, lane, xv);
 #pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            acc[0][t] = __ffma2_rn(w0[p], xv[p], acc[0][t]);
-            acc[1][t] = __ffma2_rn(w1[p], xv[p], acc[1][t]);
-          }
+          for (int p = 0; p < NP; ++p)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q][t] = __ffma2_rn(wv[q][p], xv[p], acc[q][t]);
         }
       }
       __syncwarp();
@@ -383,18 +410,21 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         phase ^= 1u;
       }
     }
-    float r[2][kMaxM];
+    float r[4][kMaxM];
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t)
         r[q][t] = (t < m) ? warp_sum(acc[q][t].x + acc[q][t].y) : 0.f;
     if (lane == 0) {
       if (ph == 0) {
-        const int row = tile * kRowsPhase0 + warp;
 #pragma unroll
-        for (int t = 0; t < kMaxM; ++t)
-          if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(r[0][t]) * r[1][t];
+        for (int j = 0; j < 2; ++j) {
+          const int row = tile * kRowsPhase0 + 2 * warp + j;
+#pragma unroll
+          for (int t = 0; t < kMaxM; ++t)
+            if (t < m) a.h[(size_t)(en.row0 + t) * a.I + row] = silu(r[j][t]) * r[2 + j][t];
+        }
         // hand the finished job to the publisher thread (see above)
         const int ps = pub_n % kPubSlots;
         if (!mbar_wait(&pub_empty[ps], (uint32_t)(((pub_n / kPubSlots) & 1) ^ 1), a.err, 0x250)) {
@@ -405,8 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
         }
       } else {
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int row = tile * kRowsPhase1 + 2 * warp + q;
+        for (int q = 0; q < 4; ++q) {
+          const int row = tile * kRowsPhase1 + 4 * warp + q;
 #pragma unroll
           for (int t = 0; t < kMaxM; ++t) {
             if (t < m) {
@@ -431,6 +461,29 @@ bool weight_map(CUtensorMap* m, const void* p, int WB, int n_mat, int rows, int 
                    3, dims, strides, box);
 }
 
+// W_gate and W_up of n_mat experts as one 4-D tensor [2][n_mat][rows][K]
+// whose outer stride is the byte distance between the two arrays (based at
+// the lower one: up_first when that is W_up), so that one box carries the
+// same rows of both. Needs the distance to be a multiple of 16 bytes, at
+// least the size of one array (they do not overlap) and below 2^40 (the
+// tensor map's stride limit); otherwise returns false and the kernel loads
+// the two matrices as separate boxes.
+bool pair_map(CUtensorMap* m, int* up_first, const void* gate, const void* up, int WB, int n_mat,
+              int rows, int K) {
+  const int ks = WB == 2 ? 256 : 128;
+  const uintptr_t pg = reinterpret_cast<uintptr_t>(gate), pu = reinterpret_cast<uintptr_t>(up);
+  const uint64_t delta = pu > pg ? pu - pg : pg - pu;
+  const uint64_t mat = (uint64_t)rows * K * WB;
+  if (delta % 16 != 0 || delta < mat * (uint64_t)n_mat || delta >= (1ull << 40)) return false;
+  *up_first = pu < pg ? 1 : 0;
+  const uint64_t dims[4] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n_mat, 2};
+  const uint64_t strides[3] = {(uint64_t)K * WB, mat, delta};
+  const uint32_t box[4] = {(uint32_t)ks, (uint32_t)kRowsPhase0, 1, 2};
+  return make_tmap(m, reinterpret_cast<const void*>(pu < pg ? pu : pg),
+                   WB == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                   dims, strides, box);
+}
+
 bool act_map(CUtensorMap* m, const float* p, int rows, int K, int ks, int box_rows) {
   const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
   const uint64_t strides[1] = {(uint64_t)K * 4};
@@ -449,10 +502,14 @@ bool build_maps(const ExpertArgs& a, Maps* M) {
   ok &= weight_map(&M->w0, a.w_gate, WB, a.E, a.I, a.d, kRowsPhase0);
   ok &= weight_map(&M->w1, a.w_up, WB, a.E, a.I, a.d, kRowsPhase0);
   ok &= weight_map(&M->w2, a.w_down, WB, a.E, a.d, a.I, kRowsPhase1);
+  M->pair = pair_map(&M->gu, &M->up_first, a.w_gate, a.w_up, WB, a.E, a.I, a.d) ? 1 : 0;
+  if (!M->pair) M->up_first = 0;
   if (a.s > 0) {
     ok &= weight_map(&M->sw0, a.ws_gate, WB, a.s, a.I, a.d, kRowsPhase0);
     ok &= weight_map(&M->sw1, a.ws_up, WB, a.s, a.I, a.d, kRowsPhase0);
     ok &= weight_map(&M->sw2, a.ws_down, WB, a.s, a.d, a.I, kRowsPhase1);
+    M->spair = pair_map(&M->sgu, &M->sup_first, a.ws_gate, a.ws_up, WB, a.s, a.I, a.d) ? 1 : 0;
+    if (!M->spair) M->sup_first = 0;
   }
   const float* xa = a.engine == 0 ? a.x32 : a.xg;
   const int xa_rows = a.engine == 0 ? a.n : P;

@@ -18,9 +18,9 @@ namespace moe {
 struct TmapKey {
   uint64_t ptr;
   int dtype, rank, swizzle;
-  uint64_t dims[3];
-  uint64_t strides[2];
-  uint32_t box[3];
+  uint64_t dims[5];
+  uint64_t strides[4];
+  uint32_t box[5];
   bool operator<(const TmapKey& o) const { return memcmp(this, &o, sizeof *this) < 0; }
 };
 
@@ -45,10 +45,11 @@ inline EncodeFn encode_fn() {
 
 // Encodes (or fetches from the cache) a tiled tensor map over a row-major
 // tensor (no swizzle unless asked). dims/box are innermost-first; strides (bytes) are those of
-// dims[1..rank-1]. Out-of-bounds elements of a box read as zero.
+// dims[1..rank-1]; rank ≤ 5. Out-of-bounds elements of a box read as zero.
 inline bool make_tmap(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int rank,
                       const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
                       CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
+  if (rank < 1 || rank > 5) return false;
   static std::mutex mu;
   static std::map<TmapKey, CUtensorMap> cache;
   TmapKey key;
@@ -70,8 +71,8 @@ inline bool make_tmap(CUtensorMap* out, const void* ptr, CUtensorMapDataType dty
   }
   EncodeFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t d[3], s[2];
-  cuuint32_t b[3], es[3] = {1, 1, 1};
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], es[5] = {1, 1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];

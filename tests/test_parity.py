@@ -107,6 +107,38 @@ def test_small_layers_every_element(name, shape, ns):
         check_pass(L, x, runner=R)
 
 
+def _rearranged(L, order):
+    """Layer L with its W_gate / W_up storage rearranged: "up-below-gate"
+    puts both in one buffer, W_up first (the CUDA-core kernel then reads the
+    pair through one map based at W_up); "gate-is-up" passes one array as
+    both (a distance of zero: the kernel loads the two as separate boxes)."""
+    def arrange(g, u):
+        if g is None:
+            return None, None
+        if order == "up-below-gate":
+            buf = torch.empty((2,) + tuple(g.shape), dtype=g.dtype, device=g.device)
+            buf[0].copy_(u)
+            buf[1].copy_(g)
+            return buf[1], buf[0]
+        return g, g
+    wg, wu = arrange(L.w_gate, L.w_up)
+    sg, su = arrange(L.ws_gate, L.ws_up)
+    return synth.LayerWeights(L.shape, L.w_router, wg, wu, L.w_down, sg, su, L.ws_down)
+
+
+@pytest.mark.parametrize("order", ["up-below-gate", "gate-is-up"])
+@pytest.mark.parametrize("shape", [LayerShape(192, 6, 3, 256, 1, W_F32),
+                                   LayerShape(576, 16, 4, 320, 2, W_BF16)],
+                         ids=["f32", "bf16"])
+def test_gate_up_storage(order, shape):
+    """Where W_gate and W_up lie relative to each other decides how the
+    CUDA-core kernel loads them; every arrangement gives the oracle's result."""
+    L = _rearranged(synth.make_layer(shape, 29, "cuda"), order)
+    R = PassRunner(L, 5)
+    for n in (1, 5):
+        check_pass(L, synth.make_pass(shape.d, n, 0.9, [321 + n]), runner=R)
+
+
 def test_tiny_workload_every_element():
     w = configs.TINY
     L = synth.make_layer(w.shape, w.weight_seed, "cuda")
@@ -221,6 +253,7 @@ def test_small_layers_on_each_expert_kernel(min_m):
     env = dict(os.environ, MOE_MMA_MIN_M=min_m)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         "tests/test_parity.py::test_small_layers_every_element",
+                        "tests/test_parity.py::test_gate_up_storage",
                         "tests/test_parity.py::test_identical_tokens_select_k_experts",
                         "tests/test_parity.py::test_repeated_runs_are_bitwise_identical"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
