@@ -37,6 +37,8 @@ WORKLOAD = "deepseek-v2-lite-shaped MoE layer: d=2048, 64 routed experts top-6 +
 REPLICAS = 4
 N_PASSES_PER_N = 2        # distinct hidden-state passes per n, alternated across steps
 EXPERT_BYTES = 3 * 2048 * 1408 * 2
+BREAKDOWN_PASSES = 8      # passes per (pass size, engine) in the per-call breakdown
+BREAKDOWN_ROUNDS = 5      # replays of each breakdown graph (median taken)
 SPIN_CYCLES = 2_000_000   # ~1 ms of device spin before a timed pass: the host queues the whole
                           # pass meanwhile, so no launch waits on the host inside the timed span
 
@@ -177,46 +179,93 @@ def kernels_per_pass():
     return 2 + 1 + 2 + 1
 
 
-def measure_breakdown(w, runners, xs, reps=3):
-    """Per-pass timing with CUDA events around the engine call and the whole
-    pass, on the launching stream; returns samples for the step-time model and
-    the expert-engine roofline numbers."""
+def capture_graph(fn):
+    """Captures fn(stream) into a CUDA graph on a side stream."""
+    import torch
+    cur = torch.cuda.current_stream()
+    s = torch.cuda.Stream()
+    s.wait_stream(cur)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fn(s)
+    cur.wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graphs(graphs, rounds):
+    """Replays the graphs round-robin `rounds` times on the current stream,
+    each replay between CUDA events after a device spin that covers the host's
+    launch; returns each graph's median replay time in seconds."""
     import torch
     stream = torch.cuda.current_stream()
+    evs = []
+    for _ in range(rounds):
+        for i, g in enumerate(graphs):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(SPIN_CYCLES // 4)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            evs.append((i, e0, e1))
+    torch.cuda.synchronize()
+    ts = [[] for _ in graphs]
+    for i, e0, e1 in evs:
+        ts[i].append(e0.elapsed_time(e1) * 1e-3)
+    return [statistics.median(t) for t in ts]
+
+
+def measure_breakdown(w, runners, xs):
+    """The expert call's time inside a pipelined pass, per pass size and
+    engine. Each of BREAKDOWN_PASSES passes (consecutive passes on different
+    weight replicas) is captured twice as a CUDA graph: route, union, expert
+    call, combine — and the same without the expert call. The graphs are
+    replayed round-robin between CUDA events on the stream; the expert call's
+    time is the difference of a pass's two medians, the fixed time the
+    second median. Returns samples for the step-time model and the roofline
+    numbers."""
     samples = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     tfix = {n: [] for n in w.pass_sizes}
     pass_ms = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
-    alg_bytes, eng_ms = 0.0, 0.0
-    launches = 0
-    for r in range(reps):
-        for rep, n, eng, q in step_plan(w, r):
-            R = runners[rep]
-            x = xs[n][q]
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            torch.cuda._sleep(SPIN_CYCLES)   # device busy while the host queues the pass
-            ev[0].record(stream)
-            R.route(x, stream)
-            R.build_union(n, stream)
-            ev[1].record(stream)
-            R.experts(x, eng, stream)
-            ev[2].record(stream)
-            R.combine(n, stream)
-            ev[3].record(stream)
-            torch.cuda.synchronize()
-            t_exp = ev[1].elapsed_time(ev[2]) * 1e-3
-            t_all = ev[0].elapsed_time(ev[3]) * 1e-3
-            b = [int(v) for v in R.bytes.cpu().tolist()]
-            sh = R.shape
-            req = (b[0] if eng == "perslot" else b[1]) + b[2]
-            samples[eng][n].append((req, t_exp))
-            tfix[n].append(t_all - t_exp)
-            pass_ms[eng][n].append(t_all * 1e3)
+    alg_bytes, eng_s, launches = 0.0, 0.0, 0
+    import torch
+    stream = torch.cuda.current_stream()
+    for n in w.pass_sizes:
+        for eng in ("perslot", "dedup"):
+            plan = [(i % REPLICAS, i % N_PASSES_PER_N) for i in range(BREAKDOWN_PASSES)]
+            reqs = []
+            for rep, q in plan:          # requested bytes of each pass (routing is deterministic)
+                R = runners[rep]
+                R.forward(xs[n][q], eng, stream)
+                b = [int(v) for v in R.bytes.cpu().tolist()]
+                reqs.append((b[0] if eng == "perslot" else b[1]) + b[2])
+
+            def one(s, rep, q, with_expert):
+                R, x = runners[rep], xs[n][q]
+                R.route(x, s)
+                R.build_union(n, s)
+                if with_expert:
+                    R.experts(x, eng, s)
+                R.combine(n, s)
+            ga = [capture_graph(lambda s, r=r, q=q: one(s, r, q, True)) for r, q in plan]
+            gb = [capture_graph(lambda s, r=r, q=q: one(s, r, q, False)) for r, q in plan]
+            t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
+            ta, tb = t[:len(plan)], t[len(plan):]
+            sh = runners[0].shape
             act = n * sh.d * 4 + n * (sh.top_k + sh.n_shared) * sh.d * 4
-            alg_bytes += req + act
-            eng_ms += t_exp * 1e3
-            launches += 1
+            for i in range(len(plan)):
+                t_exp = max(ta[i] - tb[i], 1e-9)
+                samples[eng][n].append((reqs[i], t_exp))
+                tfix[n].append(tb[i])
+                pass_ms[eng][n].append(ta[i] * 1e3)
+                alg_bytes += reqs[i] + act
+                eng_s += t_exp
+                launches += 1
+            del ga, gb
     t_fix = {n: statistics.median(v) for n, v in tfix.items()}
-    return samples, t_fix, pass_ms, alg_bytes / launches, eng_ms / launches
+    return samples, t_fix, pass_ms, alg_bytes / launches, eng_s * 1e3 / launches
 
 
 def e2e_measure(w, runners, xs, steps, warmup):
@@ -664,8 +713,9 @@ STACK_REPS = 3
 def run_stack(args):
     """26 V2-Lite-shaped layers (~30 GB), each fed the same pass, at n = 1..9
     and rho in {0, 0.5, 0.9, 0.99}. Per rho, the bandwidths are fitted on
-    layer 0's expert call run alone (L2 flushed by a 256 MB read before each pass) over
-    STACK_FIT_PASSES held-out passes (own seeds) at that rho; each stack pass
+    layer 0's expert call run alone over STACK_FIT_PASSES held-out passes
+    (own seeds) at that rho, each pass a CUDA graph behind an L2 flush (a
+    256 MB read) timed with and without its expert call; each stack pass
     is predicted from every layer's requested bytes over those bandwidths
     plus the fixed time, and compared with the measured stack pass. Prints
     one JSON line."""
@@ -708,29 +758,37 @@ def run_stack(args):
         raise RuntimeError("device error during warm-up")
 
     R0 = runners[0]
+    g_flush = capture_graph(lambda s: flush.sum())
     per_rho, fits_out = [], []
     for ri, rho in enumerate(w.rhos):
-        # fit on layer 0 run alone, held-out passes at this rho
+        # fit on layer 0 run alone, held-out passes at this rho: each pass as a
+        # CUDA graph behind an L2 flush (a 256 MB read), with and without the
+        # expert call; the flush's own graph is subtracted from the fixed time
         samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
         tfix = {n: [] for n in w.pass_sizes}
+        t_flush = time_graphs([g_flush], 2 * BREAKDOWN_ROUNDS)[0]
         for n in w.pass_sizes:
-            for x in fit_xs[(ri, n)]:
-                for eng in engines:
-                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for eng in engines:
+                reqs = []
+                for x in fit_xs[(ri, n)]:
+                    R0.forward(x, eng, stream)
+                    reqs.append(req_bytes(R0, eng))
+
+                def one(s, x, with_expert):
                     flush.sum()
-                    torch.cuda._sleep(SPIN_CYCLES)
-                    ev[0].record(stream)
-                    R0.route(x, stream)
-                    R0.build_union(n, stream)
-                    ev[1].record(stream)
-                    R0.experts(x, eng, stream)
-                    ev[2].record(stream)
-                    R0.combine(n, stream)
-                    ev[3].record(stream)
-                    torch.cuda.synchronize()
-                    t_exp = ev[1].elapsed_time(ev[2]) * 1e-3
-                    samples[eng][n].append((req_bytes(R0, eng), t_exp))
-                    tfix[n].append(ev[0].elapsed_time(ev[3]) * 1e-3 - t_exp)
+                    R0.route(x, s)
+                    R0.build_union(n, s)
+                    if with_expert:
+                        R0.experts(x, eng, s)
+                    R0.combine(n, s)
+                ga = [capture_graph(lambda s, x=x: one(s, x, True)) for x in fit_xs[(ri, n)]]
+                gb = [capture_graph(lambda s, x=x: one(s, x, False)) for x in fit_xs[(ri, n)]]
+                t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
+                k = len(ga)
+                for i in range(k):
+                    samples[eng][n].append((reqs[i], max(t[i] - t[k + i], 1e-9)))
+                    tfix[n].append(max(t[k + i] - t_flush, 0.0))
+                del ga, gb
         t_fix = {n: statistics.median(v) for n, v in tfix.items()}
         fits = {e: stepmodel.EngineFit({n: stepmodel.effective_bandwidth(
             [b for b, _ in samples[e][n]], [t for _, t in samples[e][n]]) for n in w.pass_sizes},
@@ -820,7 +878,8 @@ CASES = {"tiny": "TINY", "v2lite": "V2_LITE", "mixtral": "MIXTRAL", "v3": "V3"}
 
 def run_case(args):
     """A small single-layer case for profilers: one layer, a few passes, no
-    graph, no replicas. Prints the mean pass and engine time."""
+    replicas. Prints the expert call's time inside a graph-replayed pass and
+    alone between CUDA events."""
     import torch
     from __graft_entry__ import build
     build()
@@ -834,6 +893,22 @@ def run_case(args):
                                          [w.x_seed_base + s for s in range(w.streams)])).cuda()
     R = PassRunner(L, x.shape[0])
     st = torch.cuda.current_stream()
+    # the call inside a pass: a CUDA graph of flush (256 MB read), route,
+    # union, expert call and combine, against the same graph without the call
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
+    R.forward(x, eng, st)
+
+    def one(s, with_expert):
+        flush.sum()
+        R.route(x, s)
+        R.build_union(x.shape[0], s)
+        if with_expert:
+            R.experts(x, eng, s)
+        R.combine(x.shape[0], s)
+    ga = capture_graph(lambda s: one(s, True))
+    gb = capture_graph(lambda s: one(s, False))
+    ta, tb = time_graphs([ga, gb], args.passes)
+    # and alone between CUDA events (adds the events' and launch latency)
     ts = []
     for _ in range(args.passes):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -850,9 +925,12 @@ def run_case(args):
         raise RuntimeError("device error")
     b = [int(v) for v in R.bytes.cpu().tolist()]
     req = (b[0] if eng == "perslot" else b[1]) + b[2]
-    ms = statistics.median(ts)
+    ms = (ta - tb) * 1e3
+    ms_ev = statistics.median(ts)
     print(json.dumps({"case": args.case, "tokens": x.shape[0], "engine_ms": round(ms, 4),
                       "requested_bytes": req, "GBs": round(req / ms / 1e6, 1),
+                      "engine_ms_events": round(ms_ev, 4),
+                      "GBs_events": round(req / ms_ev / 1e6, 1),
                       "union": int(R.union_count.item())}))
 
 
