@@ -83,14 +83,27 @@ constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
 constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
 constexpr int kSmemBytes = kOffMisc + 128 * 4 + 1024;  // + slack to align the base to 1024
 
-// Token tensors read as B, each with boxes of 64 columns × h rows for
-// h = 8, 16, 32: routed-group inputs (x gathered in union order, or x for
-// per-slot), shared-expert inputs (x), phase-1 inputs (h), hi and lo halves.
-enum { kXA, kXALo, kXS, kXSLo, kHH, kHLo, kNumB };
+// Token tensors read as B, for h = 8, 16, 32 rows: routed-group inputs (x
+// gathered in union order, or x for per-slot), shared-expert inputs (x),
+// phase-1 inputs (h). Each is stored as its hi half then its lo half
+// ([2][rows][K] bf16), so one box [2][h][64] brings both halves of a
+// K-step — the B tile's rows [0, h) and [h, 2h) — and the h box spans
+// two K-steps ([2 K-steps][2][h][64]).
+enum { kXA, kXS, kHH, kNumB };
 
+// Weight maps (bf16, 128-byte swizzle, 128 rows × 64 columns per K-step).
+// gu/sgu: W_gate and W_up as one [2][E][rows][K] tensor (the outer stride is
+// the distance between the two arrays, pair/spair set when expressible;
+// up_first when W_up lies below W_gate), so one box carries both tiles of a
+// phase-0 stage; wg/wu/swg/swu load them separately otherwise. wd/swd:
+// W_down viewed as [K/64][E][rows][64] (a 128-byte stride between 64-column
+// K-steps), so one box carries the two K-steps of a phase-1 stage. An SM's
+// TMA stream completes boxes at a roughly fixed rate, so fewer boxes per
+// stage raise what one SM can pull from HBM.
 struct Maps {
-  CUtensorMap wg, wu, wd, swg, swu, swd;  // [E or s][rows][K] bf16, box 64 × 128 × 1
+  CUtensorMap wg, wu, wd, swg, swu, swd, gu, sgu;
   CUtensorMap b[3][kNumB];                // [h = 8, 16, 32][tensor]
+  int pair, spair, up_first, sup_first;
 };
 
 // Rows h of a group's B tile half for m tokens, and its index in Maps::b.
@@ -177,8 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   }
   if (warp == 1) umma::tmem_alloc(tmem_base, kTmemCols);
   if (threadIdx.x == 32 * 2) {
-    prefetch_tmap(&prm.maps.wg);
-    prefetch_tmap(&prm.maps.wu);
+    prefetch_tmap(prm.maps.pair ? &prm.maps.gu : &prm.maps.wg);
     prefetch_tmap(&prm.maps.wd);
     prefetch_tmap(&prm.maps.b[0][kXA]);
     prefetch_tmap(&prm.maps.b[0][kHH]);
@@ -259,31 +271,27 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           if (ks == piece * c.kc) stage_job[stage] = job;
           if (ph == 0) {
             const int k0 = ks * 64;
-            const CUtensorMap* xh = &bm[sh ? kXS : kXA];
-            const CUtensorMap* xl = &bm[sh ? kXSLo : kXALo];
             mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * bbytes);
-            tma_load_3d(st, sh ? &prm.maps.swg : &prm.maps.wg, k0, tile * kM, ec, &full[stage], pol_w);
-            tma_load_3d(st + kTileBytes, sh ? &prm.maps.swu : &prm.maps.wu, k0, tile * kM, ec,
-                        &full[stage], pol_w);
-            tma_load_2d(bt, xh, k0, en.arow, &full[stage], pol_x);
-            tma_load_2d(bt + bbytes, xl, k0, en.arow, &full[stage], pol_x);
+            if (sh ? prm.maps.spair : prm.maps.pair) {
+              tma_load_4d(st, sh ? &prm.maps.sgu : &prm.maps.gu, k0, tile * kM, ec, 0, &full[stage],
+                          pol_w);
+            } else {
+              tma_load_3d(st, sh ? &prm.maps.swg : &prm.maps.wg, k0, tile * kM, ec, &full[stage],
+                          pol_w);
+              tma_load_3d(st + kTileBytes, sh ? &prm.maps.swu : &prm.maps.wu, k0, tile * kM, ec,
+                          &full[stage], pol_w);
+            }
+            tma_load_3d(bt, &bm[sh ? kXS : kXA], k0, en.arow, 0, &full[stage], pol_x);
           } else {
-            const int k0 = ks * 128;
-            const CUtensorMap* wd = sh ? &prm.maps.swd : &prm.maps.wd;
-            const CUtensorMap* hh = &bm[kHH];
-            const CUtensorMap* hl = &bm[kHLo];
             mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 4 * bbytes);
-            tma_load_3d(st, wd, k0, tile * kM, ec, &full[stage], pol_w);
-            tma_load_3d(st + kTileBytes, wd, k0 + 64, tile * kM, ec, &full[stage], pol_w);
+            tma_load_4d(st, sh ? &prm.maps.swd : &prm.maps.wd, 0, tile * kM, ec, 2 * ks,
+                        &full[stage], pol_w);
             if (ks == piece * c.kc) {
               // the group's h rows must all be stored before they are read
               if (!wait_count(done0 + g, done_target, a.err, 0x340)) *abort_flag = 1;
               fence_proxy_async_global();
             }
-            tma_load_2d(bt, hh, k0, en.row0, &full[stage], pol_x);
-            tma_load_2d(bt + bbytes, hl, k0, en.row0, &full[stage], pol_x);
-            tma_load_2d(bt + kBStepBytes, hh, k0 + 64, en.row0, &full[stage], pol_x);
-            tma_load_2d(bt + kBStepBytes + bbytes, hl, k0 + 64, en.row0, &full[stage], pol_x);
+            tma_load_4d(bt, &bm[kHH], 0, en.row0, 0, 2 * ks, &full[stage], pol_x);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -330,8 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             break;
           }
           const uint32_t st = smem_addr(smem + stage * kStageBytes);
-          const uint64_t a0 = umma::desc_sw128(st);
-          const uint64_t a1 = umma::desc_sw128(st + kTileBytes);
+          // phase 0: a0 the gate tile, a1 the up tile (the pair box puts the
+          // lower array first); phase 1: the two K-steps of the down tile
+          const uint32_t swap = ph == 0 && (plan[g].src < 0 ? prm.maps.sup_first : prm.maps.up_first)
+                                    ? kTileBytes : 0u;
+          const uint64_t a0 = umma::desc_sw128(st + swap);
+          const uint64_t a1 = umma::desc_sw128(st + (kTileBytes - swap));
           const uint32_t bt = st + 2 * kTileBytes;
           const uint64_t b0 = umma::desc_sw128(bt);                   // K-step 0: hi | lo rows
           const bool first = ks == ks0;
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
               umma::mma_bf16(dacc + 64, a1 + 2 * j, b0 + 2 * j, idesc, acc);   // up · [x_hi | x_lo]
             }
           } else {
-            const uint64_t b1 = umma::desc_sw128(bt + kBStepBytes);        // K-step 1
+            const uint64_t b1 = umma::desc_sw128(bt + 2 * b_rows(m) * 128);  // K-step 1
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, (!first || j != 0) ? 1u : 0u);
@@ -637,11 +649,47 @@ bool w_map(CUtensorMap* m, const void* p, int n_mat, int rows, int K) {
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool b_map(CUtensorMap* m, const void* p, int rows, int K, int box_rows) {
-  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows};
-  const uint64_t strides[1] = {(uint64_t)K * 2};
-  const uint32_t box[2] = {64, (uint32_t)box_rows};
-  return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dims, strides, box,
+// W_gate and W_up as one [2][n_mat][rows][K] tensor based at the lower of the
+// two arrays; false (load them separately) unless their distance is a
+// non-zero multiple of 16 bytes below 2^40, the tensor map's stride limit.
+bool pair_map(CUtensorMap* m, int* up_first, const void* gate, const void* up, int n_mat,
+              int rows, int K) {
+  const uintptr_t pg = reinterpret_cast<uintptr_t>(gate), pu = reinterpret_cast<uintptr_t>(up);
+  const uint64_t delta = pu > pg ? pu - pg : pg - pu;
+  if (delta == 0 || delta % 16 != 0 || delta >= (1ull << 40)) return false;
+  *up_first = pu < pg ? 1 : 0;
+  const uint64_t dims[4] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n_mat, 2};
+  const uint64_t strides[3] = {(uint64_t)K * 2, (uint64_t)rows * K * 2, delta};
+  const uint32_t box[4] = {64, (uint32_t)kM, 1, 2};
+  return make_tmap(m, reinterpret_cast<const void*>(pu < pg ? pu : pg),
+                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// W_down [n_mat][rows][K] viewed as [K/64][n_mat][rows][64]: a box of two
+// 64-column K-steps lands as two consecutive 128-row tiles.
+bool down_map(CUtensorMap* m, const void* p, int n_mat, int rows, int K) {
+  const uint64_t dims[4] = {64, (uint64_t)rows, (uint64_t)n_mat, (uint64_t)(K / 64)};
+  const uint64_t strides[3] = {(uint64_t)K * 2, (uint64_t)rows * K * 2, 128};
+  const uint32_t box[4] = {64, (uint32_t)kM, 1, 2};
+  return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Token rows [2 (hi, lo)][rows][K] bf16: a box [2][box_rows][64] per K-step
+// (chunks = 1), or [chunks][2][box_rows][64] over consecutive K-steps (the
+// K-step dimension outermost, 128 bytes apart).
+bool b_map(CUtensorMap* m, const void* p, int rows, int K, int box_rows, int chunks) {
+  const uint64_t dims[4] = {64, (uint64_t)rows, 2, (uint64_t)(K / 64)};
+  const uint64_t strides[3] = {(uint64_t)K * 2, (uint64_t)rows * K * 2, 128};
+  const uint32_t box[4] = {64, (uint32_t)box_rows, 2, (uint32_t)chunks};
+  if (chunks == 1) {
+    const uint64_t d3[3] = {(uint64_t)K, (uint64_t)rows, 2};
+    const uint32_t b3[3] = {64, (uint32_t)box_rows, 2};
+    return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, d3, strides, b3,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -653,26 +701,31 @@ bool build_maps(const ExpertArgs& a, Maps* M) {
   bool ok = true;
   ok &= w_map(&M->wg, a.w_gate, a.E, a.I, a.d);
   ok &= w_map(&M->wu, a.w_up, a.E, a.I, a.d);
-  ok &= w_map(&M->wd, a.w_down, a.E, a.d, a.I);
+  ok &= down_map(&M->wd, a.w_down, a.E, a.d, a.I);
+  M->pair = pair_map(&M->gu, &M->up_first, a.w_gate, a.w_up, a.E, a.I, a.d) ? 1 : 0;
+  if (!M->pair) M->up_first = 0;
   if (a.s > 0) {
     ok &= w_map(&M->swg, a.ws_gate, a.s, a.I, a.d);
     ok &= w_map(&M->swu, a.ws_up, a.s, a.I, a.d);
-    ok &= w_map(&M->swd, a.ws_down, a.s, a.d, a.I);
+    ok &= down_map(&M->swd, a.ws_down, a.s, a.d, a.I);
+    M->spair = pair_map(&M->sgu, &M->sup_first, a.ws_gate, a.ws_up, a.s, a.I, a.d) ? 1 : 0;
+    if (!M->spair) M->sup_first = 0;
   }
   // Phase-0 token rows: x gathered in union order (dedup) or x itself
-  // (per-slot: an entry's row is its token); shared experts read x.
+  // (per-slot: an entry's row is its token); shared experts read x. The lo
+  // halves follow the hi halves: xg16lo = xg16 + P·d, x16lo = x16 + n·d,
+  // h16lo = h16 + hrows·I.
   const uint16_t* xa = a.engine == 1 ? a.xg16 : a.x16;
-  const uint16_t* xa_lo = a.engine == 1 ? a.xg16lo : a.x16lo;
   const int xa_rows = a.engine == 1 ? P : a.n;
+  if (a.xg16lo != a.xg16 + (size_t)P * a.d || a.x16lo != a.x16 + (size_t)a.n * a.d ||
+      a.h16lo != a.h16 + (size_t)hrows * a.I)
+    return false;
   for (int si = 0; si < 3; ++si) {
     const int br = 8 << si;
     CUtensorMap* B = M->b[si];
-    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br);
-    ok &= b_map(&B[kXALo], xa_lo, xa_rows, a.d, br);
-    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br);
-    ok &= b_map(&B[kXSLo], a.x16lo, a.n, a.d, br);
-    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br);
-    ok &= b_map(&B[kHLo], a.h16lo, hrows, a.I, br);
+    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br, 1);
+    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br, 1);
+    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br, 2);
   }
   return ok;
 }

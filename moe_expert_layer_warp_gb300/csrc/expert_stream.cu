@@ -464,17 +464,16 @@ bool weight_map(CUtensorMap* m, const void* p, int WB, int n_mat, int rows, int 
 // W_gate and W_up of n_mat experts as one 4-D tensor [2][n_mat][rows][K]
 // whose outer stride is the byte distance between the two arrays (based at
 // the lower one: up_first when that is W_up), so that one box carries the
-// same rows of both. Needs the distance to be a multiple of 16 bytes, at
-// least the size of one array (they do not overlap) and below 2^40 (the
-// tensor map's stride limit); otherwise returns false and the kernel loads
-// the two matrices as separate boxes.
+// same rows of both. Needs the distance to be a non-zero multiple of 16
+// bytes below 2^40 (the tensor map's stride limit); otherwise returns false
+// and the kernel loads the two matrices as separate boxes.
 bool pair_map(CUtensorMap* m, int* up_first, const void* gate, const void* up, int WB, int n_mat,
               int rows, int K) {
   const int ks = WB == 2 ? 256 : 128;
   const uintptr_t pg = reinterpret_cast<uintptr_t>(gate), pu = reinterpret_cast<uintptr_t>(up);
   const uint64_t delta = pu > pg ? pu - pg : pg - pu;
   const uint64_t mat = (uint64_t)rows * K * WB;
-  if (delta % 16 != 0 || delta < mat * (uint64_t)n_mat || delta >= (1ull << 40)) return false;
+  if (delta == 0 || delta % 16 != 0 || delta >= (1ull << 40)) return false;
   *up_first = pu < pg ? 1 : 0;
   const uint64_t dims[4] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n_mat, 2};
   const uint64_t strides[3] = {(uint64_t)K * WB, mat, delta};
