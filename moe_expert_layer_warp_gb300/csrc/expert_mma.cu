@@ -21,11 +21,16 @@
 // halves are separate columns of one B tile — rows [0, h) the tokens' hi
 // halves, rows [h, 2h) their lo halves, h = 8, 16 or 32 ≥ the group's tokens,
 // N = 2h — so one MMA per K-step covers both, and the epilogue adds column t
-// and column h + t. Phase 0 (gate and up, one 64-column K-step per stage, two
-// accumulators) writes h as its hi/lo halves; phase 1 (down, two K-steps per
-// stage) writes the weighted slot outputs.
+// and column h + t. Phase 0 stacks 64 rows of W_gate over the same 64 rows
+// of W_up as one 128-row A tile, so one accumulator holds both products
+// (TMEM lanes 0-63 and 64-127) and a phase-0 job covers 64 rows of I — half
+// the bytes of a 128-row gate tile plus a 128-row up tile, which halves the
+// grain of the work a call is dealt in without cutting K. The epilogue
+// warps of the up half hand their values to the gate half through shared
+// memory, which writes h as its hi/lo halves. Phase 1 (down) writes the
+// weighted slot outputs. Every stage carries two 64-column K-steps.
 //
-// Jobs. A job is (entry, 128-row tile, piece of K). When a phase has fewer
+// Jobs. A job is (entry, tile, piece of K). When a phase has fewer
 // tiles than CTAs, each tile is cut into S ≤ 8 pieces along K so that every
 // SM streams. Every piece stores its fp32 partial sums and counts
 // itself per 32-row quarter with a release reduction (nothing waits for
@@ -56,7 +61,8 @@
 namespace moe {
 namespace {
 
-constexpr int kM = 128;                             // weight rows per tile
+constexpr int kM = 128;                             // A rows per tile (MMA M)
+constexpr int kH0 = 64;                             // rows of I per phase-0 tile (gate and up)
 constexpr int kSub = kMmaSub;                       // tokens per entry (≤ MMA N)
 constexpr int kStages = 4;
 constexpr int kThreads = 384;
@@ -76,12 +82,14 @@ static_assert(kSub == 32, "the epilogue and the TMEM slots assume at most 32 tok
 constexpr int kOffBar = kStages * kStageBytes;
 constexpr int kPubSlots = 8;                        // ring of finished phase-0 jobs
 constexpr int kFinSlots = 16;                       // per finisher: ring of quarters to finish
-constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots + 2 * 4 * kFinSlots;
+constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots + 2 * 4 * kFinSlots + 2;
 constexpr int kOffPlan = kOffBar + kNumBars * 8;
 constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
 constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
 constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
-constexpr int kSmemBytes = kOffMisc + 128 * 4 + 1024;  // + slack to align the base to 1024
+constexpr int kOffXch = kOffMisc + 128 * 4;         // [kH0 rows][kSub tokens] fp32: up → gate half
+constexpr int kSmemBytes = kOffXch + kH0 * kSub * 4 + 1024;  // + slack to align the base to 1024
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 // Token tensors read as B, for h = 8, 16, 32 rows: routed-group inputs (x
 // gathered in union order, or x for per-slot), shared-expert inputs (x),
@@ -91,15 +99,16 @@ constexpr int kSmemBytes = kOffMisc + 128 * 4 + 1024;  // + slack to align the b
 // two K-steps ([2 K-steps][2][h][64]).
 enum { kXA, kXS, kHH, kNumB };
 
-// Weight maps (bf16, 128-byte swizzle, 128 rows × 64 columns per K-step).
-// gu/sgu: W_gate and W_up as one [2][E][rows][K] tensor (the outer stride is
-// the distance between the two arrays, pair/spair set when expressible;
-// up_first when W_up lies below W_gate), so one box carries both tiles of a
-// phase-0 stage; wg/wu/swg/swu load them separately otherwise. wd/swd:
-// W_down viewed as [K/64][E][rows][64] (a 128-byte stride between 64-column
-// K-steps), so one box carries the two K-steps of a phase-1 stage. An SM's
-// TMA stream completes boxes at a roughly fixed rate, so fewer boxes per
-// stage raise what one SM can pull from HBM.
+// Weight maps (bf16, 128-byte swizzle, 64-column K-steps). gu/sgu: W_gate
+// and W_up as one [K/64][2][E][I][64] tensor (the pair stride is the
+// distance between the two arrays, pair/spair set when expressible;
+// up_first when W_up lies below W_gate), so one box carries the stacked
+// 64 + 64-row A tiles of both K-steps of a phase-0 stage; wg/wu/swg/swu load
+// 64-row tiles one K-step at a time otherwise. wd/swd: W_down viewed as
+// [K/64][E][rows][64] (a 128-byte stride between 64-column K-steps), so one
+// box carries the two K-steps of a phase-1 stage. An SM's TMA stream
+// completes boxes at a roughly fixed rate, so fewer boxes per stage raise
+// what one SM can pull from HBM.
 struct Maps {
   CUtensorMap wg, wu, wd, swg, swu, swd, gu, sgu;
   CUtensorMap b[3][kNumB];                // [h = 8, 16, 32][tensor]
@@ -151,6 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   uint64_t* pub_empty = pub_full + kPubSlots;
   uint64_t* fin_full = pub_empty + kPubSlots;  // [4][kFinSlots] epilogue warp q → finisher q
   uint64_t* fin_empty = fin_full + 4 * kFinSlots;
+  uint64_t* xfull = fin_empty + 4 * kFinSlots;  // up-half epilogue warps → gate half
+  uint64_t* xempty = xfull + 1;
+  float* xch = reinterpret_cast<float*>(smem + kOffXch);
   Entry* plan = reinterpret_cast<Entry*>(smem + kOffPlan);
   int* row_out = reinterpret_cast<int*>(smem + kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + kOffRowW);
@@ -184,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       mbar_init(&fin_full[i], 1);
       mbar_init(&fin_empty[i], 1);
     }
+    mbar_init(xfull, 2);
+    mbar_init(xempty, 2);
     *abort_flag = 0;
     *max_m = 0;
     fence_mbar_init();
@@ -207,15 +221,16 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   pdl_trigger();
   const uint32_t tmem = *tmem_base;
 
-  // Partial sums: slabs of [2 (gate, up) or 1][npad tokens][128 rows] fp32.
+  // Partial sums: slabs of [npad tokens][128 A rows] fp32 (phase 0: 64 gate
+  // rows over 64 up rows).
   const int npad = *max_m <= 16 ? 16 : 32;
-  const size_t slab0 = (size_t)2 * npad * kM, slab1 = (size_t)npad * kM;  // floats
-  const size_t budget0 = a.part_bytes / 3 * 2, budget1 = a.part_bytes - budget0;
+  const size_t slab0 = (size_t)npad * kM, slab1 = (size_t)npad * kM;  // floats
+  const size_t budget0 = a.part_bytes / 2, budget1 = a.part_bytes - budget0;
   float* part0 = a.part;
   float* part1 = a.part + budget0 / 4;
   const int target = kJobsPerCta * (int)gridDim.x;
-  const Cut c0 = make_cut((a.I + kM - 1) / kM, a.d / 64, n_groups * ((a.I + kM - 1) / kM), target,
-                          budget0, slab0 * 4);
+  const Cut c0 = make_cut(a.I / kH0, (a.d + 127) / 128, n_groups * (a.I / kH0), target, budget0,
+                          slab0 * 4);
   const Cut c1 = make_cut((a.d + kM - 1) / kM, (a.I + 127) / 128,
                           n_groups * ((a.d + kM - 1) / kM), target, budget1, slab1 * 4);
   const int J0 = n_groups * c0.T * c0.S, J = J0 + n_groups * c1.T * c1.S;
@@ -270,18 +285,23 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           unsigned char* bt = st + 2 * kTileBytes;
           if (ks == piece * c.kc) stage_job[stage] = job;
           if (ph == 0) {
-            const int k0 = ks * 64;
-            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * bbytes);
+            // A: [K-step][64 rows of the lower array][64 rows of the other]
+            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 4 * bbytes);
             if (sh ? prm.maps.spair : prm.maps.pair) {
-              tma_load_4d(st, sh ? &prm.maps.sgu : &prm.maps.gu, k0, tile * kM, ec, 0, &full[stage],
-                          pol_w);
-            } else {
-              tma_load_3d(st, sh ? &prm.maps.swg : &prm.maps.wg, k0, tile * kM, ec, &full[stage],
-                          pol_w);
-              tma_load_3d(st + kTileBytes, sh ? &prm.maps.swu : &prm.maps.wu, k0, tile * kM, ec,
+              tma_load_5d(st, sh ? &prm.maps.sgu : &prm.maps.gu, 0, tile * kH0, ec, 0, 2 * ks,
                           &full[stage], pol_w);
+            } else {
+              const CUtensorMap* wg = sh ? &prm.maps.swg : &prm.maps.wg;
+              const CUtensorMap* wu = sh ? &prm.maps.swu : &prm.maps.wu;
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const int k0 = (2 * ks + j) * 64;
+                tma_load_3d(st + j * kTileBytes, wg, k0, tile * kH0, ec, &full[stage], pol_w);
+                tma_load_3d(st + j * kTileBytes + kTileBytes / 2, wu, k0, tile * kH0, ec,
+                            &full[stage], pol_w);
+              }
             }
-            tma_load_3d(bt, &bm[sh ? kXS : kXA], k0, en.arow, 0, &full[stage], pol_x);
+            tma_load_4d(bt, &bm[sh ? kXS : kXA], 0, en.arow, 0, 2 * ks, &full[stage], pol_x);
           } else {
             mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 4 * bbytes);
             tma_load_4d(st, sh ? &prm.maps.swd : &prm.maps.wd, 0, tile * kM, ec, 2 * ks,
@@ -337,31 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             ok = false;
             break;
           }
+          // the stage's two K-steps: A tiles at st and st + kTileBytes, the
+          // tokens' [hi | lo] rows at bt and bt + 2h·128 bytes
           const uint32_t st = smem_addr(smem + stage * kStageBytes);
-          // phase 0: a0 the gate tile, a1 the up tile (the pair box puts the
-          // lower array first); phase 1: the two K-steps of the down tile
-          const uint32_t swap = ph == 0 && (plan[g].src < 0 ? prm.maps.sup_first : prm.maps.up_first)
-                                    ? kTileBytes : 0u;
-          const uint64_t a0 = umma::desc_sw128(st + swap);
-          const uint64_t a1 = umma::desc_sw128(st + (kTileBytes - swap));
+          const uint64_t a0 = umma::desc_sw128(st);
+          const uint64_t a1 = umma::desc_sw128(st + kTileBytes);
           const uint32_t bt = st + 2 * kTileBytes;
           const uint64_t b0 = umma::desc_sw128(bt);                   // K-step 0: hi | lo rows
           const bool first = ks == ks0;
-          if (ph == 0) {
+          const uint64_t b1 = umma::desc_sw128(bt + 2 * b_rows(m) * 128);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t acc = (!first || j != 0) ? 1u : 0u;
-              umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, acc);        // gate · [x_hi | x_lo]
-              umma::mma_bf16(dacc + 64, a1 + 2 * j, b0 + 2 * j, idesc, acc);   // up · [x_hi | x_lo]
-            }
-          } else {
-            const uint64_t b1 = umma::desc_sw128(bt + 2 * b_rows(m) * 128);  // K-step 1
+          for (int j = 0; j < 4; ++j)
+            umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, (!first || j != 0) ? 1u : 0u);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              umma::mma_bf16(dacc, a0 + 2 * j, b0 + 2 * j, idesc, (!first || j != 0) ? 1u : 0u);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) umma::mma_bf16(dacc, a1 + 2 * j, b1 + 2 * j, idesc, 1u);
-          }
+          for (int j = 0; j < 4; ++j) umma::mma_bf16(dacc, a1 + 2 * j, b1 + 2 * j, idesc, 1u);
           issued_any = true;
           umma::commit(&empty[stage]);  // frees the stage once these MMAs have read it
           if (++stage == kStages) {
@@ -391,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     uint32_t sphase = 0;
     int pub_n = 0;  // phase-0 jobs handed to the publisher so far
     int fin_n = 0;  // quarters handed to finisher `quad` so far (lane 0)
+    int x_n = 0;    // phase-0 tiles passed through xch so far
     uint64_t* my_fin_full = fin_full + quad * kFinSlots;
     uint64_t* my_fin_empty = fin_empty + quad * kFinSlots;
     volatile int* my_fin_job = fin_job + quad * kFinSlots;
@@ -426,31 +436,29 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + slot * kSlotCols;
       // Token c's sum is column c (hi half) plus column hb + c (lo half).
       const int hb = b_rows(m);
-      uint32_t gr[32], ur[32];  // gate (phase 0) or down (phase 1) sums, up sums
+      // this warp's 32 rows of the tile: phase 0 gate or up rows (the half
+      // holding rows 64·up_first .. +63 is the gate), phase 1 down rows
+      uint32_t gr[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) gr[c] = ur[c] = 0u;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {  // q = 0: gate or down, q = 1: up
-        if (q == 1 && ph != 0) break;
-        uint32_t* r = q == 0 ? gr : ur;
-        const uint32_t tq = taddr + q * 64;
+      for (int c = 0; c < 32; ++c) gr[c] = 0u;
+      {
         uint32_t t0[16], t1[16];
         if (hb == 8) {
-          umma::ld_x16(tq, t0);
+          umma::ld_x16(taddr, t0);
           umma::wait_ld();
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            r[c] = __float_as_uint(__uint_as_float(t0[c]) + __uint_as_float(t0[8 + c]));
+            gr[c] = __float_as_uint(__uint_as_float(t0[c]) + __uint_as_float(t0[8 + c]));
         } else {
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             if (half * 16 < hb) {
-              umma::ld_x16(tq + 16 * half, t0);
-              umma::ld_x16(tq + hb + 16 * half, t1);
+              umma::ld_x16(taddr + 16 * half, t0);
+              umma::ld_x16(taddr + hb + 16 * half, t1);
               umma::wait_ld();
 #pragma unroll
               for (int c = 0; c < 16; ++c)
-                r[16 * half + c] = __float_as_uint(__uint_as_float(t0[c]) + __uint_as_float(t1[c]));
+                gr[16 * half + c] = __float_as_uint(__uint_as_float(t0[c]) + __uint_as_float(t1[c]));
             }
           }
         }
@@ -459,7 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[slot]);  // accumulator slot free again
       float* gv = reinterpret_cast<float*>(gr);
-      float* uv = reinterpret_cast<float*>(ur);
       const Cut& cut = ph == 0 ? c0 : c1;
       if (cut.S > 1) {
         // A piece: store the partial sums of the warp's 32 rows and count
@@ -469,12 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
         float* mine = (ph == 0 ? part0 : part1) +
                       ((size_t)(g * cut.T + tile) * cut.S + piece) * sfl;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (c < m) {
-            mine[c * kM + r_in] = gv[c];
-            if (ph == 0) mine[(npad + c) * kM + r_in] = uv[c];
-          }
-        }
+        for (int c = 0; c < 32; ++c)
+          if (c < m) mine[c * kM + r_in] = gv[c];
         __syncwarp();  // the warp's partials before lane 0's release
         if (lane == 0) red_release_add((ph == 0 ? cnt0 : cnt1) + (g * cut.T + tile) * 4 + quad, 1);
         if (lane == 0 && piece == cut.S - 1) {
@@ -496,17 +499,46 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       // One piece: the epilogue finishes the tile's quarter itself.
       const int row = tile * kM + r_in;
       if (ph == 0) {
-        if (row < a.I) {
+        // the up half hands its sums to the gate half (bounded waits on
+        // two mbarriers; xch holds one tile's up rows at a time)
+        const int upf = en.src < 0 ? prm.maps.sup_first : prm.maps.up_first;
+        const int hrow = r_in & (kH0 - 1);
+        const bool up_half = (quad >> 1) != upf;
+        int xok = 1;  // lane 0 waits, the warp follows its result
+        if (lane == 0)
+          xok = up_half ? mbar_wait(xempty, (uint32_t)((x_n & 1) ^ 1), a.err, 0x356)
+                        : mbar_wait(xfull, (uint32_t)(x_n & 1), a.err, 0x357);
+        xok = __shfl_sync(0xffffffffu, xok, 0);
+        __syncwarp();  // lane 0's acquire before every lane's accesses
+        if (up_half) {
+          if (xok) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (c < m) {
-              const float hv = silu(gv[c]) * uv[c];
-              const uint16_t hi = to_bf16(hv);
-              const size_t at = (size_t)(en.row0 + c) * a.I + row;
-              a.h16[at] = hi;
-              a.h16lo[at] = to_bf16(hv - __uint_as_float((uint32_t)hi << 16));
+            for (int c = 0; c < 32; ++c)
+              if (c < m) xch[hrow * kSub + c] = gv[c];
+          }
+          __syncwarp();
+          if (xok && lane == 0) mbar_arrive(xfull);
+        } else {
+          const int irow = tile * kH0 + hrow;
+          if (xok && irow < a.I) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              if (c < m) {
+                const float hv = silu(gv[c]) * xch[hrow * kSub + c];
+                const uint16_t hi = to_bf16(hv);
+                const size_t at = (size_t)(en.row0 + c) * a.I + irow;
+                a.h16[at] = hi;
+                a.h16lo[at] = to_bf16(hv - __uint_as_float((uint32_t)hi << 16));
+              }
             }
           }
+          __syncwarp();
+          if (xok && lane == 0) mbar_arrive(xempty);
+        }
+        ++x_n;
+        if (!xok) {
+          *abort_flag = 1;
+          break;
         }
         // Hand the quarter to the publisher thread: __syncwarp orders the
         // warp's h stores before lane 0's arrive (release, CTA scope).
@@ -560,7 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     // wait (bounded) until the S pieces of the quarter are counted, add the
     // pieces in piece order (lane l: row 32q + l; four tokens per round of
     // loads), finish the rows and, in phase 0, publish the quarter to the
-    // group's phase-1 jobs.
+    // group's phase-1 jobs. In phase 0 the finisher of a gate quarter also
+    // waits for and adds the up rows 64 apart (quarter q ^ 2); the finisher
+    // of an up quarter only publishes.
     const int q = warp - 8;
     const int row_in = q * 32 + lane;
     uint64_t* my_full = fin_full + q * kFinSlots;
@@ -578,18 +612,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
       int ph, g, tile, piece;
       decode(job, &ph, &g, &tile, &piece);
       const Cut& cut = ph == 0 ? c0 : c1;
-      if (lane == 0) {
-        ok = wait_count((ph == 0 ? cnt0 : cnt1) + (g * cut.T + tile) * 4 + q, cut.S, a.err, 0x361);
+      const Entry en = plan[g];
+      const int upf = en.src < 0 ? prm.maps.sup_first : prm.maps.up_first;
+      const bool up_q = ph == 0 && (q >> 1) != upf;
+      if (lane == 0 && !up_q) {
+        const int* cnt = (ph == 0 ? cnt0 : cnt1) + (g * cut.T + tile) * 4;
+        ok = wait_count(cnt + q, cut.S, a.err, 0x361) &&
+             (ph != 0 || wait_count(cnt + (q ^ 2), cut.S, a.err, 0x362));
         if (!ok) *abort_flag = 1;
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       __syncwarp();  // lane 0's acquire before every lane's reads
-      const Entry en = plan[g];
       const int m = en.m;
       const size_t sfl = ph == 0 ? slab0 : slab1;
       const float* base = (ph == 0 ? part0 : part1) + (size_t)(g * cut.T + tile) * cut.S * sfl;
-      const int row = tile * kM + row_in;
-      for (int cb = 0; ok && cb < m; cb += 4) {
+      const int row = ph == 0 ? tile * kH0 + (row_in & (kH0 - 1)) : tile * kM + row_in;
+      for (int cb = 0; ok && !up_q && cb < m; cb += 4) {
         float sg[4], su[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) sg[u] = su[u] = 0.f;
@@ -601,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             for (int u = 0; u < 4; ++u) {
               if (cb + u < m) {
                 sg[u] += __ldcg(src + (cb + u) * kM + row_in);
-                if (ph == 0) su[u] += __ldcg(src + (npad + cb + u) * kM + row_in);
+                if (ph == 0) su[u] += __ldcg(src + (cb + u) * kM + (row_in ^ kH0));
               }
             }
           }
@@ -641,28 +679,30 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   }
 }
 
+// W_gate or W_up [n_mat][rows][K] in 64-row boxes of one K-step.
 bool w_map(CUtensorMap* m, const void* p, int n_mat, int rows, int K) {
   const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n_mat};
   const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)rows * K * 2};
-  const uint32_t box[3] = {64, (uint32_t)kM, 1};
+  const uint32_t box[3] = {64, (uint32_t)kH0, 1};
   return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// W_gate and W_up as one [2][n_mat][rows][K] tensor based at the lower of the
-// two arrays; false (load them separately) unless their distance is a
-// non-zero multiple of 16 bytes below 2^40, the tensor map's stride limit.
+// W_gate and W_up as one [K/64][2][n_mat][rows][64] tensor based at the
+// lower of the two arrays: a box [2 K-steps][2][64 rows][64] is the stage's
+// two stacked A tiles. False (load them separately) unless their distance is
+// a non-zero multiple of 16 bytes below 2^40, the tensor map's stride limit.
 bool pair_map(CUtensorMap* m, int* up_first, const void* gate, const void* up, int n_mat,
               int rows, int K) {
   const uintptr_t pg = reinterpret_cast<uintptr_t>(gate), pu = reinterpret_cast<uintptr_t>(up);
   const uint64_t delta = pu > pg ? pu - pg : pg - pu;
   if (delta == 0 || delta % 16 != 0 || delta >= (1ull << 40)) return false;
   *up_first = pu < pg ? 1 : 0;
-  const uint64_t dims[4] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n_mat, 2};
-  const uint64_t strides[3] = {(uint64_t)K * 2, (uint64_t)rows * K * 2, delta};
-  const uint32_t box[4] = {64, (uint32_t)kM, 1, 2};
+  const uint64_t dims[5] = {64, (uint64_t)rows, (uint64_t)n_mat, 2, (uint64_t)(K / 64)};
+  const uint64_t strides[4] = {(uint64_t)K * 2, (uint64_t)rows * K * 2, delta, 128};
+  const uint32_t box[5] = {64, (uint32_t)kH0, 1, 2, 2};
   return make_tmap(m, reinterpret_cast<const void*>(pu < pg ? pu : pg),
-                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
+                   CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -676,19 +716,13 @@ bool down_map(CUtensorMap* m, const void* p, int n_mat, int rows, int K) {
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Token rows [2 (hi, lo)][rows][K] bf16: a box [2][box_rows][64] per K-step
-// (chunks = 1), or [chunks][2][box_rows][64] over consecutive K-steps (the
+// Token rows [2 (hi, lo)][rows][K] bf16 viewed as [K/64][2][rows][64]: a box
+// [2 K-steps][2][box_rows][64] is the B tiles of a stage's two K-steps (the
 // K-step dimension outermost, 128 bytes apart).
-bool b_map(CUtensorMap* m, const void* p, int rows, int K, int box_rows, int chunks) {
+bool b_map(CUtensorMap* m, const void* p, int rows, int K, int box_rows) {
   const uint64_t dims[4] = {64, (uint64_t)rows, 2, (uint64_t)(K / 64)};
   const uint64_t strides[3] = {(uint64_t)K * 2, (uint64_t)rows * K * 2, 128};
-  const uint32_t box[4] = {64, (uint32_t)box_rows, 2, (uint32_t)chunks};
-  if (chunks == 1) {
-    const uint64_t d3[3] = {(uint64_t)K, (uint64_t)rows, 2};
-    const uint32_t b3[3] = {64, (uint32_t)box_rows, 2};
-    return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, d3, strides, b3,
-                     CU_TENSOR_MAP_SWIZZLE_128B);
-  }
+  const uint32_t box[4] = {64, (uint32_t)box_rows, 2, 2};
   return make_tmap(m, p, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, dims, strides, box,
                    CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -723,9 +757,9 @@ bool build_maps(const ExpertArgs& a, Maps* M) {
   for (int si = 0; si < 3; ++si) {
     const int br = 8 << si;
     CUtensorMap* B = M->b[si];
-    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br, 1);
-    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br, 1);
-    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br, 2);
+    ok &= b_map(&B[kXA], xa, xa_rows, a.d, br);
+    ok &= b_map(&B[kXS], a.x16, a.n, a.d, br);
+    ok &= b_map(&B[kHH], a.h16, hrows, a.I, br);
   }
   return ok;
 }
