@@ -15,9 +15,11 @@ oracle on the same workload instead (a bounded sample per step).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -396,13 +398,22 @@ TRAFFIC_SOURCES = ("expert_stream.cu", "expert_mma.cu", "engine.cu", "plan.cuh",
                    "launch.h", "tcgen05.cuh", "tmap.h", "api.cu")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed,
+    so that the hash below changes with the code, not with its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
-    """sha256 (first 16 hex digits) over the sources of the expert call: the
-    prep kernel, both expert kernels and the choice between them."""
-    import hashlib
+    """sha256 (first 16 hex digits) over the code of the expert call's
+    sources (comments excluded): the prep kernel, both expert kernels and
+    the choice between them."""
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES:
-        h.update(open(os.path.join(ROOT, "moe_expert_layer_warp_gb300", "csrc", f), "rb").read())
+        path = os.path.join(ROOT, "moe_expert_layer_warp_gb300", "csrc", f)
+        h.update(_code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -129,8 +129,8 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
 // per-element instruction, so it keeps its rate however many tokens a group
 // holds; but it works in 128-row tiles, a group's down tiles wait for all of
 // its gate/up tiles, and with fewer tiles than SMs it must cut tiles along K
-// and add the pieces across CTAs. The CUDA-core kernel works in 16- and
-// 32-row tiles, so few groups still fill the GPU, but its arithmetic per
+// and add the pieces across CTAs. The CUDA-core kernel works in 32- and
+// 64-row tiles, so few groups still fill the GPU, but its arithmetic per
 // weight byte grows with the tokens per group. Measured on GB300
 // (DeepSeek-V2-Lite- and Mixtral-shaped layers): one-token groups
 // (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups; dedup
