@@ -132,10 +132,12 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
 // and add the pieces across CTAs. The CUDA-core kernel works in 32- and
 // 64-row tiles, so few groups still fill the GPU, but its arithmetic per
 // weight byte grows with the tokens per group. Measured on GB300
-// (DeepSeek-V2-Lite- and Mixtral-shaped layers): one-token groups
-// (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups; dedup
-// groups, which hold several tokens, go faster on the tensor cores from
-// ~350 tiles with 12 groups or more, or with 3 tokens or more per group.
+// (DeepSeek-V2-Lite-, Mixtral- and DeepSeek-V3-shaped layers): one-token
+// groups (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups,
+// and at any count when an expert spans 64 or more 128-row tiles (Mixtral,
+// V3: 1-3 % faster); dedup groups, which hold several tokens, go faster on
+// the tensor cores from ~350 tiles with 12 groups or more, or with 3 tokens
+// or more per group.
 // The groups of a dedup call are known only on the device: the estimate
 // takes half of min(E, n·k) distinct experts. MOE_MMA_MIN_M in the
 // environment (read once; for tuning) fixes instead the smallest group
@@ -153,7 +155,7 @@ int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   bool mma;
   if (engine == 0) {
     const int groups = pairs + shared;
-    mma = groups * tiles >= 400 && groups >= 12;
+    mma = groups * tiles >= 400 && groups >= 12 && tiles < 64;
   } else {
     const int routed = std::max(1, std::min(d->n_experts, pairs) / 2);
     const int groups = routed + shared;
