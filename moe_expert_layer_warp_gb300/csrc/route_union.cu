@@ -66,17 +66,22 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 #pragma unroll
   for (int t = 0; t < kGateTokens; ++t) s[t] = c[t] = 0.f;
   const float4* wrow = reinterpret_cast<const float4*>(wg + (size_t)e * d) + base4;
+  const float4* xrow = reinterpret_cast<const float4*>(x + (size_t)t0 * d) + base4;
+  const int d4 = d >> 2;
   for (int i = lane; i < chunk4; i += 32) {
+    // every load of the step first, so that they are in flight together
     const float4 w = __ldg(wrow + i);
+    float4 xv[kGateTokens];
+#pragma unroll
+    for (int t = 0; t < kGateTokens; ++t)
+      xv[t] = t < nt ? __ldg(xrow + (size_t)t * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int t = 0; t < kGateTokens; ++t) {
       if (t < nt) {
-        const float4 xv =
-            __ldg(reinterpret_cast<const float4*>(x + (size_t)(t0 + t) * d) + base4 + i);
-        dot2_step(w.x, xv.x, s[t], c[t]);
-        dot2_step(w.y, xv.y, s[t], c[t]);
-        dot2_step(w.z, xv.z, s[t], c[t]);
-        dot2_step(w.w, xv.w, s[t], c[t]);
+        dot2_step(w.x, xv[t].x, s[t], c[t]);
+        dot2_step(w.y, xv[t].y, s[t], c[t]);
+        dot2_step(w.z, xv[t].z, s[t], c[t]);
+        dot2_step(w.w, xv[t].w, s[t], c[t]);
       }
     }
   }
@@ -279,13 +284,22 @@ __global__ void __launch_bounds__(256)
   const int c4 = blockIdx.x * blockDim.x + threadIdx.x;
   if (c4 * 4 >= d) return;
   const float4* src = reinterpret_cast<const float4*>(y_slot + (size_t)t * slots * d) + c4;
-  float4 acc = __ldg(src);
-  for (int j = 1; j < slots; ++j) {
-    const float4 v = __ldg(src + (size_t)j * (d >> 2));
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
+  // every slot's load first, so that they are in flight together; then the
+  // sum in slot order
+  constexpr int kMaxSlots = MOE_MAX_TOPK + MOE_MAX_SHARED;
+  float4 v[kMaxSlots];
+#pragma unroll
+  for (int j = 0; j < kMaxSlots; ++j)
+    if (j < slots) v[j] = __ldg(src + (size_t)j * (d >> 2));
+  float4 acc = v[0];
+#pragma unroll
+  for (int j = 1; j < kMaxSlots; ++j) {
+    if (j < slots) {
+      acc.x += v[j].x;
+      acc.y += v[j].y;
+      acc.z += v[j].z;
+      acc.w += v[j].w;
+    }
   }
   reinterpret_cast<float4*>(y + (size_t)t * d)[c4] = acc;
 }
