@@ -56,6 +56,10 @@ def parse_args():
                    help="profiling case WORKLOAD:ENGINE:N (e.g. v2lite:perslot:1): runs "
                         "--passes passes of one layer and prints their mean time")
     p.add_argument("--passes", type=int, default=4)
+    p.add_argument("--sweep", default=None, choices=["tiny", "v2lite", "mixtral", "v3"],
+                   help="one layer of WORKLOAD at every pass size and rho of that workload, "
+                        "both engines: requested bytes, time and bandwidth per n, r(n), the "
+                        "byte share and the crossover")
     p.add_argument("--stack", action="store_true",
                    help="26-layer V2-Lite stack: fit the step-time model on one layer run "
                         "alone, predict the stack's passes and compare with measured ones")
@@ -945,9 +949,89 @@ def run_case(args):
                       "union": int(R.union_count.item())}))
 
 
+SWEEP_PASSES = 2    # distinct hidden-state passes per (rho, n)
+
+
+def run_sweep(args):
+    """One layer of a workload at each of its pass sizes and rhos through
+    both engines; each pass timed as run_case times it (a CUDA graph behind
+    an L2 flush, with and without the expert call). Prints one JSON line per
+    rho: requested bytes, expert-call time and bandwidth per n and engine,
+    the byte share u(n), the bandwidth ratio r(n) and the crossover."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    from moe_expert_layer_warp_gb300 import api, configs, stepmodel, synth
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    w = getattr(configs, CASES[args.sweep])
+    sh = w.shape
+    L = synth.make_layer(sh, w.weight_seed, "cuda")
+    R = PassRunner(L, max(w.pass_sizes) * w.streams)
+    st = torch.cuda.current_stream()
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
+    t_flush = time_graphs([capture_graph(lambda s: flush.sum())], 6)[0]
+    engines = ("perslot", "dedup")
+    for rho in w.rhos:
+        samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
+        tfix = {n: [] for n in w.pass_sizes}
+        for n in w.pass_sizes:
+            for f in range(SWEEP_PASSES):
+                x = torch.from_numpy(synth.make_pass(sh.d, n, rho, [
+                    w.x_seed_base + 5000 + 97 * f + 13 * s for s in range(w.streams)])).cuda()
+                m = x.shape[0]
+                for eng in engines:
+                    R.forward(x, eng, st)
+                    b = [int(v) for v in R.bytes.cpu().tolist()]
+                    req = (b[0] if eng == "perslot" else b[1]) + b[2]
+
+                    def one(s, with_expert):
+                        flush.sum()
+                        R.route(x, s)
+                        R.build_union(m, s)
+                        if with_expert:
+                            R.experts(x, eng, s)
+                        R.combine(m, s)
+                    ga = capture_graph(lambda s: one(s, True))
+                    gb = capture_graph(lambda s: one(s, False))
+                    ta, tb = time_graphs([ga, gb], 3)
+                    samples[eng][n].append((req, max(ta - tb, 1e-9)))
+                    tfix[n].append(max(tb - t_flush, 0.0))
+                    del ga, gb
+        if api.moe_last_device_error() != api.MOE_OK:
+            raise RuntimeError("device error in the sweep")
+        ns = list(w.pass_sizes)
+        bw = {e: {n: stepmodel.effective_bandwidth([b for b, _ in samples[e][n]],
+                                                   [t for _, t in samples[e][n]]) for n in ns}
+              for e in engines}
+        u = {n: stepmodel.byte_share([b for b, _ in samples["dedup"][n]],
+                                     [b for b, _ in samples["perslot"][n]]) for n in ns}
+        r = {n: bw["dedup"][n] / bw["perslot"][n] for n in ns}
+        d = {"u_bar": [round(u[n], 6) for n in ns], "r": [round(r[n], 6) for n in ns],
+             "crossover_n": stepmodel.crossover(ns, u, r),
+             "t_fix_us": [round(statistics.median(tfix[n]) * 1e6, 2) for n in ns]}
+        line = {"sweep": w.name, "rho": rho, "streams": w.streams, "n": list(w.pass_sizes),
+                "passes_per_point": SWEEP_PASSES,
+                "timing": "expert call inside a CUDA-graph-replayed pass behind a 256 MB L2 "
+                          "flush (graph with minus graph without the call)",
+                "peak_GBs": peaks()[0]}
+        for eng in engines:
+            line[eng] = {
+                "requested_MB": [round(sum(b for b, _ in samples[eng][n]) / len(samples[eng][n])
+                                       / 1e6, 1) for n in w.pass_sizes],
+                "expert_us": [round(sum(t for _, t in samples[eng][n]) / len(samples[eng][n])
+                                    * 1e6, 2) for n in w.pass_sizes],
+                "GBs": [round(sum(b for b, _ in samples[eng][n]) / sum(t for _, t in samples[eng][n])
+                              / 1e9, 1) for n in w.pass_sizes]}
+        for k in ("u_bar", "r", "crossover_n", "t_fix_us"):
+            line[k] = d[k]
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
-    if args.case:
+    if args.sweep:
+        run_sweep(args)
+    elif args.case:
         run_case(args)
     elif args.stack:
         run_stack(args)
