@@ -64,12 +64,15 @@ namespace {
 constexpr int kM = 128;                             // A rows per tile (MMA M)
 constexpr int kH0 = 64;                             // rows of I per phase-0 tile (gate and up)
 constexpr int kSub = kMmaSub;                       // tokens per entry (≤ MMA N)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 5;
 constexpr int kThreads = 384;
 constexpr int kTileBytes = kM * 128;                // [128 rows][64 bf16]
 constexpr int kBStepBytes = 2 * kSub * 128;         // one K-step of tokens: [2h ≤ 64 rows][64 bf16]
-// stage: two weight tiles, then the token tiles of one or two K-steps
-constexpr int kStageBytes = 2 * kTileBytes + 2 * kBStepBytes;
+// A stage holds the weight tiles of two K-steps, then their token tiles
+// (2 K-steps × [hi | lo] × h rows × 128 bytes). The ring's stage count is set
+// per launch from the largest h of the call: 5 stages for h ≤ 16, 4 for 32.
+constexpr int kRingBytes = 5 * (2 * kTileBytes + 2 * 2 * 16 * 128);
+static_assert(4 * (2 * kTileBytes + 2 * kBStepBytes) <= kRingBytes, "four stages at h = 32");
 constexpr int kMaxEntries = max_entries(kSub);
 constexpr int kMaxRows = MOE_MAX_PAIRS + MOE_MAX_SHARED * MOE_MAX_TOKENS;
 constexpr int kSlotCols = 128;                      // TMEM columns per accumulator slot (gate, up)
@@ -79,13 +82,13 @@ constexpr int kMaxPieces = 8;
 static_assert(kMaxEntries == kMmaEntries, "tensor-core kernel entry count");
 static_assert(kSub == 32, "the epilogue and the TMEM slots assume at most 32 tokens");
 
-constexpr int kOffBar = kStages * kStageBytes;
+constexpr int kOffBar = kRingBytes;
 constexpr int kPubSlots = 8;                        // ring of finished phase-0 jobs
 constexpr int kFinSlots = 16;                       // per finisher: ring of quarters to finish
-constexpr int kNumBars = 2 * kStages + 4 + 1 + 2 * kPubSlots + 2 * 4 * kFinSlots + 2;
+constexpr int kNumBars = 2 * kMaxStages + 4 + 1 + 2 * kPubSlots + 2 * 4 * kFinSlots + 2;
 constexpr int kOffPlan = kOffBar + kNumBars * 8;
 constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
-constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
+constexpr int kOffRowW = kOffRowOut + kMaxRows * 2;
 constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
 constexpr int kOffXch = kOffMisc + 128 * 4;         // [kH0 rows][kSub tokens] fp32: up → gate half
 constexpr int kSmemBytes = kOffXch + kH0 * kSub * 4 + 1024;  // + slack to align the base to 1024
@@ -152,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* pub_full = drain + 1;  // epilogue warps → publisher: a phase-0 job's quarters
@@ -164,10 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   uint64_t* xempty = xfull + 1;
   float* xch = reinterpret_cast<float*>(smem + kOffXch);
   Entry* plan = reinterpret_cast<Entry*>(smem + kOffPlan);
-  int* row_out = reinterpret_cast<int*>(smem + kOffRowOut);
+  uint16_t* row_out = reinterpret_cast<uint16_t*>(smem + kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + kOffRowW);
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);  // [0..15] scan scratch
-  volatile int* stage_job = misc + 16;                  // [kStages]
+  volatile int* stage_job = misc + 16;                  // [kMaxStages]
   volatile int* acc_job = misc + 24;                    // [2]
   uint32_t* tmem_base = reinterpret_cast<uint32_t*>(misc + 28);
   volatile int* abort_flag = misc + 32;
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kMaxStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -224,6 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   // Partial sums: slabs of [npad tokens][128 A rows] fp32 (phase 0: 64 gate
   // rows over 64 up rows).
   const int npad = *max_m <= 16 ? 16 : 32;
+  // the ring: stages sized for the call's largest token tile
+  const int stage_bytes = 2 * kTileBytes + 4 * b_rows(*max_m) * 128;
+  const int n_stages = min(kMaxStages, kRingBytes / stage_bytes);
   const size_t slab0 = (size_t)npad * kM, slab1 = (size_t)npad * kM;  // floats
   const size_t budget0 = a.part_bytes / 2, budget1 = a.part_bytes - budget0;
   float* part0 = a.part;
@@ -281,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             ok = false;
             break;
           }
-          unsigned char* st = smem + stage * kStageBytes;
+          unsigned char* st = smem + stage * stage_bytes;
           unsigned char* bt = st + 2 * kTileBytes;
           if (ks == piece * c.kc) stage_job[stage] = job;
           if (ph == 0) {
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
             }
             tma_load_4d(bt, &bm[kHH], 0, en.row0, 0, 2 * ks, &full[stage], pol_x);
           }
-          if (++stage == kStages) {
+          if (++stage == n_stages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           }
           // the stage's two K-steps: A tiles at st and st + kTileBytes, the
           // tokens' [hi | lo] rows at bt and bt + 2h·128 bytes
-          const uint32_t st = smem_addr(smem + stage * kStageBytes);
+          const uint32_t st = smem_addr(smem + stage * stage_bytes);
           const uint64_t a0 = umma::desc_sw128(st);
           const uint64_t a1 = umma::desc_sw128(st + kTileBytes);
           const uint32_t bt = st + 2 * kTileBytes;
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           for (int j = 0; j < 4; ++j) umma::mma_bf16(dacc, a1 + 2 * j, b1 + 2 * j, idesc, 1u);
           issued_any = true;
           umma::commit(&empty[stage]);  // frees the stage once these MMAs have read it
-          if (++stage == kStages) {
+          if (++stage == n_stages) {
             stage = 0;
             phase ^= 1u;
           }

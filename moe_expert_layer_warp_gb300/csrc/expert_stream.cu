@@ -92,7 +92,7 @@ struct Layout {
   static constexpr int kOffBar = kStages * kStageBytes;
   static constexpr int kOffPlan = kOffBar + (2 * kStages + 2 * kPubSlots) * 8;
   static constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
-  static constexpr int kOffRowW = kOffRowOut + kMaxRows * 4;
+  static constexpr int kOffRowW = kOffRowOut + kMaxRows * 2;
   static constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
   static constexpr int kBytes = kOffMisc + 64 * 4;
 };
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   uint64_t* pub_full = empty + kStages;    // consumer warps → publisher: a phase-0 job's h is stored
   uint64_t* pub_empty = pub_full + kPubSlots;
   Entry* plan = reinterpret_cast<Entry*>(smem + L::kOffPlan);
-  int* row_out = reinterpret_cast<int*>(smem + L::kOffRowOut);
+  uint16_t* row_out = reinterpret_cast<uint16_t*>(smem + L::kOffRowOut);
   float* row_w = reinterpret_cast<float*>(smem + L::kOffRowW);
   int* misc = reinterpret_cast<int*>(smem + L::kOffMisc);  // [0..31] scan scratch
   volatile int* stage_job = misc + 32;                     // [kStages]

@@ -19,13 +19,28 @@
 namespace moe {
 
 struct Entry {
-  int src;    // routed expert id (>= 0), or -(i+1) for shared expert i
-  int row0;   // first activation row (in h)
-  int m;      // tokens of this sub-group
-  int arow;   // first row of the phase-0 input box (x row or gathered-x row); phase 1 reads h at row0
-  int first;  // first entry of this group's sub-groups
-  int q;      // number of sub-groups of this group
+  int src;         // routed expert id (>= 0), or -(i+1) for shared expert i
+  int row0;        // first activation row (in h)
+  int arow;        // first row of the phase-0 input box (x row or gathered-x row); phase 1
+                   //   reads h at row0
+  uint16_t first;  // first entry of this group's sub-groups
+  uint8_t m;       // tokens of this sub-group (≤ 32)
+  uint8_t q;       // number of sub-groups of this group (≤ 32)
 };
+static_assert(sizeof(Entry) == 16, "plan entry");
+static_assert(MOE_MAX_TOKENS * (MOE_MAX_TOPK + MOE_MAX_SHARED) <= 65536, "slot rows fit 16 bits");
+static_assert((MOE_MAX_TOKENS + kCcSub - 1) / kCcSub <= 255 && kMmaSub <= 255, "sub-groups fit 8 bits");
+
+MOE_DEV Entry make_entry(int src, int row0, int m, int arow, int first, int q) {
+  Entry e;
+  e.src = src;
+  e.row0 = row0;
+  e.arow = arow;
+  e.first = (uint16_t)first;
+  e.m = (uint8_t)m;
+  e.q = (uint8_t)q;
+  return e;
+}
 
 // Job jj of a phase with T tiles per entry: the jobs of a group's q sub-groups
 // are the q·T consecutive jobs from first·T, ordered tile-major.
@@ -85,7 +100,7 @@ MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
 // MMA_SIDE selects groups with m ≥ a.mma_min_m, else the others.
 // Needs blockDim.x ≥ MOE_MAX_EXPERTS (one thread per union expert).
 template <int SUB, bool MMA_SIDE>
-MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* row_w,
+MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, float* row_w,
                        int* scratch) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int P = a.n * a.k, S = a.k + a.s;
@@ -93,12 +108,12 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   int nr = 0;
   if (a.engine == 0) {
     if (mine(1)) {
-      for (int p = tid; p < P; p += nt) plan[p] = Entry{a.topk_idx[p], p, 1, p / a.k, p, 1};
+      for (int p = tid; p < P; p += nt) plan[p] = make_entry(a.topk_idx[p], p, 1, p / a.k, p, 1);
       nr = P;
     }
     for (int p = tid; p < P; p += nt) {
       const int t = p / a.k, j = p - t * a.k;
-      row_out[p] = t * S + j;
+      row_out[p] = (uint16_t)(t * S + j);
       row_w[p] = a.topk_w[p];
     }
   } else {
@@ -117,11 +132,11 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
     const int pos = block_exclusive_scan(nsub, scratch, &nr);
     for (int q = 0; q < nsub; ++q) {
       const int rr = r0 + q * SUB;
-      plan[pos + q] = Entry{e, rr, min(SUB, m - q * SUB), rr, pos, nsub};
+      plan[pos + q] = make_entry(e, rr, min(SUB, m - q * SUB), rr, pos, nsub);
     }
     for (int r = tid; r < P; r += nt) {
       const int t = a.pair_tok[r], j = a.pair_slot[r];
-      row_out[r] = t * S + j;
+      row_out[r] = (uint16_t)(t * S + j);
       row_w[r] = a.topk_w[t * a.k + j];
     }
   }
@@ -129,11 +144,11 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, int* row_out, float* ro
   for (int q = tid; q < a.s * per; q += nt) {
     const int i = q / per, c = q - (q / per) * per;
     const int rr = P + i * a.n + c * SUB;
-    plan[nr + q] = Entry{-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB, nr + i * per, per};
+    plan[nr + q] = make_entry(-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB, nr + i * per, per);
   }
   for (int r = tid; r < a.s * a.n; r += nt) {
     const int i = r / a.n, t = r - (r / a.n) * a.n;
-    row_out[P + r] = t * S + a.k + i;
+    row_out[P + r] = (uint16_t)(t * S + a.k + i);
     row_w[P + r] = 1.f;
   }
   return nr + a.s * per;
