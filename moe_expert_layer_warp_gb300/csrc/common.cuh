@@ -97,6 +97,20 @@ MOE_DEV uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+MOE_DEV uint64_t l2_evict_normal_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Weight loads: a per-slot call of several tokens reads an expert once per
+// slot that chose it, and L2 serves the repeats only if the lines stay
+// (normal eviction); otherwise every weight is read once, so its lines go
+// first and the activations and routing data stay.
+MOE_DEV uint64_t weight_policy(int keep_weights) {
+  return keep_weights ? l2_evict_normal_policy() : l2_evict_first_policy();
+}
+
 MOE_DEV uint64_t l2_evict_last_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));

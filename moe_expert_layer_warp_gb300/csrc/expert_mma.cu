@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   if (warp == 0) {
     // ------------------------------------------------------ producer thread --
     if (lane == 0) {
-      const uint64_t pol_w = l2_evict_first_policy();
+      const uint64_t pol_w = weight_policy(a.keep_weights);
       const uint64_t pol_x = l2_evict_last_policy();
       int stage = 0;
       uint32_t phase = 0;

@@ -78,6 +78,8 @@ struct ExpertArgs {
   size_t part_bytes;
   int mma_min_m;        // groups with at least this many tokens run on tensor cores
   int cc_waits_prep;    // 1: the CUDA-core kernel directly follows the prep kernel
+  int keep_weights;     // 1: weight loads use normal L2 eviction (per-slot calls of 3+ tokens,
+                        //   whose repeated experts L2 can serve), else evict-first
   float* y_slot;
   unsigned int* err;
 };
