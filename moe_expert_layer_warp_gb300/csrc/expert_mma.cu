@@ -28,7 +28,10 @@
 // grain of the work a call is dealt in without cutting K. The epilogue
 // warps of the up half hand their values to the gate half through shared
 // memory, which writes h as its hi/lo halves. Phase 1 (down) writes the
-// weighted slot outputs. Every stage carries two 64-column K-steps.
+// weighted slot outputs. Every stage carries two 64-column K-steps; the
+// ring holds as many stages as fit for the call's largest token tile (5 for
+// h ≤ 16, 4 for h = 32), which matters most for per-slot calls, about half
+// of whose weight reads hit L2 and half miss to DRAM.
 //
 // Jobs. A job is (entry, tile, piece of K). When a phase has fewer
 // tiles than CTAs, each tile is cut into S ≤ 8 pieces along K so that every
