@@ -180,9 +180,10 @@ def enqueue_step(w, runners, xs, step_idx, stream):
 
 
 def kernels_per_pass():
-    # moe_route: gate GEMV + top-k; moe_build_union: 1; expert call: prep + one
-    # expert kernel (tensor-core or CUDA-core, chosen per call); moe_combine: 1
-    return 2 + 1 + 2 + 1
+    # moe_route_union: gate GEMV + one CTA for top-k and union; expert call:
+    # prep + one expert kernel (tensor-core or CUDA-core, chosen per call);
+    # moe_combine: 1
+    return 2 + 2 + 1
 
 
 def capture_graph(fn):
@@ -250,8 +251,7 @@ def measure_breakdown(w, runners, xs):
 
             def one(s, rep, q, with_expert):
                 R, x = runners[rep], xs[n][q]
-                R.route(x, s)
-                R.build_union(n, s)
+                R.route_union(x, s)
                 if with_expert:
                     R.experts(x, eng, s)
                 R.combine(n, s)
@@ -791,8 +791,7 @@ def run_stack(args):
 
                 def one(s, x, with_expert):
                     flush.sum()
-                    R0.route(x, s)
-                    R0.build_union(n, s)
+                    R0.route_union(x, s)
                     if with_expert:
                         R0.experts(x, eng, s)
                     R0.combine(n, s)
@@ -915,8 +914,7 @@ def run_case(args):
 
     def one(s, with_expert):
         flush.sum()
-        R.route(x, s)
-        R.build_union(x.shape[0], s)
+        R.route_union(x, s)
         if with_expert:
             R.experts(x, eng, s)
         R.combine(x.shape[0], s)
@@ -928,8 +926,7 @@ def run_case(args):
     for _ in range(args.passes):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         torch.cuda._sleep(SPIN_CYCLES)      # device busy while the host queues the pass
-        R.route(x, st)
-        R.build_union(x.shape[0], st)
+        R.route_union(x, st)
         e[0].record(st)
         R.experts(x, eng, st)
         e[1].record(st)
@@ -986,8 +983,7 @@ def run_sweep(args):
 
                     def one(s, with_expert):
                         flush.sum()
-                        R.route(x, s)
-                        R.build_union(m, s)
+                        R.route_union(x, s)
                         if with_expert:
                             R.experts(x, eng, s)
                         R.combine(m, s)

@@ -148,6 +148,19 @@ moe_status moe_route_biased(const moe_layer_desc* desc, const float* w_router, c
 moe_status moe_build_union(const moe_layer_desc* desc, const int32_t* topk_idx, int32_t n,
                            const moe_union* u, void* stream);
 
+/* Routing and union in one call: the results of moe_route_biased followed by
+ * moe_build_union on its topk_idx, bit for bit, in two kernel launches
+ * instead of three (one CTA runs every token's top-k and then builds the
+ * union from that selection without a round trip through a kernel boundary).
+ *   bias, bias_in_weights  as moe_route_biased (bias NULL: plain moe_route).
+ *   topk_idx, topk_w       [n][k] out, as moe_route.
+ *   u                      out, as moe_build_union.
+ * Argument checks and errors: those of both calls.                          */
+moe_status moe_route_union(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                           int32_t bias_in_weights, const float* x, int32_t n,
+                           int32_t* topk_idx, float* topk_w, const moe_union* u, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* Per-slot engine: every (token t, slot j) runs its own expert FFN, reading
  * that expert's weights for that slot alone (requested bytes n·k·E_b), and
  * every shared expert runs once over all n tokens.

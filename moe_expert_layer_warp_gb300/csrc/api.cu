@@ -243,6 +243,33 @@ moe_status moe_build_union(const moe_layer_desc* desc, const int32_t* topk_idx, 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_build_union launch");
 }
 
+moe_status moe_route_union(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                           int32_t bias_in_weights, const float* x, int32_t n,
+                           int32_t* topk_idx, float* topk_w, const moe_union* u, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_desc(desc));
+  if (bias_in_weights != 0 && bias_in_weights != 1) return MOE_EINVAL;
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u) != 0) return MOE_EINVAL;
+  MOE_TRY(check_n(desc, n));
+  if (!w_router || !x || !topk_idx || !topk_w) return MOE_EINVAL;
+  if (!aligned16(w_router) || !aligned16(x)) return MOE_EINVAL;
+  if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot ||
+      !u->bytes)
+    return MOE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(u->bytes) & 7u) != 0) return MOE_EINVAL;
+  MOE_TRY(check_ws(desc, n, workspace, workspace_bytes));
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  WsLayout L = ws_layout(desc, n);
+  float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.logits);
+  cudaError_t e = moe::launch_route_union(
+      desc->d, desc->inter, desc->n_experts, desc->top_k, desc->n_shared,
+      desc->wdtype == MOE_W_F32 ? 4 : 2, n, x, w_router, bias, bias_in_weights, logits, topk_idx,
+      topk_w, u->union_ids, u->union_count, u->offsets, u->pair_tok, u->pair_slot, u->bytes,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_union launch");
+}
+
 static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_layer_weights* w,
                              const float* x, int32_t n, const int32_t* topk_idx,
                              const moe_union* u, const float* topk_w, void* workspace,

@@ -41,6 +41,15 @@ cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
                          int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
                          uint64_t* bytes, unsigned int* err, cudaStream_t stream);
 
+// Routing and union in two launches: the gate GEMV, then one CTA that runs
+// the top-k of every token and builds the union from its own selection.
+cudaError_t launch_route_union(int d, int I, int E, int k, int s, int wbytes, int n,
+                               const float* x, const float* w_router, const float* bias,
+                               int bias_in_weights, float* logits, int32_t* topk_idx,
+                               float* topk_w, int32_t* union_ids, int32_t* union_count,
+                               int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
+                               uint64_t* bytes, cudaStream_t stream);
+
 // Everything the expert kernels read. h is the SwiGLU activation scratch,
 // one fp32 row of length I per (pair or shared-expert token) row.
 struct ExpertArgs {

@@ -122,15 +122,11 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 constexpr int kTopkWarps = 8;
 constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
 
-__global__ void __launch_bounds__(kTopkWarps * 32)
-    topk_kernel(int E, int k, int n, const float* __restrict__ logits,
-                const float* __restrict__ bias, int bias_in_weights,
-                int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
-  pdl_wait();
-  pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTopkWarps + warp;
-  if (t >= n) return;
+// One warp selects token t's k experts and writes their weights; the
+// selected indices also go to sel[t·k + j] when sel is not null.
+MOE_DEV void topk_token(int t, int lane, int E, int k, const float* __restrict__ logits,
+                        const float* __restrict__ bias, int bias_in_weights,
+                        int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int* sel) {
   float v[kPerLane];
   uint32_t taken = 0;
 #pragma unroll
@@ -186,7 +182,19 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   if (lane < k) {
     topk_idx[(size_t)t * k + lane] = my_e;
     topk_w[(size_t)t * k + lane] = ej / z;
+    if (sel) sel[t * k + lane] = my_e;
   }
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    topk_kernel(int E, int k, int n, const float* __restrict__ logits,
+                const float* __restrict__ bias, int bias_in_weights,
+                int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t < n) topk_token(t, lane, E, k, logits, bias, bias_in_weights, topk_idx, topk_w, nullptr);
 }
 
 // ------------------------------------------------------------------ union --
@@ -194,29 +202,25 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 // a pair inside its expert is the number of earlier pairs (token-major order)
 // with the same expert, so the result is independent of scheduling.
 constexpr int kUnionThreads = 512;
+constexpr int kRouteUnionThreads = 1024;
 
-__global__ void __launch_bounds__(kUnionThreads)
-    union_kernel(int E, int k, int n, uint64_t expert_bytes, int s,
-                 const int32_t* __restrict__ topk_idx, int32_t* __restrict__ union_ids,
-                 int32_t* __restrict__ union_count, int32_t* __restrict__ offsets,
-                 int32_t* __restrict__ pair_tok, int32_t* __restrict__ pair_slot,
-                 uint64_t* __restrict__ bytes, unsigned int* err) {
-  __shared__ int sidx[MOE_MAX_PAIRS];
-  __shared__ int cnt[MOE_MAX_EXPERTS];
-  __shared__ int start[MOE_MAX_EXPERTS];
-  pdl_wait();
-  pdl_trigger();
+struct UnionOut {
+  int32_t* union_ids;
+  int32_t* union_count;
+  int32_t* offsets;
+  int32_t* pair_tok;
+  int32_t* pair_slot;
+  uint64_t* bytes;
+};
+
+// The union from the pairs' experts sidx[0 .. n·k) in shared memory, with
+// cnt[] zeroed; every thread of the CTA calls it.
+MOE_DEV void union_body(int E, int k, int n, uint64_t expert_bytes, int s, const int* sidx,
+                        int* cnt, int* start, const UnionOut& out) {
+  int32_t* __restrict__ union_ids = out.union_ids;
+  int32_t* __restrict__ offsets = out.offsets;
   const int P = n * k;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
-  for (int p = tid; p < P; p += blockDim.x) {
-    int v = topk_idx[p];
-    if (v < 0 || v >= E) {
-      report_error(err, ERR_CHECK, 0x101);
-      v = 0;
-    }
-    sidx[p] = v;
-  }
   __syncthreads();
   for (int p = tid; p < P; p += blockDim.x) atomicAdd(&cnt[sidx[p]], 1);
   __syncthreads();
@@ -258,10 +262,10 @@ __global__ void __launch_bounds__(kUnionThreads)
     }
     if (lane == 31) {
       offsets[ip] = ic;
-      *union_count = ip;
-      bytes[0] = (uint64_t)P * expert_bytes;
-      bytes[1] = (uint64_t)ip * expert_bytes;
-      bytes[2] = (uint64_t)s * expert_bytes;
+      *out.union_count = ip;
+      out.bytes[0] = (uint64_t)P * expert_bytes;
+      out.bytes[1] = (uint64_t)ip * expert_bytes;
+      out.bytes[2] = (uint64_t)s * expert_bytes;
     }
   }
   __syncthreads();
@@ -270,9 +274,51 @@ __global__ void __launch_bounds__(kUnionThreads)
     int rank = 0;
     for (int q = 0; q < p; ++q) rank += (sidx[q] == e);
     const int row = start[e] + rank;
-    pair_tok[row] = p / k;
-    pair_slot[row] = p - (p / k) * k;
+    out.pair_tok[row] = p / k;
+    out.pair_slot[row] = p - (p / k) * k;
   }
+}
+
+__global__ void __launch_bounds__(kUnionThreads)
+    union_kernel(int E, int k, int n, uint64_t expert_bytes, int s,
+                 const int32_t* __restrict__ topk_idx, UnionOut o, unsigned int* err) {
+  __shared__ int sidx[MOE_MAX_PAIRS];
+  __shared__ int cnt[MOE_MAX_EXPERTS];
+  __shared__ int start[MOE_MAX_EXPERTS];
+  pdl_wait();
+  pdl_trigger();
+  const int P = n * k;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int p = tid; p < P; p += blockDim.x) {
+    int v = topk_idx[p];
+    if (v < 0 || v >= E) {
+      report_error(err, ERR_CHECK, 0x101);
+      v = 0;
+    }
+    sidx[p] = v;
+  }
+  union_body(E, k, n, expert_bytes, s, sidx, cnt, start, o);
+}
+
+// Top-k and union in one CTA: warp w selects tokens w, w + 32, …, into
+// topk_idx / topk_w and into shared memory, then the CTA builds the union.
+// The same selection and the same union as topk_kernel then union_kernel.
+__global__ void __launch_bounds__(kRouteUnionThreads)
+    topk_union_kernel(int E, int k, int n, uint64_t expert_bytes, int s,
+                      const float* __restrict__ logits, const float* __restrict__ bias,
+                      int bias_in_weights, int32_t* __restrict__ topk_idx,
+                      float* __restrict__ topk_w, UnionOut o) {
+  __shared__ int sidx[MOE_MAX_PAIRS];
+  __shared__ int cnt[MOE_MAX_EXPERTS];
+  __shared__ int start[MOE_MAX_EXPERTS];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
+  for (int t = warp; t < n; t += blockDim.x >> 5)
+    topk_token(t, lane, E, k, logits, bias, bias_in_weights, topk_idx, topk_w, sidx);
+  union_body(E, k, n, expert_bytes, s, sidx, cnt, start, o);
 }
 
 // ---------------------------------------------------------------- combine --
@@ -342,8 +388,26 @@ cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
                          int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
                          uint64_t* bytes, unsigned int* err, cudaStream_t stream) {
   const uint64_t eb = 3ull * (uint64_t)d * (uint64_t)I * (uint64_t)wbytes;
+  const UnionOut o{union_ids, union_count, offsets, pair_tok, pair_slot, bytes};
   return launch_pdl(union_kernel, dim3(1), dim3(kUnionThreads), 0, stream, E, k, n, eb, s,
-                    topk_idx, union_ids, union_count, offsets, pair_tok, pair_slot, bytes, err);
+                    topk_idx, o, err);
+}
+
+cudaError_t launch_route_union(int d, int I, int E, int k, int s, int wbytes, int n,
+                               const float* x, const float* w_router, const float* bias,
+                               int bias_in_weights, float* logits, int32_t* topk_idx,
+                               float* topk_w, int32_t* union_ids, int32_t* union_count,
+                               int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
+                               uint64_t* bytes, cudaStream_t stream) {
+  dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
+  cudaError_t e = launch_pdl(gate_logits_kernel, g1, dim3(kGateWarps * 32), 0, stream, d, E, n, x,
+                             w_router, logits);
+  if (e != cudaSuccess) return e;
+  const uint64_t eb = 3ull * (uint64_t)d * (uint64_t)I * (uint64_t)wbytes;
+  const UnionOut o{union_ids, union_count, offsets, pair_tok, pair_slot, bytes};
+  return launch_pdl(topk_union_kernel, dim3(1), dim3(kRouteUnionThreads), 0, stream, E, k, n, eb,
+                    s, static_cast<const float*>(logits), bias, bias_in_weights, topk_idx, topk_w,
+                    o);
 }
 
 cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,

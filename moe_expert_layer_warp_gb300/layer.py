@@ -2,8 +2,9 @@
 
 ``PassRunner`` owns the device buffers a pass needs (workspace, routing,
 union, slot outputs, output) for passes of up to ``n_max`` tokens and calls
-the library's entry points in order: moe_route → moe_build_union →
-moe_verify_perslot or moe_verify_dedup → moe_combine. Buffers are allocated
+the library's entry points in order: moe_route_union (routing and union in
+one call; moe_route and moe_build_union separately through route() and
+build_union()) → moe_verify_perslot or moe_verify_dedup → moe_combine. Buffers are allocated
 once, through torch, at construction, and so are the C arguments that point
 at them: a call only marshals x and the stream.
 """
@@ -103,6 +104,14 @@ class PassRunner:
         api._check(self._lib.moe_build_union(self._desc, self._idx, n, self._uref,
                                              api._stream(stream)), "moe_build_union")
 
+    def route_union(self, x: torch.Tensor, stream=None, _xp=None):
+        """route() then build_union() in one library call (same results)."""
+        xp = _xp or self._x(x)
+        api._check(self._lib.moe_route_union(self._desc, self._router, self._bias, self._bias_w,
+                                             xp, x.shape[0], self._idx, self._tw, self._uref,
+                                             self._ws, self._ws_bytes, api._stream(stream)),
+                   "moe_route_union")
+
     def experts(self, x: torch.Tensor, engine: str, stream=None, _xp=None):
         xp = _xp or self._x(x)
         n = x.shape[0]
@@ -140,8 +149,7 @@ class PassRunner:
             raise ValueError("engine must be %r or %r" % (PERSLOT, DEDUP))
         n = x.shape[0]
         st = api._stream(stream)
-        self.route(x, st, xp)
-        self.build_union(n, st)
+        self.route_union(x, st, xp)
         self.experts(x, engine, st, xp)
         self.combine(n, st, out)
         return out if out is not None else self.y[: n * self.shape.d].view(n, self.shape.d)

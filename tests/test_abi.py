@@ -111,3 +111,32 @@ def test_biased_route_rejects_bad_mode_and_misaligned_bias(lib):
     assert f(ctypes.byref(desc), one, one, 2, one, 4, one, one, ws, big, None) == api.MOE_EINVAL
     assert f(ctypes.byref(desc), one, ctypes.c_void_p(4098), 1, one, 4, one, one, ws, big,
              None) == api.MOE_EINVAL
+
+
+def test_route_union_checks_both_calls_arguments(lib):
+    desc = api.make_desc(LayerShape(256, 8, 2, 512, 0, W_BF16))
+    one = ctypes.c_void_p(4096)
+    ws = ctypes.c_void_p(1 << 20)
+    big = 1 << 30
+    p = ctypes.c_void_p(8192)
+    u = api.UnionC(p, p, p, p, p, p)
+    f = lib.moe_route_union
+    # the union's outputs must all be given
+    empty = api.UnionC()
+    assert f(ctypes.byref(desc), one, None, 1, one, 4, one, one, ctypes.byref(empty), ws, big,
+             None) == api.MOE_EINVAL
+    # the routing checks: mode, bias alignment, null x, n out of range, workspace size
+    assert f(ctypes.byref(desc), one, one, 2, one, 4, one, one, ctypes.byref(u), ws, big,
+             None) == api.MOE_EINVAL
+    assert f(ctypes.byref(desc), one, ctypes.c_void_p(4098), 1, one, 4, one, one,
+             ctypes.byref(u), ws, big, None) == api.MOE_EINVAL
+    assert f(ctypes.byref(desc), one, None, 1, None, 4, one, one, ctypes.byref(u), ws, big,
+             None) == api.MOE_EINVAL
+    assert f(ctypes.byref(desc), one, None, 1, one, 0, one, one, ctypes.byref(u), ws, big,
+             None) == api.MOE_EINVAL
+    assert f(ctypes.byref(desc), one, None, 1, one, 4, one, one, ctypes.byref(u), ws, 16,
+             None) == api.MOE_EINVAL
+    # byte counters must be 8-byte aligned
+    odd = api.UnionC(p, p, p, p, p, ctypes.c_void_p(8196))
+    assert f(ctypes.byref(desc), one, None, 1, one, 4, one, one, ctypes.byref(odd), ws, big,
+             None) == api.MOE_EINVAL

@@ -174,6 +174,51 @@ def test_biased_routing_and_layer(bias_in_weights):
     pu.assert_close_rms(y_dd[toks], y_o, pu.y_tol(shape), "biased dedup y")
 
 
+@pytest.mark.parametrize("shape,n,bias_mode", [
+    (LayerShape(2048, 64, 6, 1408, 2, W_BF16), 9, None),
+    (LayerShape(256, 32, 4, 128, 1, W_BF16), 128, None),        # n·k = 512, four token rounds
+    (LayerShape(128, 256, 16, 64, 1, W_F32), 32, None),         # E = 256, k = 16
+    (LayerShape(512, 32, 4, 256, 1, W_BF16), 17, 1),
+    (LayerShape(512, 32, 4, 256, 1, W_BF16), 17, 0),
+    (LayerShape(128, 8, 1, 64, 2, W_F32), 1, None),
+], ids=["v2lite-n9", "max-pairs", "max-experts-top16", "bias-in-weights", "selection-only",
+        "top1-n1"])
+def test_route_union_equals_separate_calls(shape, n, bias_mode):
+    """moe_route_union (top-k inside the union's CTA) against moe_route or
+    moe_route_biased followed by moe_build_union: every routing and union
+    output bit for bit, on the same inputs."""
+    L = synth.make_layer(shape, 57, "cuda")
+    x = torch.from_numpy(synth.make_pass(shape.d, n, 0.7, [123])).cuda()
+    bias = None
+    if bias_mode is not None:
+        bias = torch.from_numpy(np.random.default_rng(3).standard_normal(shape.n_experts)
+                                .astype(np.float32) * 0.05).cuda()
+    R = PassRunner(L, n, bias=bias, bias_in_weights=bool(bias_mode))
+
+    def outputs():
+        idx, w = (t.cpu().numpy().copy() for t in R.routing(n))
+        u = {k: (v.cpu().numpy().copy() if torch.is_tensor(v) else v)
+             for k, v in R.union(n).items()}
+        return idx, w, u
+
+    for t in (R.topk_idx, R.topk_w, R.union_ids, R.offsets, R.pair_tok, R.pair_slot):
+        t.fill_(-7)
+    R.route(x)
+    R.build_union(n)
+    a = outputs()
+    for t in (R.topk_idx, R.topk_w, R.union_ids, R.offsets, R.pair_tok, R.pair_slot):
+        t.fill_(-7)
+    R.route_union(x)
+    b = outputs()
+    from moe_expert_layer_warp_gb300 import api
+    assert api.moe_last_device_error() == api.MOE_OK
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
+    assert a[2]["count"] == b[2]["count"]
+    for key in ("union_ids", "offsets", "pair_tok", "pair_slot", "bytes"):
+        np.testing.assert_array_equal(a[2][key], b[2][key])
+
+
 def test_identical_tokens_select_k_experts():
     shape = LayerShape(512, 32, 4, 256, 1, W_BF16)
     L = synth.make_layer(shape, 5, "cuda")
