@@ -123,47 +123,56 @@ constexpr int kTopkWarps = 8;
 constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
 
 // One warp selects token t's k experts and writes their weights; the
-// selected indices also go to sel[t·k + j] when sel is not null.
+// selected indices also go to sel[t·k + j] when sel is not null. Each round
+// takes the warp maximum of order-preserving integer keys of the remaining
+// scores (redux.sync), then the lowest expert index holding that key, so
+// the larger score wins and equal scores go to the lower index.
+MOE_DEV uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;  // -0 and +0 compare equal, so they get one key
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+MOE_DEV float key_score(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 MOE_DEV void topk_token(int t, int lane, int E, int k, const float* __restrict__ logits,
                         const float* __restrict__ bias, int bias_in_weights,
                         int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int* sel) {
-  float v[kPerLane];
+  uint32_t key[kPerLane];
   uint32_t taken = 0;
 #pragma unroll
   for (int r = 0; r < kPerLane; ++r) {
     const int e = lane + 32 * r;
     if (e < E) {
-      v[r] = bias ? __fadd_rn(logits[(size_t)t * E + e], bias[e]) : logits[(size_t)t * E + e];
+      const float v =
+          bias ? __fadd_rn(logits[(size_t)t * E + e], bias[e]) : logits[(size_t)t * E + e];
+      key[r] = score_key(v);
     } else {
-      v[r] = -INFINITY;
+      key[r] = 0u;
       taken |= 1u << r;
     }
   }
   float my_v = 0.f, v0 = 0.f;
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
+    // this lane's best remaining key (the lower register, so the lower
+    // expert index, on equal keys); 0 when none remains
+    uint32_t bk = 0u;
+    int br = -1;
 #pragma unroll
     for (int r = 0; r < kPerLane; ++r) {
-      if (!((taken >> r) & 1u)) {
-        const int e = lane + 32 * r;
-        if (v[r] > bv || (v[r] == bv && e < be)) {
-          bv = v[r];
-          be = e;
-        }
+      if (!((taken >> r) & 1u) && (br < 0 || key[r] > bk)) {
+        bk = key[r];
+        br = r;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, br >= 0 ? bk : 0u);
+    const uint32_t cand = (br >= 0 && bk == mk) ? (uint32_t)(lane + 32 * br) : 0xffffffffu;
+    const int be = (int)__reduce_min_sync(0xffffffffu, cand);
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    const float bv = key_score(mk);
     if (j == 0) v0 = bv;
     if (lane == j) {
       my_v = bv;

@@ -219,6 +219,33 @@ def test_route_union_equals_separate_calls(shape, n, bias_mode):
         np.testing.assert_array_equal(a[2][key], b[2][key])
 
 
+@pytest.mark.parametrize("shape", [LayerShape(256, 64, 6, 128, 1, W_BF16),
+                                   LayerShape(128, 256, 16, 64, 1, W_F32)],
+                         ids=["E64-top6", "E256-top16"])
+def test_exact_ties_go_to_the_lower_index(shape):
+    """Experts 2i and 2i+1 get identical gate rows, so their logits are
+    bitwise equal: the selection takes the lower index first and every
+    selected odd expert follows its even twin, as the oracle orders them."""
+    L = synth.make_layer(shape, 61, "cuda")
+    L.w_router[1::2] = L.w_router[0::2]
+    n = 16
+    x = synth.make_pass(shape.d, n, 0.0, [5])
+    R = PassRunner(L, n)
+    R.route_union(torch.from_numpy(x).cuda())
+    idx, w = (t.cpu().numpy() for t in R.routing(n))
+    from moe_expert_layer_warp_gb300 import api
+    assert api.moe_last_device_error() == api.MOE_OK
+    orc = oracle.route(x, L.w_router.cpu().numpy(), shape.top_k)
+    np.testing.assert_array_equal(idx, orc["idx"])
+    for t in range(n):
+        for j, e in enumerate(idx[t]):
+            if e % 2 == 1:
+                assert j > 0 and idx[t][j - 1] == e - 1, (t, idx[t])
+    np.testing.assert_allclose(w, orc["w"], rtol=0, atol=1e-5)
+    pairs = w.reshape(n, shape.top_k // 2, 2)
+    np.testing.assert_array_equal(pairs[:, :, 0], pairs[:, :, 1])
+
+
 def test_identical_tokens_select_k_experts():
     shape = LayerShape(512, 32, 4, 256, 1, W_BF16)
     L = synth.make_layer(shape, 5, "cuda")
