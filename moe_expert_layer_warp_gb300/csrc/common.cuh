@@ -150,6 +150,21 @@ MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int 
       : "memory");
 }
 
+// Prefetch of a tensor-map box into L2 (no shared memory, no completion).
+MOE_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+MOE_DEV void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 MOE_DEV void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                          uint64_t* bar, uint64_t policy) {
   asm volatile(

@@ -186,6 +186,32 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   }
   const int n_groups = build_plan<kMaxM, false>(a, plan, row_out, row_w, misc);
   __syncthreads();
+  // Each CTA's first job is job blockIdx.x. Its weights need nothing from
+  // the prep kernel, so while that kernel runs the producer prefetches the
+  // first kStages stages of a phase-0 first job into L2 (measured on the
+  // DeepSeek-V2-Lite-shaped layer: 1.0-1.3 us off one-token passes; issuing
+  // the loads themselves that early, or prefetching the whole job, was
+  // slower: the weight traffic then delays the prep kernel).
+  if (threadIdx.x == kConsumerWarps * 32 && a.cc_waits_prep &&
+      (int)blockIdx.x < n_groups * (a.I / kRowsPhase0)) {
+    int g, tile;
+    job_entry(plan, (int)blockIdx.x, a.I / kRowsPhase0, &g, &tile);
+    const Entry en = plan[g];
+    const bool shared_expert = en.src < 0;
+    const int ecoord = shared_expert ? -en.src - 1 : en.src;
+    const int nks = min((a.d + KS - 1) / KS, kStages);
+    for (int ks = 0; ks < nks; ++ks) {
+      if (shared_expert ? prm.maps.spair : prm.maps.pair) {
+        tma_prefetch_4d(shared_expert ? &prm.maps.sgu : &prm.maps.gu, ks * KS,
+                        tile * kRowsPhase0, ecoord, 0);
+      } else {
+        tma_prefetch_3d(shared_expert ? &prm.maps.sw0 : &prm.maps.w0, ks * KS,
+                        tile * kRowsPhase0, ecoord);
+        tma_prefetch_3d(shared_expert ? &prm.maps.sw1 : &prm.maps.w1, ks * KS,
+                        tile * kRowsPhase0, ecoord);
+      }
+    }
+  }
   // The prep kernel (counters zeroed, rows gathered) must be complete. When
   // this kernel follows the tensor-core kernel, that kernel released it only
   // after its own wait on the prep kernel, so this kernel starts at once and
@@ -209,8 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      while (ok) {
-        int job = atomicAdd(job_counter, 1);
+      // the first job is blockIdx.x (prefetched above); the counter hands
+      // out jobs gridDim.x, gridDim.x + 1, … after it
+      for (bool first = true; ok; first = false) {
+        int job = first ? min((int)blockIdx.x, J) : atomicAdd(job_counter, 1) + (int)gridDim.x;
         if (job >= J) {
           // end marker for the consumers
           if (!mbar_wait(&empty[stage], phase ^ 1u, a.err, 0x201)) {
