@@ -28,6 +28,12 @@ namespace {
 constexpr int kGateWarps = 8;
 constexpr int kGateTokens = 8;
 
+// Prefetch of `bytes` (a multiple of 16) at a 16-byte aligned global
+// address into L2 (no completion).
+MOE_DEV void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 MOE_DEV void two_sum(float a, float b, float& s, float& e) {
   s = __fadd_rn(a, b);
   const float bb = __fsub_rn(s, a);
@@ -54,6 +60,9 @@ __global__ void __launch_bounds__(kGateWarps * 32)
     gate_logits_kernel(int d, int E, int n, const float* __restrict__ x,
                        const float* __restrict__ wg, float* __restrict__ logits) {
   __shared__ float part[kGateWarps][kGateTokens][2];
+  // W_g is constant: its row can move into L2 while the previous kernel
+  // finishes (one prefetch per expert row)
+  if (threadIdx.x == 0 && blockIdx.y == 0) l2_prefetch_bulk(wg + (size_t)blockIdx.x * d, d * 4);
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
