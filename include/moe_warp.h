@@ -190,6 +190,27 @@ moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights*
 moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t n, float* y,
                        void* stream);
 
+/* Engines of moe_verify_pass. */
+typedef enum { MOE_ENGINE_PERSLOT = 0, MOE_ENGINE_DEDUP = 1 } moe_engine;
+
+/* One whole verification pass in one call: moe_route_union (routing with
+ * the optional bias, and the union), then moe_verify_perslot or
+ * moe_verify_dedup, then moe_combine, on one stream; the same launches and
+ * results as those calls made one by one. For callers that issue passes
+ * from the host one at a time (no CUDA graph), it saves the per-call host
+ * cost of three calls.
+ *   weights->w_router is W_g; bias, bias_in_weights as moe_route_biased.
+ *   engine   MOE_ENGINE_PERSLOT or MOE_ENGINE_DEDUP (else MOE_EINVAL).
+ *   topk_idx, topk_w, u, y_slot   the intermediate outputs, written as the
+ *            single calls write them (caller-owned device buffers).
+ *   y        [n][d] fp32 out, as moe_combine.
+ * Returns the first failing call's status; nothing after it is launched.   */
+moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                           const float* bias, int32_t bias_in_weights, const float* x, int32_t n,
+                           int32_t engine, int32_t* topk_idx, float* topk_w, const moe_union* u,
+                           void* workspace, size_t workspace_bytes, float* y_slot, float* y,
+                           void* stream);
+
 /* Allocation-free variant of moe_verify_dedup (the sources have no
  * counterpart: this exists for callers, not for the method). Some callers
  * cannot allocate device memory: a plugin whose host framework owns all GPU

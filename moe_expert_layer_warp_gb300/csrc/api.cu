@@ -430,6 +430,25 @@ moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
 }
 
+moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                           const float* bias, int32_t bias_in_weights, const float* x, int32_t n,
+                           int32_t engine, int32_t* topk_idx, float* topk_w, const moe_union* u,
+                           void* workspace, size_t workspace_bytes, float* y_slot, float* y,
+                           void* stream) {
+  if (!weights || !y_slot || !y || (engine != MOE_ENGINE_PERSLOT && engine != MOE_ENGINE_DEDUP))
+    return MOE_EINVAL;
+  MOE_TRY(moe_route_union(desc, weights->w_router, bias, bias_in_weights, x, n, topk_idx, topk_w, u,
+                          workspace, workspace_bytes, stream));
+  if (engine == MOE_ENGINE_PERSLOT) {
+    MOE_TRY(moe_verify_perslot(desc, weights, x, n, topk_idx, topk_w, workspace, workspace_bytes,
+                               y_slot, stream));
+  } else {
+    MOE_TRY(moe_verify_dedup(desc, weights, x, n, u, topk_w, workspace, workspace_bytes, y_slot,
+                             stream));
+  }
+  return moe_combine(desc, y_slot, n, y, stream);
+}
+
 moe_status moe_diag_bounded_wait(int32_t limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return MOE_EINVAL;
   DeviceInfo* di;

@@ -2,9 +2,10 @@
 
 ``PassRunner`` owns the device buffers a pass needs (workspace, routing,
 union, slot outputs, output) for passes of up to ``n_max`` tokens and calls
-the library's entry points in order: moe_route_union (routing and union in
-one call; moe_route and moe_build_union separately through route() and
-build_union()) → moe_verify_perslot or moe_verify_dedup → moe_combine. Buffers are allocated
+the library's entry points: forward() makes one moe_verify_pass call
+(moe_route_union → moe_verify_perslot or moe_verify_dedup → moe_combine);
+route(), build_union(), route_union(), experts() and combine() make the
+single calls. Buffers are allocated
 once, through torch, at construction, and so are the C arguments that point
 at them: a call only marshals x and the stream.
 """
@@ -148,10 +149,18 @@ class PassRunner:
         if engine not in (PERSLOT, DEDUP):
             raise ValueError("engine must be %r or %r" % (PERSLOT, DEDUP))
         n = x.shape[0]
-        st = api._stream(stream)
-        self.route_union(x, st, xp)
-        self.experts(x, engine, st, xp)
-        self.combine(n, st, out)
+        y = self._y
+        if out is not None:
+            if (out.dtype != torch.float32 or out.numel() != n * self.shape.d or
+                    out.device != self.weights.device or not out.is_contiguous()):
+                raise ValueError("out must be a contiguous float32 [%d][%d] tensor on %s"
+                                 % (n, self.shape.d, self.weights.device))
+            y = ctypes.c_void_p(out.data_ptr())
+        eng = api.MOE_ENGINE_PERSLOT if engine == PERSLOT else api.MOE_ENGINE_DEDUP
+        api._check(self._lib.moe_verify_pass(self._desc, self._wref, self._bias, self._bias_w, xp,
+                                             n, eng, self._idx, self._tw, self._uref, self._ws,
+                                             self._ws_bytes, self._yslot, y, api._stream(stream)),
+                   "moe_verify_pass")
         return out if out is not None else self.y[: n * self.shape.d].view(n, self.shape.d)
 
     # -- views ---------------------------------------------------------------

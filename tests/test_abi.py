@@ -140,3 +140,22 @@ def test_route_union_checks_both_calls_arguments(lib):
     odd = api.UnionC(p, p, p, p, p, ctypes.c_void_p(8196))
     assert f(ctypes.byref(desc), one, None, 1, one, 4, one, one, ctypes.byref(odd), ws, big,
              None) == api.MOE_EINVAL
+
+
+def test_verify_pass_rejects_bad_engine_and_missing_outputs(lib):
+    desc = api.make_desc(LayerShape(256, 8, 2, 512, 0, W_BF16))
+    one = ctypes.c_void_p(4096)
+    p = ctypes.c_void_p(8192)
+    u = api.UnionC(p, p, p, p, p, p)
+    w = api.LayerWeightsC()
+    f = lib.moe_verify_pass
+    args = lambda wref, engine, y_slot, y: (ctypes.byref(desc), wref, None, 1, one, 4, engine, one,
+                                           one, ctypes.byref(u), ctypes.c_void_p(1 << 20), 1 << 30,
+                                           y_slot, y, None)
+    assert f(*args(ctypes.byref(w), 2, one, one)) == api.MOE_EINVAL      # unknown engine
+    assert f(*args(ctypes.byref(w), -1, one, one)) == api.MOE_EINVAL
+    assert f(*args(None, 0, one, one)) == api.MOE_EINVAL                 # no weights
+    assert f(*args(ctypes.byref(w), 1, None, one)) == api.MOE_EINVAL     # no y_slot
+    assert f(*args(ctypes.byref(w), 1, one, None)) == api.MOE_EINVAL     # no y
+    # the routing's own checks run first: W_g (weights.w_router) is NULL here
+    assert f(*args(ctypes.byref(w), 0, one, one)) == api.MOE_EINVAL

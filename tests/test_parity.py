@@ -246,6 +246,37 @@ def test_exact_ties_go_to_the_lower_index(shape):
     np.testing.assert_array_equal(pairs[:, :, 0], pairs[:, :, 1])
 
 
+@pytest.mark.parametrize("bias_mode", [None, 0], ids=["plain", "selection-only-bias"])
+def test_verify_pass_equals_single_calls(bias_mode):
+    """forward() (one moe_verify_pass call) against moe_route_union,
+    moe_verify_* and moe_combine made one by one: y, slot outputs and
+    routing bit for bit, for both engines."""
+    shape = LayerShape(576, 16, 4, 320, 1, W_BF16)
+    L = synth.make_layer(shape, 71, "cuda")
+    n = 11
+    x = torch.from_numpy(synth.make_pass(shape.d, n, 0.9, [19])).cuda()
+    bias = None
+    if bias_mode is not None:
+        bias = torch.from_numpy(np.random.default_rng(4).standard_normal(shape.n_experts)
+                                .astype(np.float32) * 0.05).cuda()
+    R = PassRunner(L, n, bias=bias, bias_in_weights=bool(bias_mode))
+    for eng in (PERSLOT, DEDUP):
+        y1 = R.forward(x, eng).cpu().numpy().copy()
+        s1 = R.slots(n).cpu().numpy().copy()
+        i1 = R.routing(n)[0].cpu().numpy().copy()
+        R.y.fill_(-1.0)
+        R.y_slot.fill_(-1.0)
+        R.route_union(x)
+        R.experts(x, eng)
+        R.combine(n)
+        y2 = R.y[: n * shape.d].view(n, shape.d).cpu().numpy()
+        from moe_expert_layer_warp_gb300 import api
+        assert api.moe_last_device_error() == api.MOE_OK
+        np.testing.assert_array_equal(y1.view(np.uint32), y2.view(np.uint32))
+        np.testing.assert_array_equal(s1.view(np.uint32), R.slots(n).cpu().numpy().view(np.uint32))
+        np.testing.assert_array_equal(i1, R.routing(n)[0].cpu().numpy())
+
+
 def test_identical_tokens_select_k_experts():
     shape = LayerShape(512, 32, 4, 256, 1, W_BF16)
     L = synth.make_layer(shape, 5, "cuda")
