@@ -421,10 +421,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic(name: str):
-    """DRAM bytes per launch from a committed ncu summary (``key: value``
-    lines), if its counters were taken on the current kernel sources; else
-    None."""
+TRAFFIC_FILE = "traffic_expert_call_v2lite_bench.txt"
+
+
+def load_traffic_record(name: str):
+    """The ``key: value`` lines of a committed ncu summary, if its counters
+    were taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None
@@ -435,10 +437,27 @@ def load_traffic(name: str):
             rec[k.strip()] = v.strip()
     if rec.get("sources_sha256_16") != kernel_source_hash():
         return None
+    return rec
+
+
+def load_traffic(name: str):
+    """DRAM bytes per expert call from a committed ncu summary, or None."""
+    rec = load_traffic_record(name)
     try:
-        return int(rec["dram_bytes_per_launch"])
+        return int(rec["dram_bytes_per_launch"]) if rec else None
     except (KeyError, ValueError):
         return None
+
+
+def load_perslot_dram(name: str, n_sizes: int):
+    """DRAM bytes read by one per-slot expert call at each pass size (the
+    same ncu capture), or None."""
+    rec = load_traffic_record(name)
+    try:
+        v = [int(t) for t in rec["perslot_dram_bytes_by_n"].split(",")] if rec else None
+    except (KeyError, ValueError):
+        return None
+    return v if v and len(v) == n_sizes else None
 
 
 def peaks():
@@ -649,6 +668,18 @@ def run_ours(args):
         }
         per_engine[eng]["expert_frac_of_peak"] = [round(g / peak, 3)
                                                   for g in per_engine[eng]["expert_GBs"]]
+    # The per-slot engine's DRAM bandwidth beside its requested-byte bandwidth:
+    # ncu DRAM reads of one call at each n (committed capture of this workload
+    # on these sources; every launch cold) over the call's measured time.
+    ps_dram = load_perslot_dram(TRAFFIC_FILE, len(w.pass_sizes))
+    if ps_dram:
+        t_call = [sum(s for _, s in samples["perslot"][n]) / len(samples["perslot"][n])
+                  for n in w.pass_sizes]
+        gbs = [round(b / t / 1e9, 1) for b, t in zip(ps_dram, t_call)]
+        per_engine["perslot"]["dram_GBs"] = gbs
+        per_engine["perslot"]["dram_frac_of_peak"] = [round(g / peak, 3) for g in gbs]
+    else:
+        per_engine["perslot"]["dram_GBs"] = None
     cpu = None if args.no_cpu_baseline else cpu_baseline_sample()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -667,7 +698,7 @@ def run_ours(args):
                                "down of every group",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": load_traffic("traffic_expert_call_v2lite_bench.txt")},
+                     "traffic": load_traffic(TRAFFIC_FILE)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_value(world, tokens_per_step, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
