@@ -19,9 +19,11 @@
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
 // Phase 0 computes h = silu(W_gate x) ⊙ (W_up x) in tiles of 32 rows of I;
 // phase 1 computes y_slot = w · (W_down h) in tiles of 64 rows of d. A job is
-// (sub-group, tile); the producer thread of each CTA takes the next job from
-// a global counter, and the sub-groups of one group take consecutive jobs
-// tile by tile, so that L2 serves their repeated weight tiles.
+// (sub-group, tile); CTA b's first job is job b (its first weight stages are
+// prefetched into L2 while the prep kernel still runs), after which the
+// producer thread of each CTA takes the next job from a global counter. The
+// sub-groups of one group take consecutive jobs tile by tile, so that L2
+// serves their repeated weight tiles.
 //
 // A stage holds 32 KB of weights — 32 rows of W_gate and the same 32 rows of
 // W_up, or 64 rows of W_down, × K_s = 256 bf16 / 128 fp32 columns — and the
