@@ -228,7 +228,10 @@ moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* 
  *     stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind (nothing in it needs to start at zero). Calls that overlap on
- *     the GPU — on two streams, or from two threads — race on it.          */
+ *     the GPU — on two streams, or from two threads — race on it.
+ *   - The array's address is cached per device for the life of the process,
+ *     as is the device error word's: the library must not be used across a
+ *     cudaDeviceReset (or any other teardown of the primary context).     */
 moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_weights* weights,
                                     const float* x, int32_t n, const moe_union* u,
                                     const float* topk_w, float* y_slot, void* stream);

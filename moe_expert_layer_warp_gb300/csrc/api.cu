@@ -404,8 +404,22 @@ size_t moe_noalloc_scratch_limit(void) { return kNoAllocScratchBytes; }
 moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_weights* weights,
                                     const float* x, int32_t n, const moe_union* u,
                                     const float* topk_w, float* y_slot, void* stream) {
-  MOE_TRY(check_desc(desc));
-  MOE_TRY(check_n(desc, n));
+  // Every refusal below leaves its own reason; none is left over from an
+  // earlier call.
+  g_last_cuda_err[0] = '\0';
+  auto refuse = [](moe_status st, const char* why) {
+    snprintf(g_last_cuda_err, sizeof g_last_cuda_err, "moe_verify_dedup_noalloc: %s", why);
+    return st;
+  };
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return refuse(st, "invalid or unsupported layer descriptor");
+  if (check_n(desc, n) != MOE_OK) return refuse(MOE_EINVAL, "pass size n out of range");
+  if (check_weights(desc, weights) != MOE_OK)
+    return refuse(MOE_EINVAL, "null or misaligned weight pointer");
+  if (!x || !topk_w || !y_slot || !aligned16(x))
+    return refuse(MOE_EINVAL, "null x, topk_w or y_slot, or x not 16-byte aligned");
+  if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot)
+    return refuse(MOE_EINVAL, "null union pointer");
   const size_t need = ws_layout(desc, n).total;
   if (need > kNoAllocScratchBytes) {
     snprintf(g_last_cuda_err, sizeof g_last_cuda_err,

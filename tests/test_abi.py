@@ -159,3 +159,31 @@ def test_verify_pass_rejects_bad_engine_and_missing_outputs(lib):
     assert f(*args(ctypes.byref(w), 1, one, None)) == api.MOE_EINVAL     # no y
     # the routing's own checks run first: W_g (weights.w_router) is NULL here
     assert f(*args(ctypes.byref(w), 0, one, one)) == api.MOE_EINVAL
+
+
+def test_noalloc_refusals_each_say_why(lib):
+    """Every host-side refusal of moe_verify_dedup_noalloc writes its own
+    reason, so a caller never reads one left over from an earlier call."""
+    f = lib.moe_verify_dedup_noalloc
+    desc = api.make_desc(LayerShape(256, 8, 2, 512, 0, W_BF16))
+    one = ctypes.c_void_p(4096)
+    p = ctypes.c_void_p(8192)
+    u = api.UnionC(p, p, p, p, p, p)
+    w = api.LayerWeightsC(one, one, one, one)
+    msg = lambda: lib.moe_last_cuda_error_string().decode()
+    bad = api.make_desc(LayerShape(256, 8, 9, 512, 0, W_BF16))          # k > E
+    assert f(ctypes.byref(bad), ctypes.byref(w), one, 4, ctypes.byref(u), one, one,
+             None) == api.MOE_EINVAL
+    assert "descriptor" in msg()
+    assert f(ctypes.byref(desc), ctypes.byref(w), one, 0, ctypes.byref(u), one, one,
+             None) == api.MOE_EINVAL
+    assert "pass size" in msg()
+    assert f(ctypes.byref(desc), ctypes.byref(api.LayerWeightsC()), one, 4, ctypes.byref(u), one,
+             one, None) == api.MOE_EINVAL
+    assert "weight" in msg()
+    assert f(ctypes.byref(desc), ctypes.byref(w), None, 4, ctypes.byref(u), one, one,
+             None) == api.MOE_EINVAL
+    assert "x" in msg() and "weight" not in msg()
+    assert f(ctypes.byref(desc), ctypes.byref(w), one, 4, ctypes.byref(api.UnionC()), one, one,
+             None) == api.MOE_EINVAL
+    assert "union" in msg()
