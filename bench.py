@@ -1,13 +1,21 @@
 """Benchmark: verify-pass tokens/s and expert-weight HBM GB/s, dedup vs
-per-slot, on the DeepSeek-V2-Lite-shaped MoE layer (d=2048, 64 routed experts
-top-6 + 2 shared, SwiGLU I=1408, bf16 weights, fp32 accumulate).
+per-slot, on the DeepSeek-V2-Lite-shaped 26-layer MoE stack (expert layers
+only: d=2048, 64 routed experts top-6 + 2 shared, SwiGLU I=1408, bf16 weights,
+fp32 accumulate; 29.7 GB of expert weights).
 
 One step = one verification pass at every pass size n = 1..9 (AR(1) hidden
-states, rho = 0.9) through each engine (per-slot and dedup): 18 passes of
-route → union → experts → combine, 90 tokens. The layer's weights exist in
-several independently seeded replicas and consecutive passes use different
-replicas, so every pass reads its expert weights cold from HBM (inputs larger
-than L2). The step is captured once in a CUDA graph and replayed.
+states, rho = 0.9) through all 26 layers, once with each engine (per-slot and
+dedup): 18 stack passes, 468 layer passes, 90 tokens. Every layer is fed the
+same pass (attention and residuals are outside the path). Each layer's
+weights (1.14 GB) are far larger than L2 and consecutive layers read different
+weights, so every layer reads its expert weights cold from HBM. The step is
+captured once in a CUDA graph and replayed.
+
+Besides the headline the line carries the per-call breakdown of the layers'
+passes (the step-time model's inputs), the stack check (the model fitted on
+one layer run alone against the measured stack, at four hidden-state
+correlations), and per-pass-size tables of the Mixtral- and DeepSeek-V3-shaped
+layers.
 
 Prints one JSON line (rank 0). ``--impl reference`` times the float64 CPU
 oracle on the same workload instead (a bounded sample per step).
@@ -33,10 +41,12 @@ if ROOT not in sys.path:
 
 METRIC = "verify-pass tokens/s and expert-weight HBM GB/s vs 8 TB/s, dedup vs per-slot"
 UNIT = "tokens/s"
-WORKLOAD = "deepseek-v2-lite-shaped MoE layer: d=2048, 64 routed experts top-6 + 2 shared, " \
-           "SwiGLU I=1408, bf16 weights / fp32 accumulate; verify passes n=1..9 at rho=0.9 " \
-           "through the per-slot and the dedup engine"
-REPLICAS = 4
+LAYERS = 26
+WORKLOAD = ("deepseek-v2-lite-shaped 26-layer MoE stack (expert layers only, each fed the same "
+            "pass): d=2048, 64 routed experts top-6 + 2 shared, SwiGLU I=1408, bf16 weights / "
+            "fp32 accumulate, 29.7 GB of expert weights; verify passes n=1..9 at rho=0.9 through "
+            "all 26 layers with the per-slot and the dedup engine")
+HEADLINE_RHO = 0.9
 N_PASSES_PER_N = 2        # distinct hidden-state passes per n, alternated across steps
 EXPERT_BYTES = 3 * 2048 * 1408 * 2
 BREAKDOWN_PASSES = 8      # passes per (pass size, engine) in the per-call breakdown
@@ -52,6 +62,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the stack check and the other workloads' tables (profiling runs)")
     p.add_argument("--case", default=None,
                    help="profiling case WORKLOAD:ENGINE:N (e.g. v2lite:perslot:1): runs "
                         "--passes passes of one layer and prints their mean time")
@@ -60,9 +72,17 @@ def parse_args():
                    help="one layer of WORKLOAD at every pass size and rho of that workload, "
                         "both engines: requested bytes, time and bandwidth per n, r(n), the "
                         "byte share and the crossover")
+    p.add_argument("--rho", type=float, default=None, help="--sweep: this rho only")
     p.add_argument("--stack", action="store_true",
-                   help="26-layer V2-Lite stack: fit the step-time model on one layer run "
+                   help="only the stack check: fit the step-time model on one layer run "
                         "alone, predict the stack's passes and compare with measured ones")
+    p.add_argument("--calls", default=None, choices=["v2lite", "mixtral", "v3"],
+                   help="for an ncu DRAM capture: one layer of WORKLOAD at rho = 0.9, one "
+                        "per-slot and one dedup pass at each pass size; prints each expert "
+                        "call's requested bytes in launch order")
+    p.add_argument("--dram-record", nargs=2, metavar=("CALLS_JSON", "NCU_CSV"), default=None,
+                   help="write profiles/dram_expert_calls_<workload>.txt from a --calls "
+                        "output and the ncu csv of the same command")
     return p.parse_args()
 
 
@@ -146,37 +166,35 @@ def job_value(world: int, tokens_per_step: int, ms_step: float) -> float:
     return world * tokens_per_step / (ms_step * 1e-3)
 
 
-# -------------------------------------------------------------- our engine --
-def build_workload(dev):
+# ------------------------------------------------------------- our engine --
+def build_stack(dev):
+    """The 26 layers (seed 1000 + layer), one PassRunner each, and the
+    headline's hidden-state passes: N_PASSES_PER_N per pass size at rho 0.9."""
     import torch
     from moe_expert_layer_warp_gb300 import configs, synth
     from moe_expert_layer_warp_gb300.layer import PassRunner
-    w = configs.V2_LITE
-    reps = [synth.make_layer(w.shape, w.weight_seed + 7919 * r, dev) for r in range(REPLICAS)]
-    runners = [PassRunner(L, max(w.pass_sizes)) for L in reps]
+    w = configs.V2_LITE_STACK
+    assert w.layers == LAYERS and HEADLINE_RHO in w.rhos
+    layers = [synth.make_layer(w.shape, w.weight_seed + l, dev) for l in range(w.layers)]
+    runners = [PassRunner(L, max(w.pass_sizes)) for L in layers]
     xs = {}
     for n in w.pass_sizes:
-        xs[n] = [torch.from_numpy(synth.make_pass(w.shape.d, n, w.rhos[0],
+        xs[n] = [torch.from_numpy(synth.make_pass(w.shape.d, n, HEADLINE_RHO,
                                                   [w.x_seed_base + 1000 * q + n]))
                  .to(dev) for q in range(N_PASSES_PER_N)]
     return w, runners, xs
 
 
 def step_plan(w, step_idx):
-    """(replica, n, engine, x variant) for the 18 passes of a step; consecutive
-    passes always use different replicas."""
-    plan = []
-    i = 0
-    for n in w.pass_sizes:
-        for eng in ("perslot", "dedup"):
-            plan.append(((step_idx + i) % REPLICAS, n, eng, step_idx % N_PASSES_PER_N))
-            i += 1
-    return plan
+    """(n, engine, x variant) of the 18 stack passes of a step."""
+    return [(n, eng, step_idx % N_PASSES_PER_N) for n in w.pass_sizes
+            for eng in ("perslot", "dedup")]
 
 
 def enqueue_step(w, runners, xs, step_idx, stream):
-    for rep, n, eng, q in step_plan(w, step_idx):
-        runners[rep].forward(xs[n][q], eng, stream)
+    for n, eng, q in step_plan(w, step_idx):
+        for R in runners:
+            R.forward(xs[n][q], eng, stream)
 
 
 def kernels_per_pass():
@@ -224,89 +242,92 @@ def time_graphs(graphs, rounds):
     return [statistics.median(t) for t in ts]
 
 
+def requested(R, eng):
+    """Requested expert-weight bytes of the runner's last pass with `eng`:
+    per-slot n·k·E_b or dedup |U|·E_b, plus the shared experts' s·E_b."""
+    b = [int(v) for v in R.bytes.cpu().tolist()]
+    return (b[0] if eng == "perslot" else b[1]) + b[2]
+
+
 def measure_breakdown(w, runners, xs):
     """The expert call's time inside a pipelined pass, per pass size and
-    engine. Each of BREAKDOWN_PASSES passes (consecutive passes on different
-    weight replicas) is captured twice as a CUDA graph: route, union, expert
-    call, combine — and the same without the expert call. The graphs are
-    replayed round-robin between CUDA events on the stream; the expert call's
-    time is the difference of a pass's two medians, the fixed time the
-    second median. Returns samples for the step-time model and the roofline
-    numbers."""
+    engine, on the stack's layers. Each of BREAKDOWN_PASSES passes (pass i on
+    layer i, so consecutive passes read different weights) is captured twice
+    as a CUDA graph: route, union, expert call, combine — and the same
+    without the expert call. The graphs are replayed round-robin between
+    CUDA events on the stream; the expert call's time is the difference of a
+    pass's two medians, the fixed time the second median. Returns samples
+    for the step-time model, per-pass times and the calls' requested bytes."""
     samples = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     tfix = {n: [] for n in w.pass_sizes}
     pass_ms = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
-    alg_bytes, eng_s, launches = 0.0, 0.0, 0
     import torch
     stream = torch.cuda.current_stream()
     for n in w.pass_sizes:
         for eng in ("perslot", "dedup"):
-            plan = [(i % REPLICAS, i % N_PASSES_PER_N) for i in range(BREAKDOWN_PASSES)]
+            plan = [(i % len(runners), i % N_PASSES_PER_N) for i in range(BREAKDOWN_PASSES)]
             reqs = []
-            for rep, q in plan:          # requested bytes of each pass (routing is deterministic)
-                R = runners[rep]
+            for li, q in plan:          # requested bytes of each pass (routing is deterministic)
+                R = runners[li]
                 R.forward(xs[n][q], eng, stream)
-                b = [int(v) for v in R.bytes.cpu().tolist()]
-                reqs.append((b[0] if eng == "perslot" else b[1]) + b[2])
+                reqs.append(requested(R, eng))
 
-            def one(s, rep, q, with_expert):
-                R, x = runners[rep], xs[n][q]
+            def one(s, li, q, with_expert):
+                R, x = runners[li], xs[n][q]
                 R.route_union(x, s)
                 if with_expert:
                     R.experts(x, eng, s)
                 R.combine(n, s)
-            ga = [capture_graph(lambda s, r=r, q=q: one(s, r, q, True)) for r, q in plan]
-            gb = [capture_graph(lambda s, r=r, q=q: one(s, r, q, False)) for r, q in plan]
+            ga = [capture_graph(lambda s, li=li, q=q: one(s, li, q, True)) for li, q in plan]
+            gb = [capture_graph(lambda s, li=li, q=q: one(s, li, q, False)) for li, q in plan]
             t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
             ta, tb = t[:len(plan)], t[len(plan):]
-            sh = runners[0].shape
-            act = n * sh.d * 4 + n * (sh.top_k + sh.n_shared) * sh.d * 4
             for i in range(len(plan)):
-                t_exp = max(ta[i] - tb[i], 1e-9)
-                samples[eng][n].append((reqs[i], t_exp))
+                samples[eng][n].append((reqs[i], max(ta[i] - tb[i], 1e-9)))
                 tfix[n].append(tb[i])
                 pass_ms[eng][n].append(ta[i] * 1e3)
-                alg_bytes += reqs[i] + act
-                eng_s += t_exp
-                launches += 1
             del ga, gb
     t_fix = {n: statistics.median(v) for n, v in tfix.items()}
-    return samples, t_fix, pass_ms, alg_bytes / launches, eng_s * 1e3 / launches
+    return samples, t_fix, pass_ms
 
 
 def e2e_measure(w, runners, xs, steps, warmup):
     """End to end through the public API with host buffers, as a serving loop
     runs it: each step uploads all its passes' hidden states from pinned host
-    memory in one copy, runs the passes (PassRunner.forward writing each y
-    into the step's output block) and reads the block back to pinned host
+    memory in one copy, runs every stack pass (PassRunner.forward — one
+    moe_verify_pass call — per layer, each writing its y into the step's
+    [layer][row] output block) and reads the whole block back to pinned host
     memory in one copy. One CUDA graph per step variant holds the upload, the
-    passes and the read-back; every step replays one, so every copy runs every
-    step inside the timed region."""
+    passes and the read-back; every step replays one, so every copy runs
+    every step inside the timed region."""
     import torch
     stream = torch.cuda.current_stream()
     dev = xs[w.pass_sizes[0]][0].device
     d = w.shape.d
-    n_variants = REPLICAS * N_PASSES_PER_N // math.gcd(REPLICAS, N_PASSES_PER_N)
+    n_variants = N_PASSES_PER_N
     plans = [step_plan(w, v) for v in range(n_variants)]
-    rows = sum(n for _, n, _, _ in plans[0])
+    rows = sum(n for n, _, _ in plans[0])
+    L = len(runners)
     hx = []
     for v in range(n_variants):
         blk = torch.empty((rows, d), dtype=torch.float32).pin_memory()
         r = 0
-        for _, n, _, q in plans[v]:
+        for n, _, q in plans[v]:
             blk[r:r + n].copy_(xs[n][q].cpu())
             r += n
         hx.append(blk)
-    hy = [torch.empty((rows, d), dtype=torch.float32).pin_memory() for _ in range(n_variants)]
+    hy = [torch.empty((L, rows, d), dtype=torch.float32).pin_memory() for _ in range(n_variants)]
     dx = torch.empty((rows, d), dtype=torch.float32, device=dev)
-    dy = torch.empty((rows, d), dtype=torch.float32, device=dev)
-    h2d = d2h = rows * d * 4
+    dy = torch.empty((L, rows, d), dtype=torch.float32, device=dev)
+    h2d = rows * d * 4
+    d2h = L * rows * d * 4
 
     def capture_step(v, cap):
         dx.copy_(hx[v], non_blocking=True)
         r = 0
-        for rep, n, eng, q in plans[v]:
-            runners[rep].forward(dx[r:r + n], eng, cap, out=dy[r:r + n])
+        for n, eng, q in plans[v]:
+            for li, R in enumerate(runners):
+                R.forward(dx[r:r + n], eng, cap, out=dy[li, r:r + n])
             r += n
         hy[v].copy_(dy, non_blocking=True)
 
@@ -335,50 +356,49 @@ def e2e_measure(w, runners, xs, steps, warmup):
 
 def e2e_measure_eager(w, runners, xs, steps, warmup):
     """End to end through the public API called pass by pass from Python, with
-    host buffers: every pass copies its hidden states from pinned host memory
-    and reads y back to pinned host memory, inside the timed region. The
-    copies run on a copy stream, ordered against the compute stream by events,
-    so that a pass's upload overlaps the previous pass and its read-back
-    overlaps the next (double-buffered device and host buffers). Returns the
-    device time per step and the host's issue time per step."""
+    host buffers: every stack pass copies its hidden states from pinned host
+    memory, runs the 26 layers (one moe_verify_pass call each) and reads the
+    26 layers' y back to pinned host memory, inside the timed region. The
+    copies run on a copy stream ordered against the compute stream by events,
+    so a pass's upload overlaps the previous pass and its read-back the next
+    (double-buffered device and host buffers). Returns the device time per
+    step and the host's issue time per step."""
     import torch
     stream = torch.cuda.current_stream()
     copy = torch.cuda.Stream()
     dev = xs[w.pass_sizes[0]][0].device
+    d, L = w.shape.d, len(runners)
     hx = {n: [x.cpu().pin_memory() for x in xs[n]] for n in xs}
-    hy = {n: [torch.empty((n, w.shape.d), dtype=torch.float32).pin_memory() for _ in range(2)]
+    hy = {n: [torch.empty((L, n, d), dtype=torch.float32).pin_memory() for _ in range(2)]
           for n in xs}
-    dx = {n: [torch.empty((n, w.shape.d), dtype=torch.float32, device=dev) for _ in range(2)]
+    dx = {n: [torch.empty((n, d), dtype=torch.float32, device=dev) for _ in range(2)] for n in xs}
+    dy = {n: [torch.empty((L, n, d), dtype=torch.float32, device=dev) for _ in range(2)]
           for n in xs}
-    h2d = d2h = 0
-    for n in w.pass_sizes:
-        h2d += 2 * n * w.shape.d * 4
-        d2h += 2 * n * w.shape.d * 4
-    state = {"i": 0, "done": [None, None], "read": {}}
+    h2d = sum(2 * n * d * 4 for n in w.pass_sizes)
+    d2h = sum(2 * L * n * d * 4 for n in w.pass_sizes)
+    state = {"i": 0, "done": [None, None]}
 
     def one(step_idx):
-        for rep, n, eng, q in step_plan(w, step_idx):
+        for n, eng, q in step_plan(w, step_idx):
             b = state["i"] & 1
             state["i"] += 1
             with torch.cuda.stream(copy):
                 if state["done"][b] is not None:
-                    copy.wait_event(state["done"][b])   # buffer b's previous pass is done
+                    copy.wait_event(state["done"][b])   # buffer b's previous pass is read back
                 dx[n][b].copy_(hx[n][q], non_blocking=True)
                 up = torch.cuda.Event()
                 up.record(copy)
             stream.wait_event(up)
-            if rep in state["read"]:
-                stream.wait_event(state["read"][rep])   # this runner's last y has been read
-            y = runners[rep].forward(dx[n][b], eng, stream)
+            for li, R in enumerate(runners):
+                R.forward(dx[n][b], eng, stream, out=dy[n][b][li])
             fin = torch.cuda.Event()
             fin.record(stream)
             with torch.cuda.stream(copy):
                 copy.wait_event(fin)
-                hy[n][b].copy_(y, non_blocking=True)
+                hy[n][b].copy_(dy[n][b], non_blocking=True)
                 rd = torch.cuda.Event()
                 rd.record(copy)
             state["done"][b] = rd
-            state["read"][rep] = rd
 
     for i in range(warmup):
         one(i)
@@ -398,8 +418,9 @@ def e2e_measure_eager(w, runners, xs, steps, warmup):
     return ms, h2d, d2h, host_ms
 
 
+# -------------------------------------------------- committed DRAM records --
 TRAFFIC_SOURCES = ("expert_stream.cu", "expert_mma.cu", "engine.cu", "plan.cuh", "common.cuh",
-                   "launch.h", "tcgen05.cuh", "tmap.h", "api.cu")
+                   "launch.h", "tcgen05.cuh", "tmap.h", "api.cu", "route_union.cu")
 
 
 def _code_only(text: str) -> str:
@@ -412,8 +433,8 @@ def _code_only(text: str) -> str:
 
 def kernel_source_hash() -> str:
     """sha256 (first 16 hex digits) over the code of the expert call's
-    sources (comments excluded): the prep kernel, both expert kernels and
-    the choice between them."""
+    sources (comments excluded): every kernel of a pass and the choice
+    between the expert kernels."""
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES:
         path = os.path.join(ROOT, "moe_expert_layer_warp_gb300", "csrc", f)
@@ -421,13 +442,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-TRAFFIC_FILE = "traffic_expert_call_v2lite_bench.txt"
+def dram_record_path(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", "dram_expert_calls_%s.txt" % workload)
 
 
-def load_traffic_record(name: str):
-    """The ``key: value`` lines of a committed ncu summary, if its counters
-    were taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", name)
+def load_dram_record(workload: str, check_hash: bool = True):
+    """The ``key: value`` lines of a committed ncu DRAM record (one expert
+    call per pass size and engine), if its counters were taken on the
+    current kernel sources; else None. Values are int lists."""
+    path = dram_record_path(workload)
     if not os.path.exists(path):
         return None
     rec = {}
@@ -435,29 +458,27 @@ def load_traffic_record(name: str):
         if ":" in line and not line.startswith((" ", "#")):
             k, v = line.split(":", 1)
             rec[k.strip()] = v.strip()
-    if rec.get("sources_sha256_16") != kernel_source_hash():
+    if check_hash and rec.get("sources_sha256_16") != kernel_source_hash():
         return None
-    return rec
-
-
-def load_traffic(name: str):
-    """DRAM bytes per expert call from a committed ncu summary, or None."""
-    rec = load_traffic_record(name)
+    out = {"rho": float(rec.get("rho", "nan")), "sources_sha256_16": rec.get("sources_sha256_16")}
     try:
-        return int(rec["dram_bytes_per_launch"]) if rec else None
+        for key in ("n", "perslot_requested", "perslot_dram", "dedup_requested", "dedup_dram"):
+            out[key] = [int(t) for t in rec[key].split(",")]
     except (KeyError, ValueError):
         return None
-
-
-def load_perslot_dram(name: str, n_sizes: int):
-    """DRAM bytes read by one per-slot expert call at each pass size (the
-    same ncu capture), or None."""
-    rec = load_traffic_record(name)
-    try:
-        v = [int(t) for t in rec["perslot_dram_bytes_by_n"].split(",")] if rec else None
-    except (KeyError, ValueError):
+    if not all(len(out[k]) == len(out["n"]) for k in out if isinstance(out[k], list)):
         return None
-    return v if v and len(v) == n_sizes else None
+    return out
+
+
+def dram_ratio(workload: str, rho: float):
+    """DRAM bytes over requested bytes per (engine, n) from the record, when
+    it was taken at this rho on the current sources; else None."""
+    rec = load_dram_record(workload)
+    if rec is None or abs(rec["rho"] - rho) > 1e-9:
+        return None
+    return {e: {n: rec[e + "_dram"][i] / rec[e + "_requested"][i] for i, n in enumerate(rec["n"])}
+            for e in ("perslot", "dedup")}
 
 
 def peaks():
@@ -496,14 +517,16 @@ def _oracle_token(task):
 
 
 class OracleHost:
-    """The float64 oracle, as it stands, on the bench workload's layer: one
-    thread in this process, or one spawned worker process per host core
-    (spawn, never fork: this process may hold a CUDA context)."""
+    """The float64 oracle, as it stands, on one layer of the stack (layer 0;
+    every layer has the same shape, so the oracle's cost per token and layer
+    is the same for all 26): one thread in this process, or one spawned worker
+    process per host core (spawn, never fork: this process may hold a CUDA
+    context). Stack tokens/s = token-layers/s ÷ 26."""
 
     def __init__(self):
         import tempfile
         from moe_expert_layer_warp_gb300 import configs, synth
-        w = configs.V2_LITE
+        w = configs.V2_LITE_STACK
         self.w = w
         L = synth.make_layer(w.shape, w.weight_seed, "cpu")
         self.H = {k: synth.weights_numpy(getattr(L, a)) for k, a in
@@ -511,7 +534,7 @@ class OracleHost:
                    ("su", "ws_up"), ("sd", "ws_down"))}
         self.H["wr"] = L.w_router.numpy()
         del L
-        self.passes = {n: synth.make_pass(w.shape.d, n, w.rhos[0], [w.x_seed_base + n])
+        self.passes = {n: synth.make_pass(w.shape.d, n, HEADLINE_RHO, [w.x_seed_base + n])
                        for n in w.pass_sizes}
         self.order = [(n, t) for n in w.pass_sizes for t in range(n)]
         self.tmp = tempfile.mkdtemp(prefix="moe_oracle_")
@@ -556,199 +579,33 @@ class OracleHost:
 
 def cpu_baseline_sample(budget_s=10.0):
     """The oracle as it stands on this host's cores, on a bounded sample of
-    the workload: every token of one pass at each n = 1..9 (45 tokens),
-    first on one thread, then repeated over one worker per core until about
-    budget_s. Returns the cpu_baseline dict."""
+    the workload: every token of one pass at each n = 1..9 (45 tokens)
+    through layer 0 of the stack, first on one thread, then repeated over one
+    worker per core until about budget_s; stack tokens/s = token-layers/s ÷
+    26. Returns the cpu_baseline dict."""
     host = OracleHost()
     try:
         t1 = host.single(host.order)
-        one = len(host.order) / t1
+        one = len(host.order) / t1 / LAYERS
         host.start_pool()
         t = host.parallel(host.order)
         reps = max(1, int(budget_s / max(t, 1e-3)))
         tasks = host.order * reps
         tp = host.parallel(tasks)
-        many = len(tasks) / tp
+        many = len(tasks) / tp / LAYERS
     finally:
         host.close()
-    return {"value": round(many, 3), "unit": UNIT, "cores": host.procs, "kind": "oracle",
+    return {"value": round(many, 4), "unit": UNIT, "cores": host.procs, "kind": "oracle",
             "sample": "float64 oracle (routing of each pass, layer output per token) on %d worker "
-                      "processes, one per host core: every token of one pass at each n = 1..9 of "
-                      "the same layer, %d times (%d tokens, %.1f s)" % (
+                      "processes, one per host core: every token of one pass at each n = 1..9 "
+                      "through layer 0 of the stack, %d times (%d token-layers, %.1f s); stack "
+                      "tokens/s = token-layers/s / 26 (every layer has the same shape)" % (
                           host.procs, reps, len(tasks), tp),
-            "single_thread": {"value": round(one, 3), "cores": 1,
-                              "sample": "the same 45 tokens on one thread (%.1f s)" % t1}}
+            "single_thread": {"value": round(one, 4), "cores": 1,
+                              "sample": "the same 45 token-layers on one thread (%.1f s)" % t1}}
 
 
-def run_ours(args):
-    import torch
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from __graft_entry__ import build
-    build()
-    from moe_expert_layer_warp_gb300 import api, stepmodel
-
-    w, runners, xs = build_workload(dev)
-    stream = torch.cuda.current_stream()
-    tokens_per_step = 2 * sum(w.pass_sizes)
-
-    # warm-up (also configures the kernels before graph capture)
-    for i in range(max(3, args.warmup)):
-        enqueue_step(w, runners, xs, i, stream)
-    torch.cuda.synchronize()
-    st = api.moe_last_device_error()
-    if st != api.MOE_OK:
-        raise RuntimeError("device error during warm-up: %s" % api.status_str(st))
-
-    # one graph per step variant (replica rotation and x variant depend on the step index)
-    n_variants = REPLICAS * N_PASSES_PER_N // math.gcd(REPLICAS, N_PASSES_PER_N)
-    graphs = []
-    cap_stream = torch.cuda.Stream()
-    cap_stream.wait_stream(stream)
-    with torch.cuda.stream(cap_stream):
-        for v in range(n_variants):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cap_stream):
-                enqueue_step(w, runners, xs, v, cap_stream)
-            graphs.append(g)
-    stream.wait_stream(cap_stream)
-    torch.cuda.synchronize()
-    for v in range(n_variants):
-        graphs[v].replay()
-    torch.cuda.synchronize()
-
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        graphs[i % n_variants].replay()
-    e1.record(stream)
-    e1.synchronize()
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-    value = job_value(world, tokens_per_step, ms_step)
-
-    st = api.moe_last_device_error()
-    if st != api.MOE_OK:
-        raise RuntimeError("device error in the timed region: %s" % api.status_str(st))
-
-    # breakdown for the step-time model and the engine roofline (outside the timed region)
-    samples, t_fix, pass_ms, alg_b, eng_ms = measure_breakdown(w, runners, xs)
-    rep = stepmodel.build_report(samples, t_fix)
-    e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
-    e2e_ms = max_over_ranks(e2e_ms, dev)
-    eager_ms, _, _, eager_host_ms = e2e_measure_eager(w, runners, xs, max(3, args.steps // 2), 3)
-    eager_ms = max_over_ranks(eager_ms, dev)
-
-    if rank != 0:
-        return
-    peak, peak_kind = peaks()
-    achieved = alg_b / (eng_ms * 1e-3) / 1e9
-    per_engine = {}
-    for eng in ("perslot", "dedup"):
-        per_engine[eng] = {
-            "tokens_per_s": [round(n / (statistics.median(pass_ms[eng][n]) * 1e-3), 1)
-                             for n in w.pass_sizes],
-            "pass_us": [round(statistics.median(pass_ms[eng][n]) * 1e3, 2) for n in w.pass_sizes],
-            "expert_GBs": [round(sum(b for b, _ in samples[eng][n]) /
-                                 sum(s for _, s in samples[eng][n]) / 1e9, 1)
-                           for n in w.pass_sizes],
-        }
-        per_engine[eng]["expert_frac_of_peak"] = [round(g / peak, 3)
-                                                  for g in per_engine[eng]["expert_GBs"]]
-    # The per-slot engine's DRAM bandwidth beside its requested-byte bandwidth:
-    # ncu DRAM reads of one call at each n (committed capture of this workload
-    # on these sources; every launch cold) over the call's measured time.
-    ps_dram = load_perslot_dram(TRAFFIC_FILE, len(w.pass_sizes))
-    if ps_dram:
-        t_call = [sum(s for _, s in samples["perslot"][n]) / len(samples["perslot"][n])
-                  for n in w.pass_sizes]
-        gbs = [round(b / t / 1e9, 1) for b, t in zip(ps_dram, t_call)]
-        per_engine["perslot"]["dram_GBs"] = gbs
-        per_engine["perslot"]["dram_frac_of_peak"] = [round(g / peak, 3) for g in gbs]
-    else:
-        per_engine["perslot"]["dram_GBs"] = None
-    cpu = None if args.no_cpu_baseline else cpu_baseline_sample()
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1/sqrt(fan_in)) weights, AR(1) hidden states)",
-        "config": {"workload": WORKLOAD, "tokens_per_step": tokens_per_step,
-                   "passes_per_step": 2 * len(w.pass_sizes), "pass_sizes": list(w.pass_sizes),
-                   "rho": w.rhos[0], "weight_replicas": REPLICAS,
-                   "l2": "inputs larger than L2: %d weight replicas of 1.14 GB rotated so "
-                         "consecutive passes read different replicas" % REPLICAS,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "timing": "CUDA-graph replay of each step, CUDA events on the stream"},
-        "roofline": {"kernel": "expert call: prep kernel + expert_mma_kernel (tensor cores) or "
-                               "expert_engine_kernel (CUDA cores), chosen per call; up/gate and "
-                               "down of every group",
-                     "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": load_traffic(TRAFFIC_FILE)},
-        "cpu_baseline": cpu,
-        "e2e": {"value": round(job_value(world, tokens_per_step, e2e_ms), 1), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * 2 * len(w.pass_sizes) * kernels_per_pass(),
-        "e2e_eager": {"value": round(job_value(world, tokens_per_step, eager_ms), 1),
-                      "unit": UNIT, "host_issue_ms_per_step": round(eager_host_ms, 4),
-                      "note": "the same passes and copies issued call by call from Python"},
-        "clocks": clk,
-        "engines": per_engine,
-        "stepmodel": rep.as_dict(),
-    }
-    print(json.dumps(line), flush=True)
-
-
-def run_reference(args):
-    """The reference arm: the float64 oracle, as it stands, on this host's
-    cores (one spawned worker per core), each step a bounded sample of the
-    workload's tokens. Rank 0 alone runs it."""
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return
-    host = OracleHost()
-    try:
-        host.start_pool()
-        t = host.parallel(host.order)                      # 45 tokens
-        budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-        per_step = max(1, min(2 * len(host.order), int(budget / max(t, 1e-3) * len(host.order))))
-        order = (host.order * 2)[:per_step]
-        for _ in range(args.warmup):
-            host.parallel(order)
-        el = sum(host.parallel(order) for _ in range(args.steps)) / args.steps
-    finally:
-        host.close()
-    v = per_step / el
-    desc = ("float64 oracle on the host (%d worker processes, one per core): per step, the "
-            "layer output of %d tokens taken from the n=1..9 passes of the workload, with each "
-            "pass's routing" % (host.procs, per_step))
-    print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens_per_step": per_step},
-        "cpu_baseline": {"kind": "oracle", "cores": host.procs, "sample": desc,
-                         "value": round(v, 4), "unit": UNIT},
-        "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }), flush=True)
-
-
+# ------------------------------------------------------------ stack check --
 STACK_DRAFT_COST_RATIO = 0.1601   # draft/verify cost ratio c the pages derive from FLOPs
 STACK_FIT_PASSES = 4   # held-out passes (own seeds) per (rho, n) for the bandwidth fit
 STACK_DEPTHS = (1, 4, 13, 26)     # partial stacks whose crossover is predicted and measured
@@ -756,25 +613,18 @@ STACK_AUTOCORR = 0.155   # within-stream acceptance autocorrelation p11 - p10 (p
 STACK_REPS = 3
 
 
-def run_stack(args):
-    """26 V2-Lite-shaped layers (~30 GB), each fed the same pass, at n = 1..9
-    and rho in {0, 0.5, 0.9, 0.99}. Per rho, the bandwidths are fitted on
-    layer 0's expert call run alone over STACK_FIT_PASSES held-out passes
-    (own seeds) at that rho, each pass a CUDA graph behind an L2 flush (a
-    256 MB read) timed with and without its expert call; each stack pass
-    is predicted from every layer's requested bytes over those bandwidths
-    plus the fixed time, and compared with the measured stack pass. Prints
-    one JSON line."""
+def stack_check(w, runners, dev):
+    """Per rho in {0, 0.5, 0.9, 0.99}: the bandwidths fitted on layer 0's
+    expert call run alone over STACK_FIT_PASSES held-out passes (own seeds),
+    each pass a CUDA graph behind an L2 flush (a 256 MB read) timed with and
+    without its expert call; each stack pass (and its first 1, 4 and 13
+    layers) predicted from every layer's requested bytes over those
+    bandwidths plus the fixed time, and compared with the measured stack
+    pass: the saving against its bound, the crossover per depth and the best
+    draft length, under i.i.d. and autocorrelated acceptance. Returns the
+    report dict."""
     import torch
-    from __graft_entry__ import build
-    build()
-    from moe_expert_layer_warp_gb300 import api, configs, stepmodel, synth
-    from moe_expert_layer_warp_gb300.layer import PassRunner
-    w = configs.V2_LITE_STACK
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    layers = [synth.make_layer(w.shape, w.weight_seed + l, dev) for l in range(w.layers)]
-    runners = [PassRunner(L, max(w.pass_sizes)) for L in layers]
+    from moe_expert_layer_warp_gb300 import api, stepmodel, synth
     stream = torch.cuda.current_stream()
     # read (not written) to flush L2: the flush leaves clean lines behind, as
     # the previous layer's weights do inside a stack pass
@@ -789,10 +639,6 @@ def run_stack(args):
     fit_xs = {(ri, n): [make_x(ri, rho, n, 1 + f) for f in range(STACK_FIT_PASSES)]
               for ri, rho in enumerate(w.rhos) for n in w.pass_sizes}
 
-    def req_bytes(R, eng):
-        b = [int(v) for v in R.bytes.cpu().tolist()]
-        return (b[0] if eng == "perslot" else b[1]) + b[2]
-
     for (ri, n), x in xs.items():          # warm-up: every pass once through the stack,
         for eng in engines:                # every fitted pass once through layer 0
             for R in runners:
@@ -801,15 +647,12 @@ def run_stack(args):
                 runners[0].forward(xf, eng, stream)
     torch.cuda.synchronize()
     if api.moe_last_device_error() != api.MOE_OK:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError("device error during the stack check's warm-up")
 
     R0 = runners[0]
     g_flush = capture_graph(lambda s: flush.sum())
     per_rho, fits_out = [], []
     for ri, rho in enumerate(w.rhos):
-        # fit on layer 0 run alone, held-out passes at this rho: each pass as a
-        # CUDA graph behind an L2 flush (a 256 MB read), with and without the
-        # expert call; the flush's own graph is subtracted from the fixed time
         samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
         tfix = {n: [] for n in w.pass_sizes}
         t_flush = time_graphs([g_flush], 2 * BREAKDOWN_ROUNDS)[0]
@@ -818,7 +661,7 @@ def run_stack(args):
                 reqs = []
                 for x in fit_xs[(ri, n)]:
                     R0.forward(x, eng, stream)
-                    reqs.append(req_bytes(R0, eng))
+                    reqs.append(requested(R0, eng))
 
                 def one(s, x, with_expert):
                     flush.sum()
@@ -847,8 +690,6 @@ def run_stack(args):
             "eps_perslot": [round(eps["perslot"][n], 4) for n in w.pass_sizes],
             "eps_dedup": [round(eps["dedup"][n], 4) for n in w.pass_sizes],
             "t_fix_us": [round(t_fix[n] * 1e6, 2) for n in w.pass_sizes]})
-        # the stack (and its first-L-layer partial stacks): measured passes
-        # and their per-layer requested bytes
         meas_d = {L: {e: {} for e in engines} for L in STACK_DEPTHS}
         pred_d = {L: {e: {} for e in engines} for L in STACK_DEPTHS}
         bound = {}
@@ -869,13 +710,13 @@ def run_stack(args):
                         torch.cuda.synchronize()
                         ts.append(e0.elapsed_time(e1) * 1e-3)
                     meas_d[L][eng][n] = statistics.median(ts)
-                lb[eng] = [req_bytes(R, eng) for R in runners]
+                lb[eng] = [requested(R, eng) for R in runners]
                 for L in STACK_DEPTHS:
                     pred_d[L][eng][n] = stepmodel.step_time(fits[eng], n, lb[eng][:L])
-            meas, pred = meas_d[w.layers], pred_d[w.layers]
             bound[n] = stepmodel.saving_bound(sum(lb["perslot"]), fits["perslot"].bw[n],
                                               eps["perslot"][n], sum(lb["dedup"]),
                                               fits["dedup"].bw[n], eps["dedup"][n])
+        meas, pred = meas_d[w.layers], pred_d[w.layers]
         chk = stepmodel.StackCheck(list(w.pass_sizes), meas, pred, bound,
                                    stepmodel.acceptance_grid(), STACK_DRAFT_COST_RATIO)
         d = chk.as_dict()
@@ -908,17 +749,345 @@ def run_stack(args):
         per_rho.append(d)
     if api.moe_last_device_error() != api.MOE_OK:
         raise RuntimeError("device error in the stack passes")
+    summary = {
+        "saving_inside_bound": "%d of %d" % (sum(d["saving_inside_bound"] for d in per_rho),
+                                             sum(d["points"] for d in per_rho)),
+        "crossover_predicted_equals_measured_by_depth": "%d of %d" % (
+            sum(c["measured"] == c["predicted"] for d in per_rho for c in d["crossover_by_depth"]),
+            sum(len(d["crossover_by_depth"]) for d in per_rho)),
+        "crossover_within_one_pass_size_by_depth": "%d of %d" % (
+            sum(_within_one(c["measured"], c["predicted"], max(w.pass_sizes))
+                for d in per_rho for c in d["crossover_by_depth"]),
+            sum(len(d["crossover_by_depth"]) for d in per_rho)),
+        "gamma_star_within_one": "%d of %d" % (sum(d["gamma_star_within_one"] for d in per_rho),
+                                               sum(len(d["gamma_star_measured"]) for d in per_rho)),
+    }
+    return {"stack": "deepseek-v2-lite-shaped 26-layer MoE stack (expert layers only, each fed "
+                     "the same pass), bf16 weights, %.1f GB of expert weights" % (
+                         w.layers * (w.shape.n_experts + w.shape.n_shared) * EXPERT_BYTES / 1e9),
+            "fit": {"layer": 0, "passes_per_point": STACK_FIT_PASSES,
+                    "l2": "flushed (256 MB read) before each fitted pass", "per_rho": fits_out},
+            "summary": summary, "per_rho": per_rho}
+
+
+def _within_one(a, b, n_max):
+    """Crossovers within one pass size; "never" (None) counts as n_max + 1."""
+    a = n_max + 1 if a is None else a
+    b = n_max + 1 if b is None else b
+    return abs(a - b) <= 1
+
+
+# ------------------------------------------------------ per-n layer tables --
+CASES = {"tiny": "TINY", "v2lite": "V2_LITE", "mixtral": "MIXTRAL", "v3": "V3"}
+SWEEP_PASSES = 2    # distinct hidden-state passes per (rho, n)
+
+
+def sweep_workload(name, rhos=None, passes=SWEEP_PASSES):
+    """One layer of a workload at each of its pass sizes and rhos through
+    both engines; each pass a CUDA graph behind an L2 flush (a 256 MB read),
+    timed with and without its expert call. Returns one dict per rho:
+    requested bytes, expert-call time and bandwidth per n and engine, the
+    DRAM bandwidth where a committed capture at that rho covers the current
+    kernels, the byte share u(n), the bandwidth ratio r(n) and the
+    crossover."""
+    import torch
+    from moe_expert_layer_warp_gb300 import api, configs, stepmodel, synth
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    w = getattr(configs, CASES[name])
+    sh = w.shape
+    L = synth.make_layer(sh, w.weight_seed, "cuda")
+    R = PassRunner(L, max(w.pass_sizes) * w.streams)
+    st = torch.cuda.current_stream()
+    flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
+    t_flush = time_graphs([capture_graph(lambda s: flush.sum())], 6)[0]
+    engines = ("perslot", "dedup")
+    peak = peaks()[0]
+    out = []
+    for rho in (rhos if rhos is not None else w.rhos):
+        samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
+        tfix = {n: [] for n in w.pass_sizes}
+        for n in w.pass_sizes:
+            for f in range(passes):
+                x = torch.from_numpy(synth.make_pass(sh.d, n, rho, [
+                    w.x_seed_base + 5000 + 97 * f + 13 * s for s in range(w.streams)])).cuda()
+                m = x.shape[0]
+                for eng in engines:
+                    R.forward(x, eng, st)
+                    req = requested(R, eng)
+
+                    def one(s, with_expert):
+                        flush.sum()
+                        R.route_union(x, s)
+                        if with_expert:
+                            R.experts(x, eng, s)
+                        R.combine(m, s)
+                    ga = capture_graph(lambda s: one(s, True))
+                    gb = capture_graph(lambda s: one(s, False))
+                    ta, tb = time_graphs([ga, gb], 3)
+                    samples[eng][n].append((req, max(ta - tb, 1e-9)))
+                    tfix[n].append(max(tb - t_flush, 0.0))
+                    del ga, gb
+        if api.moe_last_device_error() != api.MOE_OK:
+            raise RuntimeError("device error in the sweep")
+        ns = list(w.pass_sizes)
+        bw = {e: {n: stepmodel.effective_bandwidth([b for b, _ in samples[e][n]],
+                                                   [t for _, t in samples[e][n]]) for n in ns}
+              for e in engines}
+        u = {n: stepmodel.byte_share([b for b, _ in samples["dedup"][n]],
+                                     [b for b, _ in samples["perslot"][n]]) for n in ns}
+        r = {n: bw["dedup"][n] / bw["perslot"][n] for n in ns}
+        line = {"workload": w.name, "rho": rho, "streams": w.streams, "n": ns,
+                "passes_per_point": passes,
+                "timing": "expert call inside a CUDA-graph-replayed pass behind a 256 MB L2 "
+                          "flush (graph with minus graph without the call)",
+                "peak_GBs": peak}
+        ratio = dram_ratio(name, rho)
+        for eng in engines:
+            gbs = [bw[eng][n] / 1e9 for n in ns]
+            line[eng] = {
+                "requested_MB": [round(sum(b for b, _ in samples[eng][n]) / len(samples[eng][n])
+                                       / 1e6, 1) for n in ns],
+                "expert_us": [round(sum(t for _, t in samples[eng][n]) / len(samples[eng][n])
+                                    * 1e6, 2) for n in ns],
+                "GBs": [round(g, 1) for g in gbs],
+                "frac_of_peak": [round(g / peak, 3) for g in gbs],
+                "dram_GBs": ([round(g * ratio[eng][n * w.streams], 1)
+                              if n * w.streams in ratio[eng] else None
+                              for g, n in zip(gbs, ns)] if ratio else None)}
+            if ratio:
+                line[eng]["dram_frac_of_peak"] = [None if v is None else round(v / peak, 3)
+                                                  for v in line[eng]["dram_GBs"]]
+        line["dram_source"] = (os.path.relpath(dram_record_path(name), ROOT) + " (DRAM/requested "
+                               "bytes of one call per n at this rho, scaled by this run's requested "
+                               "bytes)") if ratio else "no capture at this rho on these sources"
+        line.update({"u_bar": [round(u[n], 6) for n in ns], "r": [round(r[n], 6) for n in ns],
+                     "crossover_n": stepmodel.crossover(ns, u, r),
+                     "t_fix_us": [round(statistics.median(tfix[n]) * 1e6, 2) for n in ns]})
+        out.append(line)
+    del R, L
+    torch.cuda.empty_cache()
+    return out
+
+
+# -------------------------------------------------------------- our arm --
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from __graft_entry__ import build
+    build()
+    from moe_expert_layer_warp_gb300 import api, stepmodel
+
+    w, runners, xs = build_stack(dev)
+    stream = torch.cuda.current_stream()
+    tokens_per_step = 2 * sum(w.pass_sizes)
+    passes_per_step = 2 * len(w.pass_sizes) * len(runners)
+
+    # warm-up (also configures the kernels before graph capture)
+    for i in range(max(3, args.warmup)):
+        enqueue_step(w, runners, xs, i, stream)
+    torch.cuda.synchronize()
+    st = api.moe_last_device_error()
+    if st != api.MOE_OK:
+        raise RuntimeError("device error during warm-up: %s" % api.status_str(st))
+
+    # one graph per step variant (the x variant depends on the step index)
+    graphs = []
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        for v in range(N_PASSES_PER_N):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap_stream):
+                enqueue_step(w, runners, xs, v, cap_stream)
+            graphs.append(g)
+    stream.wait_stream(cap_stream)
+    torch.cuda.synchronize()
+    for v in range(N_PASSES_PER_N):
+        graphs[v].replay()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        graphs[i % N_PASSES_PER_N].replay()
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms_step = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    value = job_value(world, tokens_per_step, ms_step)
+    del graphs
+
+    st = api.moe_last_device_error()
+    if st != api.MOE_OK:
+        raise RuntimeError("device error in the timed region: %s" % api.status_str(st))
+
+    # per-call breakdown on the stack's layers (outside the timed region)
+    samples, t_fix, pass_ms = measure_breakdown(w, runners, xs)
+    rep = stepmodel.build_report(samples, t_fix, layers=len(runners))
+    e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    eager_ms, _, _, eager_host_ms = e2e_measure_eager(w, runners, xs, max(3, args.steps // 4), 2)
+    eager_ms = max_over_ranks(eager_ms, dev)
+
+    stack = None
+    tables = None
+    if not args.no_extras and rank == 0:
+        stack = stack_check(w, runners, dev)
+    del runners, xs
+    torch.cuda.empty_cache()
+    if not args.no_extras and rank == 0:
+        tables = {"mixtral": sweep_workload("mixtral"), "v3": sweep_workload("v3")}
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    ns = list(w.pass_sizes)
+    sh = w.shape
+    ratio = dram_ratio("v2lite", HEADLINE_RHO)
+    per_engine = {}
+    req_b, dram_b, call_s, ncalls = 0.0, 0.0, 0.0, 0
+    for eng in ("perslot", "dedup"):
+        gbs = [sum(b for b, _ in samples[eng][n]) / sum(s for _, s in samples[eng][n]) / 1e9
+               for n in ns]
+        per_engine[eng] = {
+            "tokens_per_s_one_layer": [round(n / (statistics.median(pass_ms[eng][n]) * 1e-3), 1)
+                                       for n in ns],
+            "pass_us": [round(statistics.median(pass_ms[eng][n]) * 1e3, 2) for n in ns],
+            "expert_us": [round(sum(s for _, s in samples[eng][n]) / len(samples[eng][n]) * 1e6, 2)
+                          for n in ns],
+            "requested_MB": [round(sum(b for b, _ in samples[eng][n]) / len(samples[eng][n]) / 1e6,
+                                   1) for n in ns],
+            "expert_GBs": [round(g, 1) for g in gbs],
+            "expert_frac_of_peak": [round(g / peak, 3) for g in gbs],
+            "dram_GBs": [round(g * ratio[eng][n], 1) for g, n in zip(gbs, ns)] if ratio else None,
+        }
+        if ratio:
+            per_engine[eng]["dram_frac_of_peak"] = [round(v / peak, 3)
+                                                    for v in per_engine[eng]["dram_GBs"]]
+        for n in ns:
+            act = n * sh.d * 4 + n * (sh.top_k + sh.n_shared) * sh.d * 4
+            for b, s in samples[eng][n]:
+                req_b += b + act
+                dram_b += b * (ratio[eng][n] if ratio else float("nan")) + act
+                call_s += s
+                ncalls += 1
+    achieved = req_b / call_s / 1e9
+    achieved_dram = dram_b / call_s / 1e9 if ratio else None
+    cpu = None if args.no_cpu_baseline else cpu_baseline_sample()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1/sqrt(fan_in)) weights, AR(1) hidden states)",
+        "config": {"workload": WORKLOAD, "layers": LAYERS,
+                   "tokens_per_step": tokens_per_step, "stack_passes_per_step": 2 * len(ns),
+                   "layer_passes_per_step": passes_per_step, "pass_sizes": ns,
+                   "rho": HEADLINE_RHO,
+                   "l2": "inputs larger than L2: 26 layers of 1.14 GB, each layer pass reads "
+                         "another layer's weights than the one before it",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "timing": "CUDA-graph replay of each step, CUDA events on the stream"},
+        "roofline": {"kernel": "expert call: prep kernel + expert_mma_kernel (tensor cores) or "
+                               "expert_engine_kernel (CUDA cores), chosen per call; up/gate and "
+                               "down of every group",
+                     "bound": "hbm",
+                     "bytes": "requested: the call's expert-weight bytes as the method counts them "
+                              "(per-slot n*k*E_b + s*E_b, dedup |U|*E_b + s*E_b) plus its "
+                              "activations; per-slot requests of a repeated expert can be served "
+                              "by L2, so frac can exceed 1; frac_dram counts DRAM bytes instead",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "achieved_dram": None if achieved_dram is None else round(achieved_dram, 1),
+                     "frac_dram": None if achieved_dram is None else round(achieved_dram / peak, 4),
+                     "traffic": None if not ratio else int(round(dram_b / ncalls)),
+                     "traffic_source": (os.path.relpath(dram_record_path("v2lite"), ROOT)
+                                        if ratio else "no capture on these sources"),
+                     "calls": ncalls, "call_us_mean": round(call_s / ncalls * 1e6, 2)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(job_value(world, tokens_per_step, e2e_ms), 2), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "PassRunner.forward (moe_verify_pass) per layer, one pinned upload of "
+                        "the step's hidden states and one read-back of all 26 layers' outputs, "
+                        "captured per step variant in a CUDA graph"},
+        "gpu_launches": args.steps * passes_per_step * kernels_per_pass(),
+        "e2e_eager": {"value": round(job_value(world, tokens_per_step, eager_ms), 2),
+                      "unit": UNIT, "host_issue_ms_per_step": round(eager_host_ms, 4),
+                      "note": "the same passes and copies issued call by call from Python"},
+        "clocks": clk,
+        "layer_breakdown": {
+            "what": "one layer pass at a time on the stack's layers (8 passes per point, each on "
+                    "another layer), expert call = graph with minus graph without the call",
+            "engines": per_engine, "stepmodel": rep.as_dict()},
+        "stack_check": stack,
+        "tables": tables,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args):
+    """The reference arm: the float64 oracle, as it stands, on this host's
+    cores (one spawned worker per core), each step a bounded sample of the
+    workload: tokens of the n = 1..9 passes through layer 0 of the stack,
+    scaled to stack tokens (÷ 26). Rank 0 alone runs it."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    host = OracleHost()
+    try:
+        host.start_pool()
+        t = host.parallel(host.order)                      # 45 token-layers
+        budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+        per_step = max(1, min(2 * len(host.order), int(budget / max(t, 1e-3) * len(host.order))))
+        order = (host.order * 2)[:per_step]
+        for _ in range(args.warmup):
+            host.parallel(order)
+        el = sum(host.parallel(order) for _ in range(args.steps)) / args.steps
+    finally:
+        host.close()
+    v = per_step / LAYERS / el
+    desc = ("float64 oracle on the host (%d worker processes, one per core): per step, %d "
+            "token-layers (tokens of the n=1..9 passes through layer 0 of the stack, with each "
+            "pass's routing), counted as %d/26 stack tokens" % (host.procs, per_step, per_step))
     print(json.dumps({
-        "stack": "deepseek-v2-lite-shaped 26-layer MoE stack (expert layers only, each fed "
-                 "the same pass), bf16 weights, %.1f GB of expert weights" % (
-                     w.layers * (w.shape.n_experts + w.shape.n_shared) * EXPERT_BYTES / 1e9),
-        "fit": {"layer": 0, "passes_per_point": STACK_FIT_PASSES,
-                "l2": "flushed (256 MB read) before each fitted pass", "per_rho": fits_out},
-        "per_rho": per_rho,
+        "impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": round(per_step / LAYERS, 4)},
+        "cpu_baseline": {"kind": "oracle", "cores": host.procs, "sample": desc,
+                         "value": round(v, 5), "unit": UNIT},
+        "e2e": {"value": round(v, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
     }), flush=True)
 
 
-CASES = {"tiny": "TINY", "v2lite": "V2_LITE", "mixtral": "MIXTRAL", "v3": "V3"}
+def run_stack(args):
+    """The stack check alone (26 layers), one JSON line."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    from moe_expert_layer_warp_gb300 import configs, synth
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    w = configs.V2_LITE_STACK
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    layers = [synth.make_layer(w.shape, w.weight_seed + l, dev) for l in range(w.layers)]
+    runners = [PassRunner(L, max(w.pass_sizes)) for L in layers]
+    print(json.dumps(stack_check(w, runners, dev)), flush=True)
 
 
 def run_case(args):
@@ -966,8 +1135,7 @@ def run_case(args):
         ts.append(e[0].elapsed_time(e[1]))
     if api.moe_last_device_error() != api.MOE_OK:
         raise RuntimeError("device error")
-    b = [int(v) for v in R.bytes.cpu().tolist()]
-    req = (b[0] if eng == "perslot" else b[1]) + b[2]
+    req = requested(R, eng)
     ms = (ta - tb) * 1e3
     ms_ev = statistics.median(ts)
     print(json.dumps({"case": args.case, "tokens": x.shape[0], "engine_ms": round(ms, 4),
@@ -977,86 +1145,113 @@ def run_case(args):
                       "union": int(R.union_count.item())}))
 
 
-SWEEP_PASSES = 2    # distinct hidden-state passes per (rho, n)
-
-
 def run_sweep(args):
-    """One layer of a workload at each of its pass sizes and rhos through
-    both engines; each pass timed as run_case times it (a CUDA graph behind
-    an L2 flush, with and without the expert call). Prints one JSON line per
-    rho: requested bytes, expert-call time and bandwidth per n and engine,
-    the byte share u(n), the bandwidth ratio r(n) and the crossover."""
+    for line in sweep_workload(args.sweep, None if args.rho is None else [args.rho]):
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------- DRAM capture and record --
+DRAM_RHO = 0.9
+DRAM_CALL_WORKLOADS = {"v2lite": ("V2_LITE_STACK", 0), "mixtral": ("MIXTRAL", 0), "v3": ("V3", 0)}
+
+
+def run_calls(args):
+    """For an ncu DRAM capture of the expert calls: one layer of the
+    workload (the stack's layer 0 for v2lite) at rho = DRAM_RHO; at each pass
+    size one per-slot pass, then one dedup pass. Prints the requested bytes
+    of each expert call in launch order, as JSON."""
     import torch
     from __graft_entry__ import build
     build()
-    from moe_expert_layer_warp_gb300 import api, configs, stepmodel, synth
+    from moe_expert_layer_warp_gb300 import api, configs, synth
     from moe_expert_layer_warp_gb300.layer import PassRunner
-    w = getattr(configs, CASES[args.sweep])
-    sh = w.shape
-    L = synth.make_layer(sh, w.weight_seed, "cuda")
+    cname, _ = DRAM_CALL_WORKLOADS[args.calls]
+    w = getattr(configs, cname)
+    L = synth.make_layer(w.shape, w.weight_seed, "cuda")
     R = PassRunner(L, max(w.pass_sizes) * w.streams)
     st = torch.cuda.current_stream()
-    flush = torch.zeros(64 << 20, dtype=torch.float32, device="cuda")
-    t_flush = time_graphs([capture_graph(lambda s: flush.sum())], 6)[0]
-    engines = ("perslot", "dedup")
-    for rho in w.rhos:
-        samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
-        tfix = {n: [] for n in w.pass_sizes}
-        for n in w.pass_sizes:
-            for f in range(SWEEP_PASSES):
-                x = torch.from_numpy(synth.make_pass(sh.d, n, rho, [
-                    w.x_seed_base + 5000 + 97 * f + 13 * s for s in range(w.streams)])).cuda()
-                m = x.shape[0]
-                for eng in engines:
-                    R.forward(x, eng, st)
-                    b = [int(v) for v in R.bytes.cpu().tolist()]
-                    req = (b[0] if eng == "perslot" else b[1]) + b[2]
+    calls = []
+    for n in w.pass_sizes:
+        x = torch.from_numpy(synth.make_pass(w.shape.d, n, DRAM_RHO, [
+            w.x_seed_base + 7000 + 13 * s for s in range(w.streams)])).cuda()
+        for eng in ("perslot", "dedup"):
+            R.forward(x, eng, st)
+            torch.cuda.synchronize()
+            calls.append({"n": n * w.streams, "engine": eng, "requested": requested(R, eng)})
+    if api.moe_last_device_error() != api.MOE_OK:
+        raise RuntimeError("device error")
+    print(json.dumps({"workload": args.calls, "rho": DRAM_RHO, "calls": calls,
+                      "sources_sha256_16": kernel_source_hash()}), flush=True)
 
-                    def one(s, with_expert):
-                        flush.sum()
-                        R.route_union(x, s)
-                        if with_expert:
-                            R.experts(x, eng, s)
-                        R.combine(m, s)
-                    ga = capture_graph(lambda s: one(s, True))
-                    gb = capture_graph(lambda s: one(s, False))
-                    ta, tb = time_graphs([ga, gb], 3)
-                    samples[eng][n].append((req, max(ta - tb, 1e-9)))
-                    tfix[n].append(max(tb - t_flush, 0.0))
-                    del ga, gb
-        if api.moe_last_device_error() != api.MOE_OK:
-            raise RuntimeError("device error in the sweep")
-        ns = list(w.pass_sizes)
-        bw = {e: {n: stepmodel.effective_bandwidth([b for b, _ in samples[e][n]],
-                                                   [t for _, t in samples[e][n]]) for n in ns}
-              for e in engines}
-        u = {n: stepmodel.byte_share([b for b, _ in samples["dedup"][n]],
-                                     [b for b, _ in samples["perslot"][n]]) for n in ns}
-        r = {n: bw["dedup"][n] / bw["perslot"][n] for n in ns}
-        d = {"u_bar": [round(u[n], 6) for n in ns], "r": [round(r[n], 6) for n in ns],
-             "crossover_n": stepmodel.crossover(ns, u, r),
-             "t_fix_us": [round(statistics.median(tfix[n]) * 1e6, 2) for n in ns]}
-        line = {"sweep": w.name, "rho": rho, "streams": w.streams, "n": list(w.pass_sizes),
-                "passes_per_point": SWEEP_PASSES,
-                "timing": "expert call inside a CUDA-graph-replayed pass behind a 256 MB L2 "
-                          "flush (graph with minus graph without the call)",
-                "peak_GBs": peaks()[0]}
-        for eng in engines:
-            line[eng] = {
-                "requested_MB": [round(sum(b for b, _ in samples[eng][n]) / len(samples[eng][n])
-                                       / 1e6, 1) for n in w.pass_sizes],
-                "expert_us": [round(sum(t for _, t in samples[eng][n]) / len(samples[eng][n])
-                                    * 1e6, 2) for n in w.pass_sizes],
-                "GBs": [round(sum(b for b, _ in samples[eng][n]) / sum(t for _, t in samples[eng][n])
-                              / 1e9, 1) for n in w.pass_sizes]}
-        for k in ("u_bar", "r", "crossover_n", "t_fix_us"):
-            line[k] = d[k]
-        print(json.dumps(line), flush=True)
+
+def run_dram_record(args):
+    """Writes profiles/dram_expert_calls_<workload>.txt from the JSON that
+    --calls printed and the ncu csv (dram__bytes_read.sum and
+    dram__bytes_write.sum of the expert kernels, one launch per call, in
+    launch order) of the same command."""
+    import csv
+    calls_json, csv_path = args.dram_record
+    c = json.load(open(calls_json))
+    rows = list(csv.reader(l for l in open(csv_path) if l.startswith('"')))
+    head = rows[0]
+    ki, mi, vi, ii = (head.index(k) for k in ("Kernel Name", "Metric Name", "Metric Value", "ID"))
+    per = {}
+    names = {}
+    for r in rows[1:]:
+        if not re.search(r"expert_(mma|engine)_kernel", r[ki]):
+            continue
+        per.setdefault(int(r[ii]), 0)
+        names[int(r[ii])] = r[ki].split("(")[0].split("::")[-1]
+        if r[mi] in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            v = float(r[vi].replace(",", ""))
+            unit = r[head.index("Metric Unit")]
+            scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}[unit]
+            per[int(r[ii])] += v * scale
+    ids = sorted(per)
+    if len(ids) != len(c["calls"]):
+        raise SystemExit("%d expert-kernel launches in the csv, %d calls in the JSON"
+                         % (len(ids), len(c["calls"])))
+    tab = {"perslot": {}, "dedup": {}}
+    for i, call in zip(ids, c["calls"]):
+        tab[call["engine"]][call["n"]] = (call["requested"], int(round(per[i])), names[i])
+    ns = sorted(tab["perslot"])
+    path = dram_record_path(c["workload"])
+    with open(path, "w") as f:
+        f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one expert call per\n"
+                "# pass size and engine, %s-shaped layer, rho = %s, each call a cold pass of its own\n"
+                "# (routing differs from the bench's passes, so bench.py uses only the ratio of DRAM\n"
+                "# to requested bytes, per engine and n, and scales its own requested bytes by it).\n"
+                "# Used only while sources_sha256_16 matches the code of the kernel sources\n"
+                "# (bench.kernel_source_hash()).\n#\n"
+                "# Command (GB300, after the same command exited 0 without ncu):\n"
+                "#   python bench.py --calls %s > calls.json &&\n"
+                "#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \\\n"
+                "#       -k regex:\"expert_(mma|engine)_kernel\" --csv --log-file dram.csv \\\n"
+                "#       python bench.py --calls %s\n"
+                "#   python bench.py --dram-record calls.json dram.csv\n#\n"
+                "# n  engine   kernel                 requested MB   DRAM MB   DRAM/requested\n"
+                % (c["workload"], c["rho"], c["workload"], c["workload"]))
+        for eng in ("perslot", "dedup"):
+            for n in ns:
+                rq, dr, kn = tab[eng][n]
+                f.write("# %2d %-8s %-22s %12.1f %9.1f %8.3f\n" % (n, eng, kn, rq / 1e6, dr / 1e6,
+                                                                 dr / rq))
+        f.write("sources_sha256_16: %s\n" % c["sources_sha256_16"])
+        f.write("rho: %s\n" % c["rho"])
+        f.write("n: %s\n" % ",".join(str(n) for n in ns))
+        for eng in ("perslot", "dedup"):
+            f.write("%s_requested: %s\n" % (eng, ",".join(str(tab[eng][n][0]) for n in ns)))
+            f.write("%s_dram: %s\n" % (eng, ",".join(str(tab[eng][n][1]) for n in ns)))
+    print("wrote", os.path.relpath(path, ROOT))
 
 
 def main():
     args = parse_args()
-    if args.sweep:
+    if args.dram_record:
+        run_dram_record(args)
+    elif args.calls:
+        run_calls(args)
+    elif args.sweep:
         run_sweep(args)
     elif args.case:
         run_case(args)

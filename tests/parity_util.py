@@ -90,12 +90,32 @@ def host_layer_subset(L: synth.LayerWeights, experts):
     return out
 
 
-def oracle_outputs(L: synth.LayerWeights, x: np.ndarray, orc_route: dict, tokens):
-    """Oracle y and per-slot outputs for the listed tokens (float64)."""
-    experts = sorted(set(orc_route["idx"][list(tokens)].ravel().tolist()))
-    remap = {e: i for i, e in enumerate(experts)}
-    H = host_layer_subset(L, experts)
-    idx = np.vectorize(remap.get)(orc_route["idx"][list(tokens)]).astype(np.int32)
-    y, ys = oracle.moe_tokens(x[list(tokens)], idx, orc_route["w"][list(tokens)], H["wg"],
-                              H["wu"], H["wd"], H["sg"], H["su"], H["sd"], slots=True)
-    return y, ys
+def oracle_outputs(L: synth.LayerWeights, x: np.ndarray, orc_route: dict, tokens,
+                   max_experts: int = 32):
+    """Oracle y and per-slot outputs for the listed tokens (float64). The
+    tokens are taken in chunks whose selected experts number at most
+    max_experts (or one token's k), so that the host holds copies of only
+    those experts at a time (a DeepSeek-V3-shaped expert is 88 MB)."""
+    tokens = list(tokens)
+    chunks, cur, cur_e = [], [], set()
+    for t in tokens:
+        e = set(orc_route["idx"][t].tolist())
+        if cur and len(cur_e | e) > max_experts:
+            chunks.append(cur)
+            cur, cur_e = [], set()
+        cur.append(t)
+        cur_e |= e
+    if cur:
+        chunks.append(cur)
+    ys_all, slots_all = [], []
+    for ch in chunks:
+        experts = sorted(set(orc_route["idx"][ch].ravel().tolist()))
+        remap = {e: i for i, e in enumerate(experts)}
+        H = host_layer_subset(L, experts)
+        idx = np.vectorize(remap.get)(orc_route["idx"][ch]).astype(np.int32)
+        y, ys = oracle.moe_tokens(x[ch], idx, orc_route["w"][ch], H["wg"], H["wu"], H["wd"],
+                                  H["sg"], H["su"], H["sd"], slots=True)
+        del H
+        ys_all.append(y)
+        slots_all.append(ys)
+    return np.concatenate(ys_all), np.concatenate(slots_all)

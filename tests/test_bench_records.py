@@ -1,37 +1,81 @@
-"""Host checks of the benchmark's committed ncu records: the traffic record
-parses, is used only while its source hash matches the expert call's code
-(the first two checks skip when it does not), and its per-slot DRAM table has one entry per pass size with DRAM reads
-between the call's unique and requested expert bytes."""
+"""Host checks of the benchmark's committed ncu DRAM records and of the code
+that writes and reads them: a record is used only while its source hash
+matches the kernels' code, it round-trips from an ncu csv, and every
+committed record's DRAM bytes are plausible against the requested bytes (a
+dedup call reads each requested byte from DRAM about once; a per-slot call
+never reads more than it requests)."""
+import json
+import os
+import types
+
 import pytest
 
 import bench
-from moe_expert_layer_warp_gb300 import configs
 
 
-def test_traffic_record_matches_current_sources():
-    rec = bench.load_traffic_record(bench.TRAFFIC_FILE)
-    if rec is None:
-        pytest.skip("the traffic record was taken on other kernel sources (bench reports null)")
-    assert int(rec["dram_bytes_per_launch"]) > 0
+def _fake_capture(tmp_path, calls, dram):
+    """A --calls JSON and an ncu csv in the form ncu writes (two metrics per
+    launch, an unrelated kernel in between)."""
+    cj = tmp_path / "calls.json"
+    cj.write_text(json.dumps({"workload": "v2lite", "rho": 0.9, "calls": calls,
+                              "sources_sha256_16": bench.kernel_source_hash()}))
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+            '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+            '"Metric Value"\n')
+    lines = ["==PROF== Connected to process 1\n", head]
+    for i, (rd, wr) in enumerate(dram):
+        kn = "void unnamed>::expert_mma_kernel(unnamed>::Params)"
+        for m, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr)):
+            lines.append('"%d","1","python3","h","%s","1","7","(384, 1, 1)","(152, 1, 1)","0",'
+                         '"10.3","Command line profiler metrics","%s","byte","%s"\n'
+                         % (i, kn, m, "{:,}".format(v)))
+    cv = tmp_path / "dram.csv"
+    cv.write_text("".join(lines))
+    return str(cj), str(cv)
 
 
-def test_perslot_dram_table_is_bounded_by_requested_bytes():
-    w = configs.V2_LITE
-    sh = w.shape
-    e_b = 3 * sh.d * sh.inter * 2
-    ps = bench.load_perslot_dram(bench.TRAFFIC_FILE, len(w.pass_sizes))
-    if ps is None:
-        pytest.skip("the traffic record was taken on other kernel sources (bench reports null)")
-    assert len(ps) == len(w.pass_sizes)
-    for n, b in zip(w.pass_sizes, ps):
-        requested = (n * sh.top_k + sh.n_shared) * e_b
-        at_least = (sh.top_k + sh.n_shared) * e_b  # a pass's slots name at least k experts
-        assert 0.98 * at_least <= b <= 1.02 * requested, (n, b, requested)
-    assert bench.load_perslot_dram(bench.TRAFFIC_FILE, len(w.pass_sizes) + 1) is None
-
-
-def test_stale_record_is_ignored(monkeypatch):
+def test_dram_record_round_trip(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "dram_record_path",
+                        lambda wl: str(tmp_path / ("dram_expert_calls_%s.txt" % wl)))
+    calls, dram = [], []
+    for n in (1, 2, 3):
+        for eng, req, rd in (("perslot", 1000 * n, 700 * n), ("dedup", 900, 901)):
+            calls.append({"n": n, "engine": eng, "requested": req})
+            dram.append((rd, 3))
+    cj, cv = _fake_capture(tmp_path, calls, dram)
+    bench.run_dram_record(types.SimpleNamespace(dram_record=(cj, cv)))
+    rec = bench.load_dram_record("v2lite")
+    assert rec["n"] == [1, 2, 3] and rec["rho"] == 0.9
+    assert rec["perslot_requested"] == [1000, 2000, 3000]
+    assert rec["perslot_dram"] == [703, 1403, 2103]
+    assert rec["dedup_dram"] == [904, 904, 904]
+    r = bench.dram_ratio("v2lite", 0.9)
+    assert r["perslot"][2] == pytest.approx(1403 / 2000)
+    assert bench.dram_ratio("v2lite", 0.5) is None            # taken at another rho
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
-    assert bench.load_traffic_record(bench.TRAFFIC_FILE) is None
-    assert bench.load_traffic(bench.TRAFFIC_FILE) is None
-    assert bench.load_perslot_dram(bench.TRAFFIC_FILE, 9) is None
+    assert bench.load_dram_record("v2lite") is None           # other kernel sources
+    assert bench.dram_ratio("v2lite", 0.9) is None
+
+
+def test_dram_record_refuses_a_launch_count_mismatch(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "dram_record_path", lambda wl: str(tmp_path / "x.txt"))
+    calls = [{"n": 1, "engine": "perslot", "requested": 10},
+             {"n": 1, "engine": "dedup", "requested": 10}]
+    cj, cv = _fake_capture(tmp_path, calls, [(5, 0)])
+    with pytest.raises(SystemExit):
+        bench.run_dram_record(types.SimpleNamespace(dram_record=(cj, cv)))
+    assert not os.path.exists(tmp_path / "x.txt")
+
+
+@pytest.mark.parametrize("workload", ["v2lite", "mixtral", "v3"])
+def test_committed_records_are_plausible(workload):
+    rec = bench.load_dram_record(workload, check_hash=False)
+    if rec is None:
+        pytest.skip("no committed DRAM record for %s" % workload)
+    for i, n in enumerate(rec["n"]):
+        ps_req, ps_dr = rec["perslot_requested"][i], rec["perslot_dram"][i]
+        dd_req, dd_dr = rec["dedup_requested"][i], rec["dedup_dram"][i]
+        assert 0.97 * dd_req <= dd_dr <= 1.03 * dd_req, (workload, n, dd_req, dd_dr)
+        assert ps_dr <= 1.03 * ps_req, (workload, n, ps_req, ps_dr)
+        assert ps_dr >= 0.97 * dd_req, (workload, n)   # the same pass's unique bytes at least
+        assert ps_req >= dd_req
