@@ -291,6 +291,34 @@ def measure_breakdown(w, runners, xs):
     return samples, t_fix, pass_ms
 
 
+FUSED_PASSES = 4   # passes per (pass size, engine) in the fused-combine comparison
+
+
+def measure_fused(w, runners, xs):
+    """Pass time with the combine as a launch of its own (moe_verify_pass)
+    and fused into the expert kernel (moe_verify_pass_fused), per pass size
+    and engine: FUSED_PASSES passes on as many layers, each captured both
+    ways as a CUDA graph and replayed round-robin between CUDA events;
+    medians in microseconds."""
+    out = {"separate_us": {}, "fused_us": {}}
+    for eng in ("perslot", "dedup"):
+        sep, fus = [], []
+        for n in w.pass_sizes:
+            plan = [(i % len(runners), i % N_PASSES_PER_N) for i in range(FUSED_PASSES)]
+            ga = [capture_graph(lambda s, li=li, q=q: runners[li].forward(xs[n][q], eng, s))
+                  for li, q in plan]
+            gb = [capture_graph(lambda s, li=li, q=q: runners[li].forward(xs[n][q], eng, s,
+                                                                         fused=True))
+                  for li, q in plan]
+            t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
+            sep.append(round(statistics.median(t[:len(plan)]) * 1e6, 2))
+            fus.append(round(statistics.median(t[len(plan):]) * 1e6, 2))
+            del ga, gb
+        out["separate_us"][eng] = sep
+        out["fused_us"][eng] = fus
+    return out
+
+
 def e2e_measure(w, runners, xs, steps, warmup):
     """End to end through the public API with host buffers, as a serving loop
     runs it: each step uploads all its passes' hidden states from pinned host
@@ -938,6 +966,7 @@ def run_ours(args):
     # per-call breakdown on the stack's layers (outside the timed region)
     samples, t_fix, pass_ms = measure_breakdown(w, runners, xs)
     rep = stepmodel.build_report(samples, t_fix, layers=len(runners))
+    fused = measure_fused(w, runners, xs)
     e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
     e2e_ms = max_over_ranks(e2e_ms, dev)
     eager_ms, _, _, eager_host_ms = e2e_measure_eager(w, runners, xs, max(3, args.steps // 4), 2)
@@ -1030,8 +1059,14 @@ def run_ours(args):
         "clocks": clk,
         "layer_breakdown": {
             "what": "one layer pass at a time on the stack's layers (8 passes per point, each on "
-                    "another layer), expert call = graph with minus graph without the call",
-            "engines": per_engine, "stepmodel": rep.as_dict()},
+                    "another layer), expert call = graph with minus graph without the call; "
+                    "t_fix = routing, union and combine",
+            "engines": per_engine, "stepmodel": rep.as_dict(),
+            "fused_combine": dict(fused, what="one layer pass (graph replay, median of %d passes "
+                                  "on as many layers) with the combine as a launch of its own "
+                                  "(moe_verify_pass, the headline's path) and fused into the "
+                                  "expert kernel's last phase (moe_verify_pass_fused)"
+                                  % FUSED_PASSES)},
         "stack_check": stack,
         "tables": tables,
     }

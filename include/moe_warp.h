@@ -105,7 +105,8 @@ typedef struct {
  * must not share one. For bf16 layers it includes a fixed 24 MiB region of
  * partial sums: when a pass has too few weight tiles to keep every SM busy,
  * the engine cuts each tile's reduction into pieces and adds the pieces'
- * partial sums in a fixed order (results do not depend on scheduling).     */
+ * partial sums in a fixed order (results do not depend on scheduling). It
+ * also holds the count of moe_verify_pass_fused's combine.                  */
 size_t moe_workspace_bytes(const moe_layer_desc* desc, int32_t n_max);
 
 /* Gate GEMV, top-k and renormalised softmax
@@ -203,13 +204,34 @@ typedef enum { MOE_ENGINE_PERSLOT = 0, MOE_ENGINE_DEDUP = 1 } moe_engine;
  *   engine   MOE_ENGINE_PERSLOT or MOE_ENGINE_DEDUP (else MOE_EINVAL).
  *   topk_idx, topk_w, u, y_slot   the intermediate outputs, written as the
  *            single calls write them (caller-owned device buffers).
- *   y        [n][d] fp32 out, as moe_combine.
+ *   y        [n][d] fp32 out (16-byte aligned), as moe_combine.
  * Returns the first failing call's status; nothing after it is launched.   */
 moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* weights,
                            const float* bias, int32_t bias_in_weights, const float* x, int32_t n,
                            int32_t engine, int32_t* topk_idx, float* topk_w, const moe_union* u,
                            void* workspace, size_t workspace_bytes, float* y_slot, float* y,
                            void* stream);
+
+/* moe_verify_pass with the weighted combine fused into the expert kernel
+ * ("Deep Dive into Mixture of Experts", §2 and §5 sketches: output = shared
+ * experts + Σ weight·expert): the SwiGLU product is formed in the gate/up
+ * epilogue, each slot's weight is applied in the down epilogue, and the sum
+ * over the k+s slots is the kernel's last phase — every CTA publishes the
+ * down rows it stored with one GPU-scope release, waits (bounded) until the
+ * call's rows are all stored, and sums its share of y in slot order, the
+ * same additions in the same order as moe_combine. Same arguments and
+ * bitwise the same outputs as moe_verify_pass, one launch fewer. Measured
+ * on GB300 (DeepSeek-V2-Lite-shaped layer), a pass this way takes 1-2 us
+ * longer than moe_verify_pass: the in-kernel release and wait cost more
+ * than the combine launch they replace, which the previous kernel's tail
+ * hides (programmatic dependent launch). A call whose groups are split
+ * between the tensor-core and CUDA-core kernels (only when MOE_MMA_MIN_M
+ * forces it) runs the combine as a launch of its own.                      */
+moe_status moe_verify_pass_fused(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                                 const float* bias, int32_t bias_in_weights, const float* x,
+                                 int32_t n, int32_t engine, int32_t* topk_idx, float* topk_w,
+                                 const moe_union* u, void* workspace, size_t workspace_bytes,
+                                 float* y_slot, float* y, void* stream);
 
 /* Allocation-free variant of moe_verify_dedup (the sources have no
  * counterpart: this exists for callers, not for the method). Some callers

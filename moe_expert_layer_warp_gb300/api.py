@@ -24,7 +24,8 @@ MOE_MAX_TOKENS, MOE_MAX_PAIRS, MOE_MAX_EXPERTS, MOE_MAX_TOPK, MOE_MAX_SHARED = 1
 EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_build_union", "moe_verify_perslot",
             "moe_verify_dedup", "moe_combine", "moe_last_device_error", "moe_status_str",
             "moe_last_cuda_error_string", "moe_verify_dedup_noalloc", "moe_noalloc_scratch_limit",
-            "moe_diag_bounded_wait", "moe_route_biased", "moe_route_union", "moe_verify_pass")
+            "moe_diag_bounded_wait", "moe_route_biased", "moe_route_union", "moe_verify_pass",
+            "moe_verify_pass_fused")
 
 
 class MoeError(RuntimeError):
@@ -74,6 +75,7 @@ def load(path: str = LIB_PATH):
     lib.moe_build_union.argtypes = [D, P, I32, U, P]
     lib.moe_route_union.argtypes = [D, P, P, I32, P, I32, P, P, U, P, SZ, P]
     lib.moe_verify_pass.argtypes = [D, W, P, I32, P, I32, I32, P, P, U, P, SZ, P, P, P]
+    lib.moe_verify_pass_fused.argtypes = [D, W, P, I32, P, I32, I32, P, P, U, P, SZ, P, P, P]
     lib.moe_verify_perslot.argtypes = [D, W, P, I32, P, P, P, SZ, P, P]
     lib.moe_verify_dedup.argtypes = [D, W, P, I32, U, P, P, SZ, P, P]
     lib.moe_combine.argtypes = [D, P, I32, P, P]
@@ -88,7 +90,8 @@ def load(path: str = LIB_PATH):
     lib.moe_last_cuda_error_string.restype = ctypes.c_char_p
     for f in ("moe_route", "moe_build_union", "moe_verify_perslot", "moe_verify_dedup",
               "moe_combine", "moe_last_device_error", "moe_verify_dedup_noalloc",
-              "moe_diag_bounded_wait", "moe_route_biased", "moe_route_union", "moe_verify_pass"):
+              "moe_diag_bounded_wait", "moe_route_biased", "moe_route_union", "moe_verify_pass",
+              "moe_verify_pass_fused"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -176,6 +179,17 @@ def moe_verify_pass(desc, weights: LayerWeightsC, bias, bias_in_weights, x, n, e
                                   _ptr(topk_idx), _ptr(topk_w), ctypes.byref(u), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _ptr(y_slot),
                                   _ptr(y), _stream(stream)), "moe_verify_pass")
+
+
+def moe_verify_pass_fused(desc, weights: LayerWeightsC, bias, bias_in_weights, x, n, engine,
+                          topk_idx, topk_w, u: UnionC, workspace, y_slot, y, stream=None):
+    _check(load().moe_verify_pass_fused(ctypes.byref(desc), ctypes.byref(weights), _ptr(bias),
+                                        1 if bias_in_weights else 0, _ptr(x), n, engine,
+                                        _ptr(topk_idx), _ptr(topk_w), ctypes.byref(u),
+                                        _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _ptr(y_slot), _ptr(y), _stream(stream)),
+           "moe_verify_pass_fused")
 
 
 def moe_verify_perslot(desc, weights: LayerWeightsC, x, n, topk_idx, topk_w, workspace, y_slot,

@@ -86,9 +86,10 @@ moe_status check_n(const moe_layer_desc* d, int32_t n) {
 //   x32      [n_max][d] fp32          a copy of x (CUDA-core kernel input)
 //   sync     [kCcSyncInts] int32      CUDA-core kernel job counter, group counts
 //   sync_mma [kMmaSyncInts] int32     tensor-core kernel job counter, group counts, piece counts
+//   ydone    [64] int32                phase-1 units stored, for the combine fused into the kernel
 //   part     [kMmaPartBytes]           tensor-core kernel partial sums of K pieces (bf16 layers)
 struct WsLayout {
-  size_t logits, h, h16, xg, xg16, x16, x32, sync, sync_mma, part, part_bytes, total;
+  size_t logits, h, h16, xg, xg16, x16, x32, sync, sync_mma, ydone, part, part_bytes, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -116,6 +117,8 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
   off = align256(off + (size_t)moe::kCcSyncInts * 4);
   L.sync_mma = off;
   off = align256(off + (size_t)moe::kMmaSyncInts * 4);
+  L.ydone = off;
+  off = align256(off + 64 * 4);
   L.part = off;
   L.part_bytes = d->wdtype == MOE_W_BF16 ? moe::kMmaPartBytes : 0;
   off = align256(off + L.part_bytes);
@@ -270,10 +273,11 @@ moe_status moe_route_union(const moe_layer_desc* desc, const float* w_router, co
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_union launch");
 }
 
+// One expert-engine call; y non-null fuses the combine into the down epilogue.
 static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_layer_weights* w,
                              const float* x, int32_t n, const int32_t* topk_idx,
                              const moe_union* u, const float* topk_w, void* workspace,
-                             size_t workspace_bytes, float* y_slot, void* stream) {
+                             size_t workspace_bytes, float* y_slot, float* y, void* stream) {
   MOE_TRY(check_desc(desc));
   MOE_TRY(check_n(desc, n));
   MOE_TRY(check_weights(desc, w));
@@ -327,6 +331,8 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   // fp32 tolerance), so every fp32 group stays on the CUDA-core kernel.
   a.mma_min_m = desc->wdtype == MOE_W_BF16 ? mma_min_m(desc, engine, n) : 0x7fffffff;
   a.y_slot = y_slot;
+  a.y = y;
+  a.ydone = reinterpret_cast<int*>(ws + L.ydone);
   // Measured on GB300 (V2-Lite): normal eviction of the weight lines speeds
   // per-slot calls of 5 and 9 tokens by 2-4 % and slows 1- and 2-token
   // calls and dedup calls, which repeat no expert, by 0.4-3 %.
@@ -344,7 +350,7 @@ moe_status moe_verify_perslot(const moe_layer_desc* desc, const moe_layer_weight
                               float* y_slot, void* stream) {
   if (!topk_idx) return MOE_EINVAL;
   return run_engine(0, desc, weights, x, n, topk_idx, nullptr, topk_w, workspace,
-                    workspace_bytes, y_slot, stream);
+                    workspace_bytes, y_slot, nullptr, stream);
 }
 
 moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights* weights,
@@ -354,7 +360,7 @@ moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights*
   if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot)
     return MOE_EINVAL;
   return run_engine(1, desc, weights, x, n, nullptr, u, topk_w, workspace, workspace_bytes,
-                    y_slot, stream);
+                    y_slot, nullptr, stream);
 }
 
 // ------------------------------------------------ allocation-free variant --
@@ -414,12 +420,6 @@ moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_
   moe_status st = check_desc(desc);
   if (st != MOE_OK) return refuse(st, "invalid or unsupported layer descriptor");
   if (check_n(desc, n) != MOE_OK) return refuse(MOE_EINVAL, "pass size n out of range");
-  if (check_weights(desc, weights) != MOE_OK)
-    return refuse(MOE_EINVAL, "null or misaligned weight pointer");
-  if (!x || !topk_w || !y_slot || !aligned16(x))
-    return refuse(MOE_EINVAL, "null x, topk_w or y_slot, or x not 16-byte aligned");
-  if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot)
-    return refuse(MOE_EINVAL, "null union pointer");
   const size_t need = ws_layout(desc, n).total;
   if (need > kNoAllocScratchBytes) {
     snprintf(g_last_cuda_err, sizeof g_last_cuda_err,
@@ -428,6 +428,12 @@ moe_status moe_verify_dedup_noalloc(const moe_layer_desc* desc, const moe_layer_
              need, kNoAllocScratchBytes);
     return MOE_EINVAL;
   }
+  if (check_weights(desc, weights) != MOE_OK)
+    return refuse(MOE_EINVAL, "null or misaligned weight pointer");
+  if (!x || !topk_w || !y_slot || !aligned16(x))
+    return refuse(MOE_EINVAL, "null x, topk_w or y_slot, or x not 16-byte aligned");
+  if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot)
+    return refuse(MOE_EINVAL, "null union pointer");
   void* scratch = nullptr;
   MOE_TRY(noalloc_scratch(&scratch));
   return moe_verify_dedup(desc, weights, x, n, u, topk_w, scratch, kNoAllocScratchBytes, y_slot,
@@ -444,23 +450,46 @@ moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_combine launch");
 }
 
+// A whole pass: routing and union, one engine, and the combine either as a
+// launch of its own (fused = false) or as the expert kernel's last phase.
+static moe_status verify_pass(bool fused, const moe_layer_desc* desc,
+                              const moe_layer_weights* weights, const float* bias,
+                              int32_t bias_in_weights, const float* x, int32_t n, int32_t engine,
+                              int32_t* topk_idx, float* topk_w, const moe_union* u,
+                              void* workspace, size_t workspace_bytes, float* y_slot, float* y,
+                              void* stream) {
+  if (!weights || !y_slot || !y || (engine != MOE_ENGINE_PERSLOT && engine != MOE_ENGINE_DEDUP))
+    return MOE_EINVAL;
+  if (!aligned16(y_slot) || !aligned16(y)) return MOE_EINVAL;
+  MOE_TRY(moe_route_union(desc, weights->w_router, bias, bias_in_weights, x, n, topk_idx, topk_w, u,
+                          workspace, workspace_bytes, stream));
+  float* y_fused = fused ? y : nullptr;
+  if (engine == MOE_ENGINE_PERSLOT) {
+    MOE_TRY(run_engine(0, desc, weights, x, n, topk_idx, nullptr, topk_w, workspace,
+                       workspace_bytes, y_slot, y_fused, stream));
+  } else {
+    MOE_TRY(run_engine(1, desc, weights, x, n, nullptr, u, topk_w, workspace, workspace_bytes,
+                       y_slot, y_fused, stream));
+  }
+  return fused ? MOE_OK : moe_combine(desc, y_slot, n, y, stream);
+}
+
 moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* weights,
                            const float* bias, int32_t bias_in_weights, const float* x, int32_t n,
                            int32_t engine, int32_t* topk_idx, float* topk_w, const moe_union* u,
                            void* workspace, size_t workspace_bytes, float* y_slot, float* y,
                            void* stream) {
-  if (!weights || !y_slot || !y || (engine != MOE_ENGINE_PERSLOT && engine != MOE_ENGINE_DEDUP))
-    return MOE_EINVAL;
-  MOE_TRY(moe_route_union(desc, weights->w_router, bias, bias_in_weights, x, n, topk_idx, topk_w, u,
-                          workspace, workspace_bytes, stream));
-  if (engine == MOE_ENGINE_PERSLOT) {
-    MOE_TRY(moe_verify_perslot(desc, weights, x, n, topk_idx, topk_w, workspace, workspace_bytes,
-                               y_slot, stream));
-  } else {
-    MOE_TRY(moe_verify_dedup(desc, weights, x, n, u, topk_w, workspace, workspace_bytes, y_slot,
-                             stream));
-  }
-  return moe_combine(desc, y_slot, n, y, stream);
+  return verify_pass(false, desc, weights, bias, bias_in_weights, x, n, engine, topk_idx, topk_w,
+                     u, workspace, workspace_bytes, y_slot, y, stream);
+}
+
+moe_status moe_verify_pass_fused(const moe_layer_desc* desc, const moe_layer_weights* weights,
+                                 const float* bias, int32_t bias_in_weights, const float* x,
+                                 int32_t n, int32_t engine, int32_t* topk_idx, float* topk_w,
+                                 const moe_union* u, void* workspace, size_t workspace_bytes,
+                                 float* y_slot, float* y, void* stream) {
+  return verify_pass(true, desc, weights, bias, bias_in_weights, x, n, engine, topk_idx, topk_w,
+                     u, workspace, workspace_bytes, y_slot, y, stream);
 }
 
 moe_status moe_diag_bounded_wait(int32_t limit_us, void* stream) {

@@ -17,7 +17,8 @@ MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
 
 // Runs right before the expert kernels and lets them launch as soon as it
 // starts (programmatic dependent launch); they wait for it before touching
-// its outputs. The grid zeroes both kernels' job counters and group counts.
+// its outputs. The grid zeroes both kernels' job counters and group counts,
+// and the fused combine's count when the call has one.
 // Blocks [0, gather_rows): xg[r] = x[pair_tok[r]] (fp32) and its bf16 hi/lo
 // halves (dedup, union order). Blocks [gather_rows, gather_rows + n): x32 =
 // a copy of x and, for bf16 layers, the bf16 hi/lo halves of x.
@@ -28,14 +29,16 @@ __global__ void __launch_bounds__(256)
                        uint16_t* __restrict__ xg16, uint16_t* __restrict__ xg16lo,
                        float* __restrict__ x32, uint16_t* __restrict__ x16,
                        uint16_t* __restrict__ x16lo, int* __restrict__ sync_cc,
-                       int* __restrict__ sync_mma) {
+                       int* __restrict__ sync_mma, int* __restrict__ ydone) {
   pdl_wait();     // the union (dedup) or routing that precedes it
   pdl_trigger();
-  {  // counters, spread over the grid (int4 stores; both regions are 256-byte aligned)
+  {  // counters, spread over the grid (int4 stores; every region is 256-byte aligned and
+     // padded to 256 bytes)
     const int nt = gridDim.x * blockDim.x, t = blockIdx.x * blockDim.x + threadIdx.x;
     const int4 z = make_int4(0, 0, 0, 0);
     for (int i = t; i < (kCcSyncInts + 3) / 4; i += nt) reinterpret_cast<int4*>(sync_cc)[i] = z;
     for (int i = t; i < (kMmaSyncInts + 3) / 4; i += nt) reinterpret_cast<int4*>(sync_mma)[i] = z;
+    if (t == 0 && ydone) *reinterpret_cast<int4*>(ydone) = z;
   }
   const int b = blockIdx.x;
   const float* src;
@@ -73,7 +76,8 @@ cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t 
   const int gather = a.engine == 1 ? a.n * a.k : 0;
   cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + a.n, 4)), dim3(256), 0, stream,
                              a.d, a.n, gather, a.wdtype == 1 ? 1 : 0, a.x, a.pair_tok, a.xg,
-                             a.xg16, a.xg16lo, a.x32, a.x16, a.x16lo, a.sync, a.sync_mma);
+                             a.xg16, a.xg16lo, a.x32, a.x16, a.x16lo, a.sync, a.sync_mma,
+                             a.y ? a.ydone : nullptr);
   if (e != cudaSuccess) return e;
   // The tensor-core kernel runs only where a group can reach mma_min_m
   // tokens: a group never holds more than the pass's n tokens, and per-slot
@@ -84,11 +88,18 @@ cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t 
   const bool cc = !(mma && a.mma_min_m <= 1);
   ExpertArgs b = a;
   b.cc_waits_prep = mma ? 0 : 1;
+  // The combine is fused into the expert kernel's last phase when one kernel
+  // runs the whole call; a call split between the two kernels (only when
+  // MOE_MMA_MIN_M forces it) combines in a launch of its own afterwards.
+  const bool split = mma && cc;
+  if (split) b.y = nullptr;
   if (mma) {
     e = launch_expert_mma(b, num_sms, stream);
     if (e != cudaSuccess || !cc) return e;
   }
-  return launch_expert_cc(b, num_sms, stream);
+  e = launch_expert_cc(b, num_sms, stream);
+  if (e != cudaSuccess || !split || !a.y) return e;
+  return launch_combine(a.d, a.k + a.s, a.n, a.y_slot, a.y, stream);
 }
 
 }  // namespace moe

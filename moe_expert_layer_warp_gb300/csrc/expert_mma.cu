@@ -28,7 +28,10 @@
 // grain of the work a call is dealt in without cutting K. The epilogue
 // warps of the up half hand their values to the gate half through shared
 // memory, which writes h as its hi/lo halves. Phase 1 (down) writes the
-// weighted slot outputs. Every stage carries two 64-column K-steps; the
+// weighted slot outputs. When the call fuses the combine, every CTA counts
+// the row quarters it stored and, after its last job, takes part in the
+// kernel's last phase (tail_combine): once the whole call's quarters are
+// stored, it sums its share of y over the slots in slot order. Every stage carries two 64-column K-steps; the
 // ring holds as many stages as fit for the call's largest token tile (5 for
 // h ≤ 16, 4 for h = 32), which matters most for per-slot calls, about half
 // of whose weight reads hit L2 and half miss to DRAM.
@@ -93,7 +96,7 @@ constexpr int kOffPlan = kOffBar + kNumBars * 8;
 constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
 constexpr int kOffRowW = kOffRowOut + kMaxRows * 2;
 constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
-constexpr int kOffXch = kOffMisc + 128 * 4;         // [kH0 rows][kSub tokens] fp32: up → gate half
+constexpr int kOffXch = kOffMisc + 160 * 4;         // [kH0 rows][kSub tokens] fp32: up → gate half
 constexpr int kSmemBytes = kOffXch + kH0 * kSub * 4 + 1024;  // + slack to align the base to 1024
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
@@ -181,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
   int* pub_cnt = misc + 44;                             // [kPubSlots] quarters finished
   int* max_m = misc + 52;
   volatile int* fin_job = misc + 64;                    // [4][kFinSlots]
+  int* tail_flag = misc + 128;                          // fused combine: the wait's outcome
+  int* ph1_done = misc + 129;                           // phase-1 row quarters stored by this CTA
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -204,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     }
     mbar_init(xfull, 2);
     mbar_init(xempty, 2);
+    *ph1_done = 0;
     *abort_flag = 0;
     *max_m = 0;
     fence_mbar_init();
@@ -563,14 +569,17 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           }
         }
         ++pub_n;
-      } else if (row < a.d) {
+      } else {
+        if (tile * kM + quad * 32 < a.d) {  // warp-uniform: d is a multiple of 32
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (c < m) {
-            const int rr = en.row0 + c;
-            a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * gv[c];
+          for (int c = 0; c < 32; ++c) {
+            if (c < m) {
+              const int rr = en.row0 + c;
+              a.y_slot[(size_t)row_out[rr] * a.d + row] = row_w[rr] * gv[c];
+            }
           }
         }
+        if (lane == 0) atomicAdd(ph1_done, 1);  // one row quarter stored (fused combine)
       }
       if (++slot == 2) {
         slot = 0;
@@ -672,6 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
           }
         }
       }
+      if (ph == 1 && ok && lane == 0) atomicAdd(ph1_done, 1);  // one row quarter (fused combine)
       __syncwarp();  // every lane's stores before lane 0's release
       if (lane == 0) {
         if (ph == 0 && ok) red_release_add(done0 + g, 1);
@@ -686,6 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     umma::fence_after_sync();
     umma::tmem_dealloc(tmem, kTmemCols);
   }
+  // The combine fused as the last phase: every (entry, phase-1 tile) stores
+  // four row quarters, through the epilogue or the finishers.
+  if (a.y)
+    tail_combine(a, ph1_done, n_groups * c1.T * 4, abort_flag, tail_flag, (int)threadIdx.x,
+                 kThreads, [] { __syncthreads(); });
 }
 
 // W_gate or W_up [n_mat][rows][K] in 64-row boxes of one K-step.

@@ -40,7 +40,11 @@
 // columns of every token, so every weight byte is read from shared memory
 // once and used for all tokens of the sub-group. Columns beyond K arrive
 // zero-filled from the TMA and contribute nothing. A publisher warp makes
-// finished phase-0 tiles visible to other CTAs' phase-1 jobs.
+// finished phase-0 tiles visible to other CTAs' phase-1 jobs. When the call
+// fuses the combine, the consumer warps count the phase-1 rows they stored
+// and, after the CTA's last job, take part in the kernel's last phase
+// (tail_combine): once the whole call's rows are stored, they sum their
+// share of y over the slots in slot order.
 #include <math.h>
 
 #include "moe_warp.h"
@@ -96,7 +100,7 @@ struct Layout {
   static constexpr int kOffRowOut = kOffPlan + kMaxEntries * (int)sizeof(Entry);
   static constexpr int kOffRowW = kOffRowOut + kMaxRows * 2;
   static constexpr int kOffMisc = kOffRowW + kMaxRows * 4;
-  static constexpr int kBytes = kOffMisc + 64 * 4;
+  static constexpr int kBytes = kOffMisc + 96 * 4;
 };
 
 // Columns a lane owns inside a stage, chosen so that its shared-memory reads
@@ -167,6 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   volatile int* stage_job = misc + 32;                     // [kStages]
   volatile int* abort_flag = misc + 48;
   volatile int* pub_entry = misc + 52;                     // [kPubSlots]
+  int* tail_flag = misc + 64;                              // fused combine: the wait's outcome
+  int* ph1_done = misc + 65;                               // phase-1 warp rows stored by this CTA
+  int* tail_target = misc + 66;                            // ... and by the whole call
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -178,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
       mbar_init(&pub_full[i], kConsumerWarps);
       mbar_init(&pub_empty[i], 1);
     }
+    *ph1_done = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -227,6 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   int* job_counter = a.sync;
   int* done0 = a.sync + 1;
   const int done_target = T0;  // one publication per phase-0 tile
+  // every (entry, phase-1 tile) stores sixteen warp rows of four; kept in
+  // shared memory, so that the consumer loop holds no register for it
+  if (threadIdx.x == 0) *tail_target = n_groups * T1 * kConsumerWarps;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------ producer thread --
@@ -359,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     return;
   }
 
+
   // --------------------------------------------------------- consumer warps --
   // Warp w owns four weight rows of every stage: in phase 0 gate rows 2w and
   // 2w+1 and the same up rows of the 32-row tile (so h for those rows is
@@ -368,12 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
   int stage = 0;
   uint32_t phase = 0;
   int pub_n = 0;  // phase-0 jobs handed to the publisher so far
+  // Every exit below is taken by the whole warp, and every path leads to the
+  // consumers' last phase (consumers_done), where all 16 consumer warps meet.
   for (;;) {
-    if (!mbar_wait(&full[stage], phase, a.err, 0x220)) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err, 0x220))) {
       *abort_flag = 1;
-      return;
+      goto consumers_done;
     }
-    if (*abort_flag) return;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) goto consumers_done;
     const int job = stage_job[stage];
     if (job < 0) {
       // end marker for the publisher
@@ -413,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
 #pragma unroll
       for (int t = 0; t < kMaxM; ++t) acc[q][t] = make_float2(0.f, 0.f);
     for (int ks = 0; ks < nks; ++ks) {
-      if (ks > 0 && !mbar_wait(&full[stage], phase, a.err, 0x221)) {
+      if (ks > 0 && !__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err, 0x221))) {
         *abort_flag = 1;
-        return;
+        goto consumers_done;
       }
       const unsigned char* st = smem + stage * L::kStageBytes;
       const float* sx = reinterpret_cast<const float*>(st + L::kWBytes);
@@ -475,10 +489,19 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
             }
           }
         }
+        atomicAdd(ph1_done, 1);  // this warp's rows of the tile (fused combine)
       }
     }
     if (ph == 0) ++pub_n;
   }
+consumers_done:
+  // The combine fused as the last phase: every (entry, phase-1 tile) stores
+  // sixteen warp rows of four (one per consumer warp). The producer and
+  // publisher warps have left; the consumers synchronise on barrier 1.
+  if (a.y)
+    tail_combine(a, ph1_done, *tail_target, abort_flag, tail_flag, (int)threadIdx.x,
+                 kConsumerWarps * 32,
+                 [] { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory"); });
 }
 
 // ------------------------------------------------------------------ host --

@@ -192,4 +192,55 @@ MOE_DEV bool wait_count(const int* p, int target, unsigned int* err, unsigned in
   return true;
 }
 
+// The weighted combine fused into the expert kernel as its last phase
+// ("Deep Dive into Mixture of Experts", §2 and §5 sketches: the layer output
+// is the weighted sum of the selected experts plus the shared experts). Every
+// CTA of the kernel calls it once, with all its threads, after the CTA's last
+// job: *mine (shared memory) counts the phase-1 units (row quarters or warp
+// rows) the CTA stored, `target` the units the whole call stores. The CTA publishes
+// its count with one GPU-scope release (its threads' slot stores are ordered
+// before it by the barrier), waits (bounded, acquire) until the call's count
+// reaches the target, then sums its share of the [n][d/4] float4 columns:
+// y[t] = Σ_j y_slot[t][j] in slot order j = 0, 1, …, the same additions in
+// the same order as moe_combine, so y is bitwise what a separate combine
+// gives. A CTA that never ran a job adds nothing to the count, so nothing
+// here needs the grid to be resident at once. `flag` is one int of shared
+// memory; bar_sync() synchronises the calling threads (all of which call
+// this). Returns false if the CTA had stopped on an error (`abort`) or the
+// wait expired (recorded).
+template <typename Bar>
+MOE_DEV bool tail_combine(const ExpertArgs& a, const int* mine, int target,
+                          const volatile int* abort, int* flag, int tid, int nthreads,
+                          Bar bar_sync) {
+  bar_sync();  // every calling thread's slot stores and counts before thread 0's release
+  if (tid == 0) {
+    // a CTA that stopped on an error publishes nothing (the others' waits
+    // then expire and report it too)
+    int ok = 0;
+    if (*abort == 0) {
+      red_release_add(a.ydone, *reinterpret_cast<const volatile int*>(mine));
+      ok = wait_count(a.ydone, target, a.err, 0x500) ? 1 : 0;
+    }
+    *reinterpret_cast<volatile int*>(flag) = ok;
+  }
+  bar_sync();
+  if (*reinterpret_cast<volatile int*>(flag) == 0) return false;
+  const int S = a.k + a.s, d4 = a.d >> 2;
+  const int items = a.n * d4;
+  for (int i = blockIdx.x * nthreads + tid; i < items; i += gridDim.x * nthreads) {
+    const int t = i / d4, c4 = i - t * d4;
+    const float4* src = reinterpret_cast<const float4*>(a.y_slot + (size_t)t * S * a.d) + c4;
+    float4 acc = __ldcg(src);
+    for (int j = 1; j < S; ++j) {
+      const float4 v = __ldcg(src + (size_t)j * d4);
+      acc.x = __fadd_rn(acc.x, v.x);
+      acc.y = __fadd_rn(acc.y, v.y);
+      acc.z = __fadd_rn(acc.z, v.z);
+      acc.w = __fadd_rn(acc.w, v.w);
+    }
+    reinterpret_cast<float4*>(a.y + (size_t)t * a.d)[c4] = acc;
+  }
+  return true;
+}
+
 }  // namespace moe

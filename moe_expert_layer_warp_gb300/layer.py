@@ -3,7 +3,8 @@
 ``PassRunner`` owns the device buffers a pass needs (workspace, routing,
 union, slot outputs, output) for passes of up to ``n_max`` tokens and calls
 the library's entry points: forward() makes one moe_verify_pass call
-(moe_route_union → moe_verify_perslot or moe_verify_dedup → moe_combine);
+(moe_route_union → moe_verify_perslot or moe_verify_dedup → moe_combine), or
+one moe_verify_pass_fused call (the combine inside the expert kernel);
 route(), build_union(), route_union(), experts() and combine() make the
 single calls. Buffers are allocated
 once, through torch, at construction, and so are the C arguments that point
@@ -141,10 +142,12 @@ class PassRunner:
 
     # -- a whole pass ---------------------------------------------------------
     def forward(self, x: torch.Tensor, engine: str = DEDUP, stream=None,
-                out: torch.Tensor = None) -> torch.Tensor:
+                out: torch.Tensor = None, fused: bool = False) -> torch.Tensor:
         """y [n][d] for the pass x [n][d] (fp32, on the layer's device),
         written to `out` if given (a contiguous fp32 [n][d] device tensor),
-        else to the runner's own buffer (overwritten by its next pass)."""
+        else to the runner's own buffer (overwritten by its next pass).
+        fused: moe_verify_pass_fused (the combine as the expert kernel's last
+        phase) instead of moe_verify_pass; the same results bit for bit."""
         xp = self._x(x)
         if engine not in (PERSLOT, DEDUP):
             raise ValueError("engine must be %r or %r" % (PERSLOT, DEDUP))
@@ -157,10 +160,11 @@ class PassRunner:
                                  % (n, self.shape.d, self.weights.device))
             y = ctypes.c_void_p(out.data_ptr())
         eng = api.MOE_ENGINE_PERSLOT if engine == PERSLOT else api.MOE_ENGINE_DEDUP
-        api._check(self._lib.moe_verify_pass(self._desc, self._wref, self._bias, self._bias_w, xp,
-                                             n, eng, self._idx, self._tw, self._uref, self._ws,
-                                             self._ws_bytes, self._yslot, y, api._stream(stream)),
-                   "moe_verify_pass")
+        f = self._lib.moe_verify_pass_fused if fused else self._lib.moe_verify_pass
+        api._check(f(self._desc, self._wref, self._bias, self._bias_w, xp, n, eng, self._idx,
+                     self._tw, self._uref, self._ws, self._ws_bytes, self._yslot, y,
+                     api._stream(stream)),
+                   "moe_verify_pass_fused" if fused else "moe_verify_pass")
         return out if out is not None else self.y[: n * self.shape.d].view(n, self.shape.d)
 
     # -- views ---------------------------------------------------------------

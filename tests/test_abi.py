@@ -52,7 +52,7 @@ def test_workspace_bytes_closed_form(lib):
         want = (a256(n * sh.n_experts * 4) + a256(hrows * sh.inter * 4) + a256(2 * hrows * sh.inter * 2)
                 + a256(n * sh.top_k * sh.d * 4) + a256(2 * n * sh.top_k * sh.d * 2)
                 + a256(2 * n * sh.d * 2) + a256(n * sh.d * 4) + a256(CC_SYNC_INTS * 4)
-                + a256(MMA_SYNC_INTS * 4)
+                + a256(MMA_SYNC_INTS * 4) + 256
                 + (MMA_PART_BYTES if sh.wdtype == W_BF16 else 0))
         assert got == want, w.name
 
@@ -187,3 +187,15 @@ def test_noalloc_refusals_each_say_why(lib):
     assert f(ctypes.byref(desc), ctypes.byref(w), one, 4, ctypes.byref(api.UnionC()), one, one,
              None) == api.MOE_EINVAL
     assert "union" in msg()
+
+
+def test_noalloc_size_refusal_comes_before_pointer_checks(lib):
+    """A pass above the static maximum is refused for its size whatever else
+    is wrong with the call (the caller learns first that it needs a
+    workspace)."""
+    big = api.make_desc(LayerShape(7168, 256, 8, 2048, 1, W_BF16))
+    one = ctypes.c_void_p(4096)
+    st = lib.moe_verify_dedup_noalloc(ctypes.byref(big), ctypes.byref(api.LayerWeightsC()), one, 64,
+                                      ctypes.byref(api.UnionC()), one, one, None)
+    assert st == api.MOE_EINVAL
+    assert "static maximum" in lib.moe_last_cuda_error_string().decode()

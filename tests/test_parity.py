@@ -52,6 +52,12 @@ def run_both(L, x_np, runner=None):
     u = {k: (v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in R.union(n).items()}
     y_dd = R.forward(x, DEDUP).cpu().numpy()
     slots_dd = R.slots(n).cpu().numpy()
+    # the pass with the combine fused into the expert kernel: the same y, bit for bit
+    for eng, y_ref in ((PERSLOT, y_ps), (DEDUP, y_dd)):
+        R.y.fill_(float("nan"))
+        y_f = R.forward(x, eng, fused=True).cpu().numpy()
+        np.testing.assert_array_equal(y_f.view(np.uint32), y_ref.view(np.uint32),
+                                      err_msg="fused combine, %s" % eng)
     from moe_expert_layer_warp_gb300 import api
     assert api.moe_last_device_error() == api.MOE_OK
     out.update(y_ps=y_ps, y_dd=y_dd, slots_ps=slots_ps, slots_dd=slots_dd, idx=idx, w=w, u=u)
@@ -248,12 +254,15 @@ def test_exact_ties_go_to_the_lower_index(shape):
     np.testing.assert_array_equal(pairs[:, :, 0], pairs[:, :, 1])
 
 
+@pytest.mark.parametrize("shape", [LayerShape(576, 16, 4, 320, 1, W_BF16),
+                                   LayerShape(192, 6, 3, 256, 2, W_F32)], ids=["bf16", "f32"])
 @pytest.mark.parametrize("bias_mode", [None, 0], ids=["plain", "selection-only-bias"])
-def test_verify_pass_equals_single_calls(bias_mode):
-    """forward() (one moe_verify_pass call) against moe_route_union,
-    moe_verify_* and moe_combine made one by one: y, slot outputs and
-    routing bit for bit, for both engines."""
-    shape = LayerShape(576, 16, 4, 320, 1, W_BF16)
+@pytest.mark.parametrize("fused", [False, True], ids=["verify-pass", "verify-pass-fused"])
+def test_verify_pass_equals_single_calls(bias_mode, shape, fused):
+    """forward() — one moe_verify_pass call, or one moe_verify_pass_fused
+    call (the combine as the expert kernel's last phase) — against
+    moe_route_union, moe_verify_* and moe_combine made one by one: y, slot
+    outputs and routing bit for bit, for both engines."""
     L = synth.make_layer(shape, 71, "cuda")
     n = 11
     x = torch.from_numpy(synth.make_pass(shape.d, n, 0.9, [19])).cuda()
@@ -263,7 +272,8 @@ def test_verify_pass_equals_single_calls(bias_mode):
                                 .astype(np.float32) * 0.05).cuda()
     R = PassRunner(L, n, bias=bias, bias_in_weights=bool(bias_mode))
     for eng in (PERSLOT, DEDUP):
-        y1 = R.forward(x, eng).cpu().numpy().copy()
+        R.y.fill_(float("nan"))     # an element the fused combine missed would stay NaN
+        y1 = R.forward(x, eng, fused=fused).cpu().numpy().copy()
         s1 = R.slots(n).cpu().numpy().copy()
         i1 = R.routing(n)[0].cpu().numpy().copy()
         R.y.fill_(-1.0)
@@ -349,12 +359,16 @@ def test_v2_lite_stack_layers_full_size():
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("min_m", ["1000", "1"], ids=["cuda-core-only", "tensor-core-only"])
+@pytest.mark.parametrize("min_m", ["1000", "1", "3"],
+                         ids=["cuda-core-only", "tensor-core-only", "both-kernels-in-one-call"])
 def test_small_layers_on_each_expert_kernel(min_m):
     """bf16 calls pick one expert kernel by size; MOE_MMA_MIN_M (read once per
     process, hence a child process) forces every group of the same small
     layers onto the CUDA-core kernel (1000) or the tensor-core kernel (1),
-    cutting tiles along K wherever they are few."""
+    cutting tiles along K wherever they are few, or splits one call's groups
+    between the two kernels by size (3: groups of three or more tokens on
+    the tensor cores), so that both kernels add to the same fused-combine
+    counts."""
     import os
     import subprocess
     import sys
@@ -364,6 +378,7 @@ def test_small_layers_on_each_expert_kernel(min_m):
                         "tests/test_parity.py::test_small_layers_every_element",
                         "tests/test_parity.py::test_gate_up_storage",
                         "tests/test_parity.py::test_identical_tokens_select_k_experts",
-                        "tests/test_parity.py::test_repeated_runs_are_bitwise_identical"],
+                        "tests/test_parity.py::test_repeated_runs_are_bitwise_identical",
+                        "tests/test_parity.py::test_verify_pass_equals_single_calls"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
