@@ -2,7 +2,9 @@
 //
 // A "group" is one expert applied to a set of tokens whose activation rows
 // are consecutive rows of the h scratch:
-//   per-slot: one group per (token, slot) pair, rows in pair order t·k + j;
+//   per-slot: one group per (token, slot) pair, rows in pair order t·k + j
+//             (the pairs that chose the same expert are sibling entries, so
+//             that their jobs run side by side; each still reads the expert);
 //   dedup:    one group per union expert, rows in the union's (expert, token)
 //             order (moe_build_union's offsets);
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
@@ -25,7 +27,7 @@ struct Entry {
                    //   reads h at row0
   uint16_t first;  // first entry of this group's sub-groups
   uint8_t m;       // tokens of this sub-group (≤ 32)
-  uint8_t q;       // number of sub-groups of this group (≤ 32)
+  uint8_t q;       // number of sibling entries of this group (≤ 255)
 };
 static_assert(sizeof(Entry) == 16, "plan entry");
 static_assert(MOE_MAX_TOKENS * (MOE_MAX_TOPK + MOE_MAX_SHARED) <= 65536, "slot rows fit 16 bits");
@@ -108,7 +110,39 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
   int nr = 0;
   if (a.engine == 0) {
     if (mine(1)) {
-      for (int p = tid; p < P; p += nt) plan[p] = make_entry(a.topk_idx[p], p, 1, p / a.k, p, 1);
+      // One entry per (token, slot) pair — every slot still streams its own
+      // expert's weights — but the pairs that chose the same expert are
+      // siblings of one group, so their jobs run tile by tile side by side
+      // and L2 serves the repeated reads at the same moment. Entries in
+      // (expert, pair) order: a counting sort with row_w and row_out as its
+      // scratch (both rewritten below). An expert id outside [0, E) is
+      // recorded as an error and read as expert 0.
+      int* cnt = reinterpret_cast<int*>(row_w);
+      int* start = cnt + MOE_MAX_EXPERTS;
+      uint16_t* eid = row_out;
+      for (int e = tid; e < a.E; e += nt) cnt[e] = 0;
+      for (int p = tid; p < P; p += nt) {
+        int e = a.topk_idx[p];
+        if (e < 0 || e >= a.E) {
+          report_error(a.err, ERR_CHECK, 0x231);
+          e = 0;
+        }
+        eid[p] = (uint16_t)e;
+      }
+      __syncthreads();
+      for (int p = tid; p < P; p += nt) atomicAdd(&cnt[eid[p]], 1);
+      __syncthreads();
+      int total;
+      const int off = block_exclusive_scan(tid < a.E ? cnt[tid] : 0, scratch, &total);
+      if (tid < a.E) start[tid] = off;
+      __syncthreads();
+      for (int p = tid; p < P; p += nt) {
+        const int e = eid[p];
+        int rank = 0;
+        for (int q = 0; q < p; ++q) rank += (eid[q] == e);
+        plan[start[e] + rank] = make_entry(e, p, 1, p / a.k, start[e], cnt[e]);
+      }
+      __syncthreads();
       nr = P;
     }
     for (int p = tid; p < P; p += nt) {
