@@ -1263,7 +1263,8 @@ def run_dram_record(args):
                 "#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none \\\n"
                 "#       -k regex:\"expert_(mma|engine)_kernel\" --csv --log-file dram.csv \\\n"
                 "#       python bench.py --calls %s\n"
-                "#   python bench.py --dram-record calls.json dram.csv\n#\n"
+                "#   python bench.py --dram-record calls.json dram.csv\n"
+                "# The two metrics take one ncu pass per launch (nothing is saved or restored).\n#\n"
                 "# n  engine   kernel                 requested MB   DRAM MB   DRAM/requested\n"
                 % (c["workload"], c["rho"], c["workload"], c["workload"]))
         for eng in ("perslot", "dedup"):

@@ -134,17 +134,21 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
 // its gate/up tiles, and with fewer tiles than SMs it must cut tiles along K
 // and add the pieces across CTAs. The CUDA-core kernel works in 32- and
 // 64-row tiles, so few groups still fill the GPU, but its arithmetic per
-// weight byte grows with the tokens per group. Measured on GB300
-// (DeepSeek-V2-Lite-, Mixtral- and DeepSeek-V3-shaped layers): one-token
-// groups (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups,
-// and at any count when an expert spans 64 or more 128-row tiles (Mixtral,
-// V3: 1-3 % faster); dedup groups, which hold several tokens, go faster on
-// the tensor cores from ~350 tiles with 12 groups or more, or with 3 tokens
-// or more per group.
+// weight byte grows with the tokens per group. Measured on GB300 with each
+// kernel forced (DeepSeek-V2-Lite-, Mixtral- and DeepSeek-V3-shaped layers,
+// per-slot pairs of one expert run side by side): one-token groups
+// (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups, and at
+// any count when an expert spans 128 or more 128-row tiles (Mixtral: 3-6 %
+// faster; V3, 72 tiles, is 9 % faster on the tensor cores); dedup groups,
+// which hold several tokens, go faster on the tensor cores from ~350 tiles
+// with 15 groups or more, or with 3 tokens or more per group.
 // The groups of a dedup call are known only on the device: the estimate
-// takes half of min(E, n·k) distinct experts. MOE_MMA_MIN_M in the
-// environment (read once; for tuning) fixes instead the smallest group
-// that runs on the tensor cores.
+// takes half of min(E, n·k) distinct experts, which the union reaches at
+// hidden-state correlations near 0.9; far from it (0 or 0.99) the estimate
+// can pick the slower kernel for mid-size passes (measured: up to 6-10 % on
+// the V2-Lite- and Mixtral-shaped calls at 4-6 tokens). MOE_MMA_MIN_M in the
+// environment (read once; for tuning) fixes instead the smallest group that
+// runs on the tensor cores.
 int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   static const int forced = [] {
     const char* e = getenv("MOE_MMA_MIN_M");
@@ -158,11 +162,11 @@ int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   bool mma;
   if (engine == 0) {
     const int groups = pairs + shared;
-    mma = groups * tiles >= 400 && groups >= 12 && tiles < 64;
+    mma = groups * tiles >= 400 && groups >= 12 && tiles < 128;
   } else {
     const int routed = std::max(1, std::min(d->n_experts, pairs) / 2);
     const int groups = routed + shared;
-    mma = groups * tiles >= 350 && (groups >= 12 || pairs >= 3 * routed);
+    mma = groups * tiles >= 350 && (groups >= 15 || pairs >= 3 * routed);
   }
   return mma ? 1 : 0x7fffffff;
 }
