@@ -249,6 +249,12 @@ def requested(R, eng):
     return (b[0] if eng == "perslot" else b[1]) + b[2]
 
 
+def unique_bytes(R):
+    """The runner's last pass's distinct expert bytes, |U|·E_b + s·E_b."""
+    b = [int(v) for v in R.bytes.cpu().tolist()]
+    return b[1] + b[2]
+
+
 def measure_breakdown(w, runners, xs):
     """The expert call's time inside a pipelined pass, per pass size and
     engine, on the stack's layers. Each of BREAKDOWN_PASSES passes (pass i on
@@ -259,6 +265,7 @@ def measure_breakdown(w, runners, xs):
     pass's two medians, the fixed time the second median. Returns samples
     for the step-time model, per-pass times and the calls' requested bytes."""
     samples = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
+    uniq = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     tfix = {n: [] for n in w.pass_sizes}
     pass_ms = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     import torch
@@ -271,6 +278,7 @@ def measure_breakdown(w, runners, xs):
                 R = runners[li]
                 R.forward(xs[n][q], eng, stream)
                 reqs.append(requested(R, eng))
+                uniq[eng][n].append(unique_bytes(R))
 
             def one(s, li, q, with_expert):
                 R, x = runners[li], xs[n][q]
@@ -288,7 +296,7 @@ def measure_breakdown(w, runners, xs):
                 pass_ms[eng][n].append(ta[i] * 1e3)
             del ga, gb
     t_fix = {n: statistics.median(v) for n, v in tfix.items()}
-    return samples, t_fix, pass_ms
+    return samples, t_fix, pass_ms, uniq
 
 
 FUSED_PASSES = 4   # passes per (pass size, engine) in the fused-combine comparison
@@ -499,14 +507,19 @@ def load_dram_record(workload: str, check_hash: bool = True):
     return out
 
 
-def dram_ratio(workload: str, rho: float):
-    """DRAM bytes over requested bytes per (engine, n) from the record, when
-    it was taken at this rho on the current sources; else None."""
+def dram_factor(workload: str):
+    """DRAM bytes of an expert call over its pass's unique expert bytes (the
+    union's, |U|·E_b + s·E_b, which is what the dedup engine requests), per
+    engine and pass size, from the record, when it was taken on the current
+    sources; else None. Both engines read each distinct expert of a pass
+    from DRAM about once — the per-slot engine runs the slots of one expert
+    side by side, so L2 serves the repeats — so the factor is near 1 and
+    does not depend on the routing; the record's rho is stated beside it."""
     rec = load_dram_record(workload)
-    if rec is None or abs(rec["rho"] - rho) > 1e-9:
+    if rec is None:
         return None
-    return {e: {n: rec[e + "_dram"][i] / rec[e + "_requested"][i] for i, n in enumerate(rec["n"])}
-            for e in ("perslot", "dedup")}
+    return {e: {n: rec[e + "_dram"][i] / rec["dedup_requested"][i]
+                for i, n in enumerate(rec["n"])} for e in ("perslot", "dedup")}
 
 
 def peaks():
@@ -833,6 +846,7 @@ def sweep_workload(name, rhos=None, passes=SWEEP_PASSES):
     out = []
     for rho in (rhos if rhos is not None else w.rhos):
         samples = {e: {n: [] for n in w.pass_sizes} for e in engines}
+        uniq = {e: {n: [] for n in w.pass_sizes} for e in engines}
         tfix = {n: [] for n in w.pass_sizes}
         for n in w.pass_sizes:
             for f in range(passes):
@@ -842,6 +856,7 @@ def sweep_workload(name, rhos=None, passes=SWEEP_PASSES):
                 for eng in engines:
                     R.forward(x, eng, st)
                     req = requested(R, eng)
+                    uniq[eng][n].append(unique_bytes(R))
 
                     def one(s, with_expert):
                         flush.sum()
@@ -869,9 +884,12 @@ def sweep_workload(name, rhos=None, passes=SWEEP_PASSES):
                 "timing": "expert call inside a CUDA-graph-replayed pass behind a 256 MB L2 "
                           "flush (graph with minus graph without the call)",
                 "peak_GBs": peak}
-        ratio = dram_ratio(name, rho)
+        fac = dram_factor(name)
         for eng in engines:
             gbs = [bw[eng][n] / 1e9 for n in ns]
+            f = [fac[eng].get(n * w.streams) if fac else None for n in ns]
+            dram = [None if fn is None else sum(uniq[eng][n]) * fn /
+                    sum(t for _, t in samples[eng][n]) / 1e9 for n, fn in zip(ns, f)]
             line[eng] = {
                 "requested_MB": [round(sum(b for b, _ in samples[eng][n]) / len(samples[eng][n])
                                        / 1e6, 1) for n in ns],
@@ -879,15 +897,12 @@ def sweep_workload(name, rhos=None, passes=SWEEP_PASSES):
                                     * 1e6, 2) for n in ns],
                 "GBs": [round(g, 1) for g in gbs],
                 "frac_of_peak": [round(g / peak, 3) for g in gbs],
-                "dram_GBs": ([round(g * ratio[eng][n * w.streams], 1)
-                              if n * w.streams in ratio[eng] else None
-                              for g, n in zip(gbs, ns)] if ratio else None)}
-            if ratio:
-                line[eng]["dram_frac_of_peak"] = [None if v is None else round(v / peak, 3)
-                                                  for v in line[eng]["dram_GBs"]]
-        line["dram_source"] = (os.path.relpath(dram_record_path(name), ROOT) + " (DRAM/requested "
-                               "bytes of one call per n at this rho, scaled by this run's requested "
-                               "bytes)") if ratio else "no capture at this rho on these sources"
+                "dram_GBs": [None if v is None else round(v, 1) for v in dram],
+                "dram_frac_of_peak": [None if v is None else round(v / peak, 3) for v in dram]}
+        line["dram_source"] = (os.path.relpath(dram_record_path(name), ROOT) + ": DRAM bytes = "
+                               "each pass's unique expert bytes x the factor ncu measured per "
+                               "engine and n on one call (rho %s)" % load_dram_record(name)["rho"]
+                               if fac else "no capture on these sources")
         line.update({"u_bar": [round(u[n], 6) for n in ns], "r": [round(r[n], 6) for n in ns],
                      "crossover_n": stepmodel.crossover(ns, u, r),
                      "t_fix_us": [round(statistics.median(tfix[n]) * 1e6, 2) for n in ns]})
@@ -964,7 +979,7 @@ def run_ours(args):
         raise RuntimeError("device error in the timed region: %s" % api.status_str(st))
 
     # per-call breakdown on the stack's layers (outside the timed region)
-    samples, t_fix, pass_ms = measure_breakdown(w, runners, xs)
+    samples, t_fix, pass_ms, uniq = measure_breakdown(w, runners, xs)
     rep = stepmodel.build_report(samples, t_fix, layers=len(runners))
     fused = measure_fused(w, runners, xs)
     e2e_ms, h2d, d2h = e2e_measure(w, runners, xs, max(3, args.steps // 2), 3)
@@ -986,12 +1001,14 @@ def run_ours(args):
     peak, peak_kind = peaks()
     ns = list(w.pass_sizes)
     sh = w.shape
-    ratio = dram_ratio("v2lite", HEADLINE_RHO)
+    fac = dram_factor("v2lite")
     per_engine = {}
     req_b, dram_b, call_s, ncalls = 0.0, 0.0, 0.0, 0
     for eng in ("perslot", "dedup"):
         gbs = [sum(b for b, _ in samples[eng][n]) / sum(s for _, s in samples[eng][n]) / 1e9
                for n in ns]
+        dram = ([sum(uniq[eng][n]) * fac[eng][n] / sum(s for _, s in samples[eng][n]) / 1e9
+                 for n in ns] if fac else None)
         per_engine[eng] = {
             "tokens_per_s_one_layer": [round(n / (statistics.median(pass_ms[eng][n]) * 1e-3), 1)
                                        for n in ns],
@@ -1002,20 +1019,19 @@ def run_ours(args):
                                    1) for n in ns],
             "expert_GBs": [round(g, 1) for g in gbs],
             "expert_frac_of_peak": [round(g / peak, 3) for g in gbs],
-            "dram_GBs": [round(g * ratio[eng][n], 1) for g, n in zip(gbs, ns)] if ratio else None,
+            "dram_GBs": [round(g, 1) for g in dram] if dram else None,
         }
-        if ratio:
-            per_engine[eng]["dram_frac_of_peak"] = [round(v / peak, 3)
-                                                    for v in per_engine[eng]["dram_GBs"]]
+        if dram:
+            per_engine[eng]["dram_frac_of_peak"] = [round(v / peak, 3) for v in dram]
         for n in ns:
             act = n * sh.d * 4 + n * (sh.top_k + sh.n_shared) * sh.d * 4
-            for b, s in samples[eng][n]:
+            for (b, s), u in zip(samples[eng][n], uniq[eng][n]):
                 req_b += b + act
-                dram_b += b * (ratio[eng][n] if ratio else float("nan")) + act
+                dram_b += (u * fac[eng][n] if fac else float("nan")) + act
                 call_s += s
                 ncalls += 1
     achieved = req_b / call_s / 1e9
-    achieved_dram = dram_b / call_s / 1e9 if ratio else None
+    achieved_dram = dram_b / call_s / 1e9 if fac else None
     cpu = None if args.no_cpu_baseline else cpu_baseline_sample()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -1042,9 +1058,11 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "achieved_dram": None if achieved_dram is None else round(achieved_dram, 1),
                      "frac_dram": None if achieved_dram is None else round(achieved_dram / peak, 4),
-                     "traffic": None if not ratio else int(round(dram_b / ncalls)),
-                     "traffic_source": (os.path.relpath(dram_record_path("v2lite"), ROOT)
-                                        if ratio else "no capture on these sources"),
+                     "traffic": None if not fac else int(round(dram_b / ncalls)),
+                     "traffic_source": (os.path.relpath(dram_record_path("v2lite"), ROOT) +
+                                        ": DRAM bytes per call = the pass's unique expert bytes "
+                                        "x the factor ncu measured per engine and n (1.000-1.021)"
+                                        if fac else "no capture on these sources"),
                      "calls": ncalls, "call_us_mean": round(call_s / ncalls * 1e6, 2)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_value(world, tokens_per_step, e2e_ms), 2), "unit": UNIT,
@@ -1254,8 +1272,9 @@ def run_dram_record(args):
     with open(path, "w") as f:
         f.write("# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one expert call per\n"
                 "# pass size and engine, %s-shaped layer, rho = %s, each call a cold pass of its own\n"
-                "# (routing differs from the bench's passes, so bench.py uses only the ratio of DRAM\n"
-                "# to requested bytes, per engine and n, and scales its own requested bytes by it).\n"
+                "# (routing differs from the bench's passes, so bench.py uses the ratio of DRAM bytes\n"
+                "# to the pass's unique expert bytes, per engine and n, and scales each of its own\n"
+                "# passes' unique bytes by it).\n"
                 "# Used only while sources_sha256_16 matches the code of the kernel sources\n"
                 "# (bench.kernel_source_hash()).\n#\n"
                 "# Command (GB300, after the same command exited 0 without ncu):\n"

@@ -49,12 +49,12 @@ def test_dram_record_round_trip(tmp_path, monkeypatch):
     assert rec["perslot_requested"] == [1000, 2000, 3000]
     assert rec["perslot_dram"] == [703, 1403, 2103]
     assert rec["dedup_dram"] == [904, 904, 904]
-    r = bench.dram_ratio("v2lite", 0.9)
-    assert r["perslot"][2] == pytest.approx(1403 / 2000)
-    assert bench.dram_ratio("v2lite", 0.5) is None            # taken at another rho
+    f = bench.dram_factor("v2lite")
+    assert f["perslot"][2] == pytest.approx(1403 / 900)       # over the pass's unique bytes
+    assert f["dedup"][3] == pytest.approx(904 / 900)
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
     assert bench.load_dram_record("v2lite") is None           # other kernel sources
-    assert bench.dram_ratio("v2lite", 0.9) is None
+    assert bench.dram_factor("v2lite") is None
 
 
 def test_dram_record_refuses_a_launch_count_mismatch(tmp_path, monkeypatch):
