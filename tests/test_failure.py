@@ -42,3 +42,37 @@ def test_bounded_wait_rejects_limits_out_of_range():
     lib = api.load()
     assert lib.moe_diag_bounded_wait(0, None) == api.MOE_EINVAL
     assert lib.moe_diag_bounded_wait(2_000_000, None) == api.MOE_EINVAL
+
+
+def test_expert_index_out_of_range_is_reported_not_read():
+    """A per-slot call given an expert index outside [0, E) (a caller's bug):
+    the kernel's own check records it and reads expert 0 instead, so nothing
+    is read out of bounds; moe_last_device_error reports MOE_EDEVICE, and the
+    next pass is correct."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from moe_expert_layer_warp_gb300 import api, build, synth
+    from moe_expert_layer_warp_gb300.configs import LayerShape, W_BF16
+    from moe_expert_layer_warp_gb300.layer import PassRunner
+    from oracle import oracle
+    build.build()
+    assert api.moe_last_device_error() == api.MOE_OK
+    shape = LayerShape(576, 16, 4, 320, 1, W_BF16)
+    L = synth.make_layer(shape, 13, "cuda")
+    n = 5
+    R = PassRunner(L, n)
+    x_np = synth.make_pass(shape.d, n, 0.9, [77])
+    x = torch.from_numpy(x_np).cuda()
+    R.route_union(x)
+    R.topk_idx[3] = shape.n_experts + 83                     # not an expert of this layer
+    R.experts(x, "perslot")
+    assert api.moe_last_device_error() == api.MOE_EDEVICE
+    assert api.moe_last_device_error() == api.MOE_OK          # the word was cleared
+    y = R.forward(x, "perslot").cpu().numpy()
+    assert api.moe_last_device_error() == api.MOE_OK
+    r = oracle.route(x_np, L.w_router.cpu().numpy(), shape.top_k)
+    y_o = oracle.moe_tokens(x_np, r["idx"], r["w"], synth.weights_numpy(L.w_gate),
+                            synth.weights_numpy(L.w_up), synth.weights_numpy(L.w_down),
+                            synth.weights_numpy(L.ws_gate), synth.weights_numpy(L.ws_up),
+                            synth.weights_numpy(L.ws_down))
+    assert np.max(np.abs(y - y_o)) <= 2e-2 * np.sqrt(np.mean(y_o ** 2))
