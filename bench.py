@@ -259,11 +259,12 @@ def measure_breakdown(w, runners, xs):
     """The expert call's time inside a pipelined pass, per pass size and
     engine, on the stack's layers. Each of BREAKDOWN_PASSES passes (pass i on
     layer i, so consecutive passes read different weights) is captured twice
-    as a CUDA graph: route, union, expert call, combine — and the same
-    without the expert call. The graphs are replayed round-robin between
-    CUDA events on the stream; the expert call's time is the difference of a
-    pass's two medians, the fixed time the second median. Returns samples
-    for the step-time model, per-pass times and the calls' requested bytes."""
+    as a CUDA graph: the whole pass (one moe_verify_pass: route, union,
+    expert call, combine) — and its routing, union and combine alone. The
+    graphs are replayed round-robin between CUDA events on the stream; the
+    expert call's time is the difference of a pass's two medians, the fixed
+    time the second median. Returns samples for the step-time model,
+    per-pass times and the calls' requested bytes."""
     samples = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     uniq = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     tfix = {n: [] for n in w.pass_sizes}
@@ -282,10 +283,11 @@ def measure_breakdown(w, runners, xs):
 
             def one(s, li, q, with_expert):
                 R, x = runners[li], xs[n][q]
-                R.route_union(x, s)
-                if with_expert:
-                    R.experts(x, eng, s)
-                R.combine(n, s)
+                if with_expert:          # the whole pass, as the user calls it
+                    R.forward(x, eng, s)
+                else:                    # its fixed part: routing, union and combine
+                    R.route_union(x, s)
+                    R.combine(n, s)
             ga = [capture_graph(lambda s, li=li, q=q: one(s, li, q, True)) for li, q in plan]
             gb = [capture_graph(lambda s, li=li, q=q: one(s, li, q, False)) for li, q in plan]
             t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
@@ -706,10 +708,11 @@ def stack_check(w, runners, dev):
 
                 def one(s, x, with_expert):
                     flush.sum()
-                    R0.route_union(x, s)
                     if with_expert:
-                        R0.experts(x, eng, s)
-                    R0.combine(n, s)
+                        R0.forward(x, eng, s)
+                    else:
+                        R0.route_union(x, s)
+                        R0.combine(n, s)
                 ga = [capture_graph(lambda s, x=x: one(s, x, True)) for x in fit_xs[(ri, n)]]
                 gb = [capture_graph(lambda s, x=x: one(s, x, False)) for x in fit_xs[(ri, n)]]
                 t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
@@ -860,10 +863,11 @@ def sweep_workload(name, rhos=None, passes=SWEEP_PASSES):
 
                     def one(s, with_expert):
                         flush.sum()
-                        R.route_union(x, s)
                         if with_expert:
-                            R.experts(x, eng, s)
-                        R.combine(m, s)
+                            R.forward(x, eng, s)
+                        else:
+                            R.route_union(x, s)
+                            R.combine(m, s)
                     ga = capture_graph(lambda s: one(s, True))
                     gb = capture_graph(lambda s: one(s, False))
                     ta, tb = time_graphs([ga, gb], 3)
@@ -1167,10 +1171,11 @@ def run_case(args):
 
     def one(s, with_expert):
         flush.sum()
-        R.route_union(x, s)
         if with_expert:
-            R.experts(x, eng, s)
-        R.combine(x.shape[0], s)
+            R.forward(x, eng, s)
+        else:
+            R.route_union(x, s)
+            R.combine(x.shape[0], s)
     ga = capture_graph(lambda s: one(s, True))
     gb = capture_graph(lambda s: one(s, False))
     ta, tb = time_graphs([ga, gb], args.passes)
