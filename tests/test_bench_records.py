@@ -79,3 +79,27 @@ def test_committed_records_are_plausible(workload):
         assert ps_dr <= 1.03 * ps_req, (workload, n, ps_req, ps_dr)
         assert ps_dr >= 0.97 * dd_req, (workload, n)   # the same pass's unique bytes at least
         assert ps_req >= dd_req
+
+
+def test_crossovers_within_one_pass_size():
+    """The stack check's "within one pass size" count: "never" (None) counts
+    as one past the largest measured pass size."""
+    assert bench._within_one(2, 2, 9) and bench._within_one(2, 3, 9)
+    assert not bench._within_one(2, 4, 9)
+    assert bench._within_one(None, 9, 9) and bench._within_one(9, None, 9)
+    assert not bench._within_one(None, 8, 9)
+    assert bench._within_one(None, None, 9)
+
+
+def test_headline_step_plan_covers_both_engines_at_every_pass_size():
+    """One bench step: every pass size once with each engine (18 stack passes,
+    90 tokens), the hidden-state variant alternating by step."""
+    from moe_expert_layer_warp_gb300 import configs
+    w = configs.V2_LITE_STACK
+    for step in range(4):
+        plan = bench.step_plan(w, step)
+        assert sorted((n, e) for n, e, _ in plan) == sorted(
+            (n, e) for n in w.pass_sizes for e in ("perslot", "dedup"))
+        assert {q for _, _, q in plan} == {step % bench.N_PASSES_PER_N}
+    assert sum(n for n, _, _ in bench.step_plan(w, 0)) == 90
+    assert bench.kernels_per_pass() * 2 * len(w.pass_sizes) * w.layers == 2340
