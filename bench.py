@@ -814,6 +814,26 @@ def stack_check(w, runners, dev):
             "summary": summary, "per_rho": per_rho}
 
 
+def best_engine_rate(stack):
+    """Stack tokens/s of a pass at each n = 1..9 with the faster engine at
+    that n, from the stack check's measured 26-layer passes at the headline
+    rho (each a single pass timed between CUDA events, not graph-replayed);
+    None without the stack check."""
+    if not stack:
+        return None
+    for d in stack["per_rho"]:
+        if abs(d["rho"] - HEADLINE_RHO) < 1e-9:
+            ps, dd = d["measured_us"]["perslot"], d["measured_us"]["dedup"]
+            best = [min(a, b) for a, b in zip(ps, dd)]
+            return {"tokens_per_s": round(sum(d["n"]) / (sum(best) * 1e-6), 2),
+                    "engine_by_n": ["dedup" if b < a else "perslot" for a, b in zip(ps, dd)],
+                    "per_slot_only_tokens_per_s": round(sum(d["n"]) / (sum(ps) * 1e-6), 2),
+                    "dedup_only_tokens_per_s": round(sum(d["n"]) / (sum(dd) * 1e-6), 2),
+                    "what": "one stack pass at each n = 1..9 (rho %.2f) with the faster engine at "
+                            "each n, from the stack check's measured passes" % HEADLINE_RHO}
+    return None
+
+
 def _within_one(a, b, n_max):
     """Crossovers within one pass size; "never" (None) counts as n_max + 1."""
     a = n_max + 1 if a is None else a
@@ -1090,6 +1110,7 @@ def run_ours(args):
                                   "expert kernel's last phase (moe_verify_pass_fused)"
                                   % FUSED_PASSES)},
         "stack_check": stack,
+        "best_engine": best_engine_rate(stack),
         "tables": tables,
     }
     print(json.dumps(line), flush=True)

@@ -103,3 +103,15 @@ def test_headline_step_plan_covers_both_engines_at_every_pass_size():
         assert {q for _, _, q in plan} == {step % bench.N_PASSES_PER_N}
     assert sum(n for n, _, _ in bench.step_plan(w, 0)) == 90
     assert bench.kernels_per_pass() * 2 * len(w.pass_sizes) * w.layers == 2340
+
+
+def test_best_engine_rate_takes_the_faster_engine_at_each_n():
+    stack = {"per_rho": [
+        {"rho": 0.5, "n": [1, 2], "measured_us": {"perslot": [1.0, 1.0], "dedup": [1.0, 1.0]}},
+        {"rho": bench.HEADLINE_RHO, "n": [1, 2, 3],
+         "measured_us": {"perslot": [100.0, 300.0, 500.0], "dedup": [110.0, 200.0, 250.0]}}]}
+    r = bench.best_engine_rate(stack)
+    assert r["engine_by_n"] == ["perslot", "dedup", "dedup"]
+    assert r["tokens_per_s"] == pytest.approx(6 / 550e-6, rel=1e-6)
+    assert r["per_slot_only_tokens_per_s"] == pytest.approx(6 / 900e-6, rel=1e-6)
+    assert bench.best_engine_rate(None) is None
