@@ -7,9 +7,11 @@ k = 1, the largest pass (n·k = 512), the most shared experts (4, split into
 sub-groups past 32 tokens), the most experts and largest top-k (256, 16),
 the smallest dimensions (d = I = 64), n = 1 and identical tokens. The five
 workload shapes run at full size in the launch configuration the benchmark
-times: one pass of each of the V2-Lite (n = 9), Mixtral (n = 16, rho = 0) and
-V3 (64 tokens) layers is compared with the oracle on every token, the other
-full-size passes on sampled tokens (routing, union and bytes on every token).
+times and are compared with the oracle on every token — the V2-Lite layer at
+every pass size, two layers of the 26-layer stack, the Mixtral layer at
+n = 1, 2, 8 and 16 (rho = 0) and the V3 layer's 64 tokens — except one
+Mixtral pass (n = 16, rho = 0.9), sampled on its last token (routing, union
+and bytes on every token).
 Both engines are checked, and against each other.
 """
 import gc
@@ -313,14 +315,13 @@ def _workload_pass(w, n, rho, p):
 
 
 def test_v2_lite_layer_full_size():
-    """Every pass size; the largest pass (n = 9) on every token, the others
-    on their first and last tokens."""
+    """Every pass size, every token."""
     w = configs.V2_LITE
     L = synth.make_layer(w.shape, w.weight_seed, "cuda")
     R = PassRunner(L, max(w.pass_sizes))
     for n in w.pass_sizes:
         x = _workload_pass(w, n, w.rhos[0], 0)
-        check_pass(L, x, tokens=None if n == max(w.pass_sizes) else sorted({0, n - 1}), runner=R)
+        check_pass(L, x, runner=R)
     del L, R
     torch.cuda.empty_cache()
 
@@ -329,11 +330,11 @@ def test_mixtral_layer_full_size():
     w = configs.MIXTRAL
     L = synth.make_layer(w.shape, w.weight_seed, "cuda")
     R = PassRunner(L, max(w.pass_sizes))
-    # n = 16 at rho = 0 (the most distinct experts) on every token; the
-    # other passes on their last token
+    # n = 16 at rho = 0 (the most distinct experts) and n <= 8 on every
+    # token; n = 16 at rho = 0.9 on its last token
     for n, rho in [(1, 0.9), (2, 0.0), (8, 0.5), (16, 0.9), (16, 0.0)]:
         x = _workload_pass(w, n, rho, 0)
-        check_pass(L, x, tokens=None if (n, rho) == (16, 0.0) else [n - 1], runner=R)
+        check_pass(L, x, tokens=[n - 1] if (n, rho) == (16, 0.9) else None, runner=R)
     del L, R
     torch.cuda.empty_cache()
 
@@ -354,7 +355,7 @@ def test_v2_lite_stack_layers_full_size():
     for layer in (0, w.layers - 1):
         L = synth.make_layer(w.shape, w.weight_seed + layer, "cuda")
         x = _workload_pass(w, 9, 0.99, 0)
-        check_pass(L, x, tokens=[4])
+        check_pass(L, x)
         del L
         torch.cuda.empty_cache()
 
