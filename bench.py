@@ -198,10 +198,10 @@ def enqueue_step(w, runners, xs, step_idx, stream):
 
 
 def kernels_per_pass():
-    # moe_route_union: gate GEMV + one CTA for top-k and union; expert call:
-    # prep + one expert kernel (tensor-core or CUDA-core, chosen per call);
-    # moe_combine: 1
-    return 2 + 2 + 1
+    # moe_verify_pass: the gate GEMV (which also does the expert call's prep
+    # work), the top-k/union kernel (which also gathers the dedup rows), one
+    # expert kernel (tensor-core or CUDA-core, chosen per call), the combine
+    return 2 + 1 + 1
 
 
 def capture_graph(fn):

@@ -250,10 +250,14 @@ moe_status moe_build_union(const moe_layer_desc* desc, const int32_t* topk_idx, 
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_build_union launch");
 }
 
-moe_status moe_route_union(const moe_layer_desc* desc, const float* w_router, const float* bias,
-                           int32_t bias_in_weights, const float* x, int32_t n,
-                           int32_t* topk_idx, float* topk_w, const moe_union* u, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+moe_status check_route_union(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                             int32_t bias_in_weights, const float* x, int32_t n,
+                             const int32_t* topk_idx, const float* topk_w, const moe_union* u,
+                             const void* workspace, size_t workspace_bytes) {
   MOE_TRY(check_desc(desc));
   if (bias_in_weights != 0 && bias_in_weights != 1) return MOE_EINVAL;
   if (bias && (reinterpret_cast<uintptr_t>(bias) & 3u) != 0) return MOE_EINVAL;
@@ -264,31 +268,61 @@ moe_status moe_route_union(const moe_layer_desc* desc, const float* w_router, co
       !u->bytes)
     return MOE_EINVAL;
   if ((reinterpret_cast<uintptr_t>(u->bytes) & 7u) != 0) return MOE_EINVAL;
-  MOE_TRY(check_ws(desc, n, workspace, workspace_bytes));
-  DeviceInfo* di;
-  MOE_TRY(device_info(&di));
+  return check_ws(desc, n, workspace, workspace_bytes);
+}
+
+// Routing and union (arguments already checked); prep: null, or the pass's
+// prep work done by the routing kernels.
+moe_status launch_route_union(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                              int32_t bias_in_weights, const float* x, int32_t n,
+                              int32_t* topk_idx, float* topk_w, const moe_union* u,
+                              void* workspace, const moe::PassPrep* prep, void* stream) {
   WsLayout L = ws_layout(desc, n);
   float* logits = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.logits);
   cudaError_t e = moe::launch_route_union(
       desc->d, desc->inter, desc->n_experts, desc->top_k, desc->n_shared,
       desc->wdtype == MOE_W_F32 ? 4 : 2, n, x, w_router, bias, bias_in_weights, logits, topk_idx,
-      topk_w, u->union_ids, u->union_count, u->offsets, u->pair_tok, u->pair_slot, u->bytes,
+      topk_w, u->union_ids, u->union_count, u->offsets, u->pair_tok, u->pair_slot, u->bytes, prep,
       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_route_union launch");
 }
 
-// One expert-engine call; y non-null fuses the combine into the down epilogue.
-static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_layer_weights* w,
-                             const float* x, int32_t n, const int32_t* topk_idx,
-                             const moe_union* u, const float* topk_w, void* workspace,
-                             size_t workspace_bytes, float* y_slot, float* y, void* stream) {
+}  // namespace
+
+extern "C" {
+
+moe_status moe_route_union(const moe_layer_desc* desc, const float* w_router, const float* bias,
+                           int32_t bias_in_weights, const float* x, int32_t n,
+                           int32_t* topk_idx, float* topk_w, const moe_union* u, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  MOE_TRY(check_route_union(desc, w_router, bias, bias_in_weights, x, n, topk_idx, topk_w, u,
+                            workspace, workspace_bytes));
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  return launch_route_union(desc, w_router, bias, bias_in_weights, x, n, topk_idx, topk_w, u,
+                            workspace, nullptr, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+moe_status check_engine(const moe_layer_desc* desc, const moe_layer_weights* w, const float* x,
+                        int32_t n, const float* topk_w, const void* workspace,
+                        size_t workspace_bytes, const float* y_slot) {
   MOE_TRY(check_desc(desc));
   MOE_TRY(check_n(desc, n));
   MOE_TRY(check_weights(desc, w));
   if (!x || !topk_w || !y_slot || !aligned16(x)) return MOE_EINVAL;
-  MOE_TRY(check_ws(desc, n, workspace, workspace_bytes));
-  DeviceInfo* di;
-  MOE_TRY(device_info(&di));
+  return check_ws(desc, n, workspace, workspace_bytes);
+}
+
+// The arguments of one expert-engine call (already checked); y non-null
+// fuses the combine into the expert kernel's last phase.
+moe::ExpertArgs expert_args(int engine, const moe_layer_desc* desc, const moe_layer_weights* w,
+                            const float* x, int32_t n, const int32_t* topk_idx,
+                            const moe_union* u, const float* topk_w, void* workspace,
+                            float* y_slot, float* y, const DeviceInfo* di) {
   WsLayout L = ws_layout(desc, n);
   moe::ExpertArgs a;
   memset(&a, 0, sizeof a);
@@ -342,11 +376,27 @@ static moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_l
   // calls and dedup calls, which repeat no expert, by 0.4-3 %.
   a.keep_weights = engine == 0 && n >= 3 ? 1 : 0;
   a.err = di->err;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = moe::launch_expert_engine(a, di->num_sms, s);
+  return a;
+}
+
+// One expert-engine call with its own prep kernel.
+moe_status run_engine(int engine, const moe_layer_desc* desc, const moe_layer_weights* w,
+                      const float* x, int32_t n, const int32_t* topk_idx, const moe_union* u,
+                      const float* topk_w, void* workspace, size_t workspace_bytes,
+                      float* y_slot, void* stream) {
+  MOE_TRY(check_engine(desc, w, x, n, topk_w, workspace, workspace_bytes, y_slot));
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  const moe::ExpertArgs a =
+      expert_args(engine, desc, w, x, n, topk_idx, u, topk_w, workspace, y_slot, nullptr, di);
+  cudaError_t e = moe::launch_expert_engine(a, di->num_sms, false, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "expert engine launch");
   return MOE_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 moe_status moe_verify_perslot(const moe_layer_desc* desc, const moe_layer_weights* weights,
                               const float* x, int32_t n, const int32_t* topk_idx,
@@ -354,7 +404,7 @@ moe_status moe_verify_perslot(const moe_layer_desc* desc, const moe_layer_weight
                               float* y_slot, void* stream) {
   if (!topk_idx) return MOE_EINVAL;
   return run_engine(0, desc, weights, x, n, topk_idx, nullptr, topk_w, workspace,
-                    workspace_bytes, y_slot, nullptr, stream);
+                    workspace_bytes, y_slot, stream);
 }
 
 moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights* weights,
@@ -364,7 +414,7 @@ moe_status moe_verify_dedup(const moe_layer_desc* desc, const moe_layer_weights*
   if (!u || !u->union_ids || !u->union_count || !u->offsets || !u->pair_tok || !u->pair_slot)
     return MOE_EINVAL;
   return run_engine(1, desc, weights, x, n, nullptr, u, topk_w, workspace, workspace_bytes,
-                    y_slot, nullptr, stream);
+                    y_slot, stream);
 }
 
 // ------------------------------------------------ allocation-free variant --
@@ -456,6 +506,8 @@ moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t 
 
 // A whole pass: routing and union, one engine, and the combine either as a
 // launch of its own (fused = false) or as the expert kernel's last phase.
+// The routing kernels also do the expert call's prep work (PassPrep), so
+// that the expert kernel follows them directly.
 static moe_status verify_pass(bool fused, const moe_layer_desc* desc,
                               const moe_layer_weights* weights, const float* bias,
                               int32_t bias_in_weights, const float* x, int32_t n, int32_t engine,
@@ -465,16 +517,35 @@ static moe_status verify_pass(bool fused, const moe_layer_desc* desc,
   if (!weights || !y_slot || !y || (engine != MOE_ENGINE_PERSLOT && engine != MOE_ENGINE_DEDUP))
     return MOE_EINVAL;
   if (!aligned16(y_slot) || !aligned16(y)) return MOE_EINVAL;
-  MOE_TRY(moe_route_union(desc, weights->w_router, bias, bias_in_weights, x, n, topk_idx, topk_w, u,
-                          workspace, workspace_bytes, stream));
-  float* y_fused = fused ? y : nullptr;
-  if (engine == MOE_ENGINE_PERSLOT) {
-    MOE_TRY(run_engine(0, desc, weights, x, n, topk_idx, nullptr, topk_w, workspace,
-                       workspace_bytes, y_slot, y_fused, stream));
-  } else {
-    MOE_TRY(run_engine(1, desc, weights, x, n, nullptr, u, topk_w, workspace, workspace_bytes,
-                       y_slot, y_fused, stream));
+  MOE_TRY(check_route_union(desc, weights->w_router, bias, bias_in_weights, x, n, topk_idx, topk_w,
+                            u, workspace, workspace_bytes));
+  MOE_TRY(check_engine(desc, weights, x, n, topk_w, workspace, workspace_bytes, y_slot));
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  const int eng = engine == MOE_ENGINE_PERSLOT ? 0 : 1;
+  const moe::ExpertArgs a =
+      expert_args(eng, desc, weights, x, n, eng == 0 ? topk_idx : nullptr, eng == 1 ? u : nullptr,
+                  topk_w, workspace, y_slot, fused ? y : nullptr, di);
+  const bool bf16 = desc->wdtype == MOE_W_BF16;
+  moe::PassPrep pp;
+  memset(&pp, 0, sizeof pp);
+  pp.x32 = a.x32;
+  pp.x16 = bf16 ? a.x16 : nullptr;
+  pp.x16lo = bf16 ? a.x16lo : nullptr;
+  pp.sync_cc = a.sync;
+  pp.sync_mma = a.sync_mma;
+  pp.ydone = a.y ? a.ydone : nullptr;
+  if (eng == 1) {
+    pp.xg = a.xg;
+    pp.xg16 = bf16 ? a.xg16 : nullptr;
+    pp.xg16lo = bf16 ? a.xg16lo : nullptr;
+    const int pairs = n * desc->top_k;
+    pp.gather_rows = (pairs + di->num_sms - 1) / di->num_sms;
   }
+  MOE_TRY(launch_route_union(desc, weights->w_router, bias, bias_in_weights, x, n, topk_idx, topk_w,
+                             u, workspace, &pp, stream));
+  cudaError_t e = moe::launch_expert_engine(a, di->num_sms, true, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "expert engine launch");
   return fused ? MOE_OK : moe_combine(desc, y_slot, n, y, stream);
 }
 

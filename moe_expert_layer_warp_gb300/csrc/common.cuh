@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -150,21 +151,6 @@ MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int 
       : "memory");
 }
 
-// Prefetch of a tensor-map box into L2 (no shared memory, no completion).
-MOE_DEV void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
-MOE_DEV void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-
 MOE_DEV void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                          uint64_t* bar, uint64_t policy) {
   asm volatile(
@@ -201,6 +187,20 @@ MOE_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::
 // ---------------------------------------------------------- small utils --
 MOE_DEV float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 MOE_DEV float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Four fp32 values as bf16 hi/lo halves: hi = bf16(v), lo = bf16(v − hi),
+// so hi + lo holds v to about 16 more mantissa bits than hi alone.
+MOE_DEV void split_bf16x4(float4 v, uint2* hi, uint2* lo) {
+  const uint2 h = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  *hi = h;
+  *lo = make_uint2(pack_bf16x2(v.x - bf16lo(h.x), v.y - bf16hi(h.x)),
+                   pack_bf16x2(v.z - bf16lo(h.y), v.w - bf16hi(h.y)));
+}
 
 MOE_DEV float warp_sum(float v) {
 #pragma unroll

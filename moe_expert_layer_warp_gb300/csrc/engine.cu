@@ -10,11 +10,6 @@
 namespace moe {
 namespace {
 
-MOE_DEV uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // Runs right before the expert kernels and lets them launch as soon as it
 // starts (programmatic dependent launch); they wait for it before touching
 // its outputs. The grid zeroes both kernels' job counters and group counts,
@@ -61,24 +56,22 @@ __global__ void __launch_bounds__(256)
   for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
     const float4 v = __ldg(reinterpret_cast<const float4*>(src) + i);
     reinterpret_cast<float4*>(dst32)[i] = v;
-    if (!hi) continue;
-    const uint2 h = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-    const uint2 l = make_uint2(pack_bf16x2(v.x - bf16lo(h.x), v.y - bf16hi(h.x)),
-                               pack_bf16x2(v.z - bf16lo(h.y), v.w - bf16hi(h.y)));
-    reinterpret_cast<uint2*>(hi)[i] = h;
-    reinterpret_cast<uint2*>(lo)[i] = l;
+    if (hi) split_bf16x4(v, reinterpret_cast<uint2*>(hi) + i, reinterpret_cast<uint2*>(lo) + i);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream) {
-  const int gather = a.engine == 1 ? a.n * a.k : 0;
-  cudaError_t e = launch_pdl(engine_prep_kernel, dim3(max(gather + a.n, 4)), dim3(256), 0, stream,
-                             a.d, a.n, gather, a.wdtype == 1 ? 1 : 0, a.x, a.pair_tok, a.xg,
-                             a.xg16, a.xg16lo, a.x32, a.x16, a.x16lo, a.sync, a.sync_mma,
-                             a.y ? a.ydone : nullptr);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, bool prepped,
+                                 cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (!prepped) {
+    const int gather = a.engine == 1 ? a.n * a.k : 0;
+    e = launch_pdl(engine_prep_kernel, dim3(max(gather + a.n, 4)), dim3(256), 0, stream, a.d, a.n,
+                   gather, a.wdtype == 1 ? 1 : 0, a.x, a.pair_tok, a.xg, a.xg16, a.xg16lo, a.x32,
+                   a.x16, a.x16lo, a.sync, a.sync_mma, a.y ? a.ydone : nullptr);
+    if (e != cudaSuccess) return e;
+  }
   // The tensor-core kernel runs only where a group can reach mma_min_m
   // tokens: a group never holds more than the pass's n tokens, and per-slot
   // routed groups hold one. The CUDA-core kernel runs unless every group

@@ -155,6 +155,10 @@ MOE_DEV Cut make_cut(int T, int nks, int tiles, int target, size_t budget, size_
 
 MOE_DEV uint16_t to_bf16(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
+static_assert(MOE_MAX_EXPERTS <= kThreads && MOE_MAX_PAIRS <= 2 * kThreads,
+              "build_plan: one thread per expert, two pairs per thread");
+static_assert(kMaxRows >= 2 * MOE_MAX_EXPERTS, "build_plan: row_w holds its sort scratch");
+
 __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_constant__ Params prm) {
   const ExpertArgs& a = prm.a;
   extern __shared__ unsigned char smem_raw[];
@@ -221,16 +225,20 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     prefetch_tmap(&prm.maps.b[0][kXA]);
     prefetch_tmap(&prm.maps.b[0][kHH]);
   }
-  const int n_groups = build_plan<kSub, true>(a, plan, row_out, row_w, misc);
-  __syncthreads();
-  for (int i = threadIdx.x; i < n_groups; i += blockDim.x) atomicMax(max_m, plan[i].m);
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
-  pdl_wait();     // prep kernel's outputs
+  // The kernel before this one — the prep kernel, or the top-k/union kernel
+  // of a whole pass — has written the routing, the union and the rows this
+  // kernel reads, and zeroed its counters.
+  pdl_wait();
   // The CUDA-core kernel, if it runs, may start now on SMs this kernel leaves
-  // free: it needs nothing from this kernel, and the prep kernel is complete.
+  // free: it needs nothing from this kernel, and its inputs are complete.
   pdl_trigger();
+  const int n_groups = build_plan<kSub, true>(a, plan, row_out, row_w, misc);
+  __syncthreads();
+  for (int i = threadIdx.x; i < n_groups; i += blockDim.x) atomicMax(max_m, plan[i].m);
+  __syncthreads();
   const uint32_t tmem = *tmem_base;
 
   // Partial sums: slabs of [npad tokens][128 A rows] fp32 (phase 0: 64 gate

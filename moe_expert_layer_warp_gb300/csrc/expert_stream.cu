@@ -19,9 +19,8 @@
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
 // Phase 0 computes h = silu(W_gate x) ⊙ (W_up x) in tiles of 32 rows of I;
 // phase 1 computes y_slot = w · (W_down h) in tiles of 64 rows of d. A job is
-// (sub-group, tile); CTA b's first job is job b (its first weight stages are
-// prefetched into L2 while the prep kernel still runs), after which the
-// producer thread of each CTA takes the next job from a global counter. The
+// (sub-group, tile); CTA b's first job is job b, after which the producer
+// thread of each CTA takes the next job from a global counter. The
 // sub-groups of one group take consecutive jobs tile by tile, so that L2
 // serves their repeated weight tiles.
 //
@@ -147,6 +146,10 @@ struct LaneMap<4> {
   }
 };
 
+static_assert(MOE_MAX_EXPERTS <= kThreads && MOE_MAX_PAIRS <= 2 * kThreads,
+              "build_plan: one thread per expert, two pairs per thread");
+static_assert(kMaxRows >= 2 * MOE_MAX_EXPERTS, "build_plan: row_w holds its sort scratch");
+
 // One launch runs both phases. Jobs 0 .. J0-1 are phase-0 jobs (group-major),
 // jobs J0 .. J0+J1-1 phase-1 jobs (group-major); the producer thread of each
 // CTA takes the next job from a global counter, so every job taken belongs to
@@ -194,40 +197,16 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     prefetch_tmap(&prm.maps.w2);
     prefetch_tmap(&prm.maps.a1);
   }
-  const int n_groups = build_plan<kMaxM, false>(a, plan, row_out, row_w, misc);
-  __syncthreads();
-  // Each CTA's first job is job blockIdx.x. Its weights need nothing from
-  // the prep kernel, so while that kernel runs the producer prefetches the
-  // first kStages stages of a phase-0 first job into L2 (measured on the
-  // DeepSeek-V2-Lite-shaped layer: 1.0-1.3 us off one-token passes; issuing
-  // the loads themselves that early, or prefetching the whole job, was
-  // slower: the weight traffic then delays the prep kernel).
-  if (threadIdx.x == kConsumerWarps * 32 && a.cc_waits_prep &&
-      (int)blockIdx.x < n_groups * (a.I / kRowsPhase0)) {
-    int g, tile;
-    job_entry(plan, (int)blockIdx.x, a.I / kRowsPhase0, &g, &tile);
-    const Entry en = plan[g];
-    const bool shared_expert = en.src < 0;
-    const int ecoord = shared_expert ? -en.src - 1 : en.src;
-    const int nks = min((a.d + KS - 1) / KS, kStages);
-    for (int ks = 0; ks < nks; ++ks) {
-      if (shared_expert ? prm.maps.spair : prm.maps.pair) {
-        tma_prefetch_4d(shared_expert ? &prm.maps.sgu : &prm.maps.gu, ks * KS,
-                        tile * kRowsPhase0, ecoord, 0);
-      } else {
-        tma_prefetch_3d(shared_expert ? &prm.maps.sw0 : &prm.maps.w0, ks * KS,
-                        tile * kRowsPhase0, ecoord);
-        tma_prefetch_3d(shared_expert ? &prm.maps.sw1 : &prm.maps.w1, ks * KS,
-                        tile * kRowsPhase0, ecoord);
-      }
-    }
-  }
-  // The prep kernel (counters zeroed, rows gathered) must be complete. When
-  // this kernel follows the tensor-core kernel, that kernel released it only
-  // after its own wait on the prep kernel, so this kernel starts at once and
-  // waits for the tensor-core kernel only before it exits (below).
+  // The kernel before this one — the prep kernel, or the top-k/union kernel
+  // of a whole pass — must be complete: it wrote the routing, the union and
+  // the rows this kernel reads, and zeroed its counters. When this kernel
+  // follows the tensor-core kernel, that kernel released it only after its
+  // own wait, so this kernel starts at once and waits for the tensor-core
+  // kernel only before it exits (below).
   if (a.cc_waits_prep) pdl_wait();
   pdl_trigger();
+  const int n_groups = build_plan<kMaxM, false>(a, plan, row_out, row_w, misc);
+  __syncthreads();
 
   const int T0 = a.I / kRowsPhase0, T1 = a.d / kRowsPhase1;
   const int J0 = n_groups * T0, J = J0 + n_groups * T1;
@@ -248,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      // the first job is blockIdx.x (prefetched above); the counter hands
+      // the first job is blockIdx.x; the counter hands
       // out jobs gridDim.x, gridDim.x + 1, … after it
       for (bool first = true; ok; first = false) {
         int job = first ? min((int)blockIdx.x, J) : atomicAdd(job_counter, 1) + (int)gridDim.x;

@@ -41,14 +41,37 @@ cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
                          int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
                          uint64_t* bytes, unsigned int* err, cudaStream_t stream);
 
-// Routing and union in two launches: the gate GEMV, then one CTA that runs
-// the top-k of every token and builds the union from its own selection.
+// What the expert call's prep kernel does, done instead by the routing
+// kernels of a whole pass (moe_verify_pass), so that the expert kernel
+// directly follows the routing. The gate kernel zeroes the expert kernels'
+// counters (and ydone, when not null) and writes x32 = x and, when x16 is
+// not null, x's bf16 hi/lo halves (x16, x16lo); with xg not null the
+// top-k/union kernel also gathers the dedup rows: xg[r] = x[pair_tok[r]]
+// and their bf16 hi/lo halves (xg16, xg16lo), in union order.
+struct PassPrep {
+  float* x32;
+  uint16_t* x16;
+  uint16_t* x16lo;
+  int* sync_cc;
+  int* sync_mma;
+  int* ydone;
+  float* xg;
+  uint16_t* xg16;
+  uint16_t* xg16lo;
+  int gather_rows;  // union rows gathered per top-k/union CTA (≥ 1 when xg is not null)
+};
+
+// Routing and union in two launches: the gate GEMV, then the top-k of every
+// token and the union built from that selection (one CTA; or, when prep
+// gathers dedup rows, one CTA per prep->gather_rows rows, each computing the
+// same selection and union, CTA 0 writing them out). prep: null, or the
+// pass's prep work (above).
 cudaError_t launch_route_union(int d, int I, int E, int k, int s, int wbytes, int n,
                                const float* x, const float* w_router, const float* bias,
                                int bias_in_weights, float* logits, int32_t* topk_idx,
                                float* topk_w, int32_t* union_ids, int32_t* union_count,
                                int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
-                               uint64_t* bytes, cudaStream_t stream);
+                               uint64_t* bytes, const PassPrep* prep, cudaStream_t stream);
 
 // Everything the expert kernels read. h is the SwiGLU activation scratch,
 // one fp32 row of length I per (pair or shared-expert token) row.
@@ -86,7 +109,8 @@ struct ExpertArgs {
   float* part;          // [part_bytes] tensor-core kernel's partial sums of jobs cut along K
   size_t part_bytes;
   int mma_min_m;        // groups with at least this many tokens run on tensor cores
-  int cc_waits_prep;    // 1: the CUDA-core kernel directly follows the prep kernel
+  int cc_waits_prep;    // 1: the CUDA-core kernel directly follows the prep kernel (or the
+                        //   pass's top-k/union kernel), not the tensor-core kernel
   int keep_weights;     // 1: weight loads use normal L2 eviction (per-slot calls of 3+ tokens,
                         //   whose repeated experts L2 can serve), else evict-first
   float* y_slot;
@@ -97,8 +121,10 @@ struct ExpertArgs {
 
 // The expert engine of one call: a prep kernel (counters zeroed, rows
 // gathered and rounded for the tensor cores), the tensor-core kernel (bf16
-// weights only) and the CUDA-core kernel.
-cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, cudaStream_t stream);
+// weights only) and the CUDA-core kernel. prepped: the routing kernels just
+// before did the prep work (PassPrep), so no prep kernel runs.
+cudaError_t launch_expert_engine(const ExpertArgs& a, int num_sms, bool prepped,
+                                 cudaStream_t stream);
 
 // Expert FFNs of the groups below mma_min_m tokens on CUDA cores in one
 // persistent launch, weights streamed through a ring of shared-memory stages

@@ -81,14 +81,16 @@ MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
   }
   if (lane == 31) scratch[warp] = inc;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int w = 0; w < nwarps; ++w) {
-      const int c = scratch[w];
-      scratch[w] = run;
-      run += c;
+  if (warp == 0) {  // exclusive scan of the warp totals (nwarps ≤ 32)
+    const int c = lane < nwarps ? scratch[lane] : 0;
+    int run = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, run, o);
+      if (lane >= o) run += t;
     }
-    scratch[nwarps] = run;
+    if (lane < nwarps) scratch[lane] = run - c;
+    if (lane == 31) scratch[nwarps] = run;
   }
   __syncthreads();
   const int r = scratch[warp] + inc - v;
@@ -100,7 +102,9 @@ MOE_DEV int block_exclusive_scan(int v, int* scratch, int* total) {
 // Builds this kernel's entries and the per-row output maps (slot row,
 // combine weight) in shared memory; returns the number of entries.
 // MMA_SIDE selects groups with m ≥ a.mma_min_m, else the others.
-// Needs blockDim.x ≥ MOE_MAX_EXPERTS (one thread per union expert).
+// Needs blockDim.x ≥ MOE_MAX_EXPERTS (one thread per union expert),
+// 2·blockDim.x ≥ MOE_MAX_PAIRS (a thread loads at most two pairs) and room
+// for 2·MOE_MAX_EXPERTS ints in row_w (the per-slot sort's scratch).
 template <int SUB, bool MMA_SIDE>
 MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, float* row_w,
                        int* scratch) {
@@ -109,25 +113,43 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
   auto mine = [&](int m) { return (m >= a.mma_min_m) == MMA_SIDE; };
   int nr = 0;
   if (a.engine == 0) {
+    // every global load first, so that one round trip serves them (a thread
+    // holds at most two pairs)
+    float wreg[2] = {0.f, 0.f};
+    int ereg[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int p = tid + i * nt;
+      if (p < P) {
+        wreg[i] = a.topk_w[p];
+        ereg[i] = a.topk_idx[p];
+      }
+    }
     if (mine(1)) {
       // One entry per (token, slot) pair — every slot still streams its own
       // expert's weights — but the pairs that chose the same expert are
       // siblings of one group, so their jobs run tile by tile side by side
       // and L2 serves the repeated reads at the same moment. Entries in
-      // (expert, pair) order: a counting sort with row_w and row_out as its
-      // scratch (both rewritten below). An expert id outside [0, E) is
+      // (expert, pair) order: a stable counting sort with row_w and row_out
+      // as its scratch (both rewritten below). The order must not depend on
+      // scheduling: every CTA builds the same plan, and a job number names
+      // the same entry in all of them. An expert id outside [0, E) is
       // recorded as an error and read as expert 0.
       int* cnt = reinterpret_cast<int*>(row_w);
       int* start = cnt + MOE_MAX_EXPERTS;
       uint16_t* eid = row_out;
       for (int e = tid; e < a.E; e += nt) cnt[e] = 0;
-      for (int p = tid; p < P; p += nt) {
-        int e = a.topk_idx[p];
-        if (e < 0 || e >= a.E) {
-          report_error(a.err, ERR_CHECK, 0x231);
-          e = 0;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int p = tid + i * nt;
+        if (p < P) {
+          int e = ereg[i];
+          if (e < 0 || e >= a.E) {
+            report_error(a.err, ERR_CHECK, 0x231);
+            e = 0;
+          }
+          eid[p] = (uint16_t)e;
         }
-        eid[p] = (uint16_t)e;
       }
       __syncthreads();
       for (int p = tid; p < P; p += nt) atomicAdd(&cnt[eid[p]], 1);
@@ -145,33 +167,58 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
       __syncthreads();
       nr = P;
     }
-    for (int p = tid; p < P; p += nt) {
-      const int t = p / a.k, j = p - t * a.k;
-      row_out[p] = (uint16_t)(t * S + j);
-      row_w[p] = a.topk_w[p];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int p = tid + i * nt;
+      if (p < P) {
+        const int t = p / a.k, j = p - t * a.k;
+        row_out[p] = (uint16_t)(t * S + j);
+        row_w[p] = wreg[i];
+      }
     }
   } else {
+    // every load that needs no other first, so that one round trip serves
+    // them: the union's count, expert tid's entry (read for every tid < E;
+    // the arrays hold E and E + 1 ints), and rows tid, tid + nt's pairs
     int U = *a.union_count;
-    if (U < 0 || U > a.E) {  // not a union of this layer: run nothing, flag it
-      if (tid == 0) report_error(a.err, ERR_CHECK, 0x230);
-      U = 0;
-    }
     int m = 0, e = 0, r0 = 0;
-    if (tid < U) {
+    if (tid < a.E) {
       r0 = a.offsets[tid];
       m = a.offsets[tid + 1] - r0;
       e = a.union_ids[tid];
     }
+    int ptok[2] = {0, 0}, pslot[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = tid + i * nt;
+      if (r < P) {
+        ptok[i] = a.pair_tok[r];
+        pslot[i] = a.pair_slot[r];
+      }
+    }
+    if (U < 0 || U > a.E) {  // not a union of this layer: run nothing, flag it
+      if (tid == 0) report_error(a.err, ERR_CHECK, 0x230);
+      U = 0;
+    }
+    if (tid >= U) m = e = r0 = 0;
     const int nsub = (m > 0 && mine(m)) ? (m + SUB - 1) / SUB : 0;
     const int pos = block_exclusive_scan(nsub, scratch, &nr);
     for (int q = 0; q < nsub; ++q) {
       const int rr = r0 + q * SUB;
       plan[pos + q] = make_entry(e, rr, min(SUB, m - q * SUB), rr, pos, nsub);
     }
-    for (int r = tid; r < P; r += nt) {
-      const int t = a.pair_tok[r], j = a.pair_slot[r];
-      row_out[r] = (uint16_t)(t * S + j);
-      row_w[r] = a.topk_w[t * a.k + j];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = tid + i * nt;
+      if (r < P) {
+        int t = ptok[i], j = pslot[i];
+        if (t < 0 || t >= a.n || j < 0 || j >= a.k) {  // not a pair of this pass: flag it
+          report_error(a.err, ERR_CHECK, 0x232);
+          t = j = 0;
+        }
+        row_out[r] = (uint16_t)(t * S + j);
+        row_w[r] = a.topk_w[t * a.k + j];
+      }
     }
   }
   const int per = mine(a.n) ? (a.n + SUB - 1) / SUB : 0;
@@ -261,16 +308,29 @@ MOE_DEV bool tail_combine(const ExpertArgs& a, const int* mine, int target,
   if (*reinterpret_cast<volatile int*>(flag) == 0) return false;
   const int S = a.k + a.s, d4 = a.d >> 2;
   const int items = a.n * d4;
+  // The slots' loads go out kChunk at a time, so that one L2 round trip
+  // serves up to kChunk slots; the additions stay in slot order.
+  constexpr int kChunk = 8;
   for (int i = blockIdx.x * nthreads + tid; i < items; i += gridDim.x * nthreads) {
     const int t = i / d4, c4 = i - t * d4;
     const float4* src = reinterpret_cast<const float4*>(a.y_slot + (size_t)t * S * a.d) + c4;
-    float4 acc = __ldcg(src);
-    for (int j = 1; j < S; ++j) {
-      const float4 v = __ldcg(src + (size_t)j * d4);
-      acc.x = __fadd_rn(acc.x, v.x);
-      acc.y = __fadd_rn(acc.y, v.y);
-      acc.z = __fadd_rn(acc.z, v.z);
-      acc.w = __fadd_rn(acc.w, v.w);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < S; j0 += kChunk) {
+      float4 v[kChunk];
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        if (j0 + j < S) v[j] = __ldcg(src + (size_t)(j0 + j) * d4);
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j) {
+        if (j0 + j == 0) {
+          acc = v[0];
+        } else if (j0 + j < S) {
+          acc.x = __fadd_rn(acc.x, v[j].x);
+          acc.y = __fadd_rn(acc.y, v[j].y);
+          acc.z = __fadd_rn(acc.z, v[j].z);
+          acc.w = __fadd_rn(acc.w, v[j].w);
+        }
+      }
     }
     reinterpret_cast<float4*>(a.y + (size_t)t * a.d)[c4] = acc;
   }

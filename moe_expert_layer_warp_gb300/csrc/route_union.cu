@@ -8,6 +8,7 @@
 // Bytes, Kernel Bandwidth and the Best Draft Length", abstract (the union of
 // selected experts is what a deduplicating engine reads once per pass).
 #include <math.h>
+#include <string.h>
 
 #include "moe_warp.h"
 #include "common.cuh"
@@ -56,9 +57,24 @@ MOE_DEV void pair_add(float& s, float& c, float s2, float c2) {
   s = sn;
 }
 
+// The pass's prep work that needs only x (PassPrep), done by the gate: the
+// expert kernels' counters are zeroed over the whole grid (int4 stores:
+// every region is 256-byte aligned and padded to 256 bytes), and x32 = x and
+// x's bf16 halves are written from the x values the dot products load, the
+// CTAs of expert e writing the float4 columns c with c mod E = e (so that no
+// SM stores much).
+MOE_DEV void pass_prep_zero(const PassPrep& pp) {
+  const int nt = gridDim.x * gridDim.y * blockDim.x;
+  const int t = (blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+  const int4 z = make_int4(0, 0, 0, 0);
+  for (int i = t; i < (kCcSyncInts + 3) / 4; i += nt) reinterpret_cast<int4*>(pp.sync_cc)[i] = z;
+  for (int i = t; i < (kMmaSyncInts + 3) / 4; i += nt) reinterpret_cast<int4*>(pp.sync_mma)[i] = z;
+  if (t == 0 && pp.ydone) *reinterpret_cast<int4*>(pp.ydone) = z;
+}
+
 __global__ void __launch_bounds__(kGateWarps * 32)
     gate_logits_kernel(int d, int E, int n, const float* __restrict__ x,
-                       const float* __restrict__ wg, float* __restrict__ logits) {
+                       const float* __restrict__ wg, float* __restrict__ logits, PassPrep pp) {
   __shared__ float part[kGateWarps][kGateTokens][2];
   // W_g is constant: its row can move into L2 while the previous kernel
   // finishes (one prefetch per expert row)
@@ -67,6 +83,8 @@ __global__ void __launch_bounds__(kGateWarps * 32)
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x;
+  if (pp.x32) pass_prep_zero(pp);
+  const bool write_x = pp.x32 != nullptr;
   const int t0 = blockIdx.y * kGateTokens;
   const int nt = min(kGateTokens, n - t0);
   const int chunk4 = (d / kGateWarps) >> 2;  // float4s per warp (d is a multiple of 64)
@@ -84,6 +102,18 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 #pragma unroll
     for (int t = 0; t < kGateTokens; ++t)
       xv[t] = t < nt ? __ldg(xrow + (size_t)t * d4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (write_x && (base4 + i) % E == e) {
+#pragma unroll
+      for (int t = 0; t < kGateTokens; ++t) {
+        if (t < nt) {
+          const size_t o = (size_t)(t0 + t) * d4 + base4 + i;
+          reinterpret_cast<float4*>(pp.x32)[o] = xv[t];
+          if (pp.x16)
+            split_bf16x4(xv[t], reinterpret_cast<uint2*>(pp.x16) + o,
+                         reinterpret_cast<uint2*>(pp.x16lo) + o);
+        }
+      }
+    }
 #pragma unroll
     for (int t = 0; t < kGateTokens; ++t) {
       if (t < nt) {
@@ -131,8 +161,9 @@ __global__ void __launch_bounds__(kGateWarps * 32)
 constexpr int kTopkWarps = 8;
 constexpr int kPerLane = MOE_MAX_EXPERTS / 32;
 
-// One warp selects token t's k experts and writes their weights; the
-// selected indices also go to sel[t·k + j] when sel is not null. Each round
+// One warp selects token t's k experts and writes them and their weights to
+// topk_idx / topk_w (when not null); the selected indices also go to
+// sel[t·k + j] when sel is not null. Each round
 // takes the warp maximum of order-preserving integer keys of the remaining
 // scores (redux.sync), then the lowest expert index holding that key, so
 // the larger score wins and equal scores go to the lower index.
@@ -198,8 +229,10 @@ MOE_DEV void topk_token(int t, int lane, int E, int k, const float* __restrict__
   const float ej = (lane < k) ? expf(my_v - v0) : 0.f;
   const float z = warp_sum(ej);
   if (lane < k) {
-    topk_idx[(size_t)t * k + lane] = my_e;
-    topk_w[(size_t)t * k + lane] = ej / z;
+    if (topk_idx) {
+      topk_idx[(size_t)t * k + lane] = my_e;
+      topk_w[(size_t)t * k + lane] = ej / z;
+    }
     if (sel) sel[t * k + lane] = my_e;
   }
 }
@@ -232,9 +265,11 @@ struct UnionOut {
 };
 
 // The union from the pairs' experts sidx[0 .. n·k) in shared memory, with
-// cnt[] zeroed; every thread of the CTA calls it.
+// cnt[] zeroed; every thread of the CTA calls it. write: the CTA writes the
+// union out; rtok (shared memory, or null): receives the token of each row
+// of the union order.
 MOE_DEV void union_body(int E, int k, int n, uint64_t expert_bytes, int s, const int* sidx,
-                        int* cnt, int* start, const UnionOut& out) {
+                        int* cnt, int* start, const UnionOut& out, bool write, int* rtok) {
   int32_t* __restrict__ union_ids = out.union_ids;
   int32_t* __restrict__ offsets = out.offsets;
   const int P = n * k;
@@ -271,14 +306,16 @@ MOE_DEV void union_body(int E, int k, int n, uint64_t expert_bytes, int s, const
       if (e < E) {
         start[e] = ec;
         if (lc[r] > 0) {
-          union_ids[ep] = e;
-          offsets[ep] = ec;
+          if (write) {
+            union_ids[ep] = e;
+            offsets[ep] = ec;
+          }
           ++ep;
         }
         ec += lc[r];
       }
     }
-    if (lane == 31) {
+    if (lane == 31 && write) {
       offsets[ip] = ic;
       *out.union_count = ip;
       out.bytes[0] = (uint64_t)P * expert_bytes;
@@ -292,8 +329,11 @@ MOE_DEV void union_body(int E, int k, int n, uint64_t expert_bytes, int s, const
     int rank = 0;
     for (int q = 0; q < p; ++q) rank += (sidx[q] == e);
     const int row = start[e] + rank;
-    out.pair_tok[row] = p / k;
-    out.pair_slot[row] = p - (p / k) * k;
+    if (write) {
+      out.pair_tok[row] = p / k;
+      out.pair_slot[row] = p - (p / k) * k;
+    }
+    if (rtok) rtok[row] = p / k;
   }
 }
 
@@ -316,27 +356,66 @@ __global__ void __launch_bounds__(kUnionThreads)
     }
     sidx[p] = v;
   }
-  union_body(E, k, n, expert_bytes, s, sidx, cnt, start, o);
+  union_body(E, k, n, expert_bytes, s, sidx, cnt, start, o, true, nullptr);
 }
 
-// Top-k and union in one CTA: warp w selects tokens w, w + 32, …, into
-// topk_idx / topk_w and into shared memory, then the CTA builds the union.
-// The same selection and the same union as topk_kernel then union_kernel.
+// Top-k and union: warp w selects tokens w, w + 32, …, into shared memory,
+// then the CTA builds the union; the same selection and the same union as
+// topk_kernel then union_kernel. CTA 0 writes them out (topk_idx / topk_w
+// and the union). When pp.xg is not null (a whole dedup pass), every CTA
+// computes the same selection and union from the same logits, and CTA c
+// gathers union rows [c·R, (c+1)·R), R = pp.gather_rows: xg[r] =
+// x[pair_tok[r]] and, when pp.xg16 is not null, its bf16 hi/lo halves (R is
+// chosen so that the grid spans the SMs: one SM stores only a few rows fast).
+
 __global__ void __launch_bounds__(kRouteUnionThreads)
     topk_union_kernel(int E, int k, int n, uint64_t expert_bytes, int s,
                       const float* __restrict__ logits, const float* __restrict__ bias,
                       int bias_in_weights, int32_t* __restrict__ topk_idx,
-                      float* __restrict__ topk_w, UnionOut o) {
+                      float* __restrict__ topk_w, UnionOut o, int d, const float* __restrict__ x,
+                      PassPrep pp) {
   __shared__ int sidx[MOE_MAX_PAIRS];
   __shared__ int cnt[MOE_MAX_EXPERTS];
   __shared__ int start[MOE_MAX_EXPERTS];
+  __shared__ int rtok[MOE_MAX_PAIRS];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool write = blockIdx.x == 0;
   for (int e = tid; e < E; e += blockDim.x) cnt[e] = 0;
   for (int t = warp; t < n; t += blockDim.x >> 5)
-    topk_token(t, lane, E, k, logits, bias, bias_in_weights, topk_idx, topk_w, sidx);
-  union_body(E, k, n, expert_bytes, s, sidx, cnt, start, o);
+    topk_token(t, lane, E, k, logits, bias, bias_in_weights, write ? topk_idx : nullptr,
+               topk_w, sidx);
+  union_body(E, k, n, expert_bytes, s, sidx, cnt, start, o, write, pp.xg ? rtok : nullptr);
+  if (!pp.xg) return;
+  __syncthreads();  // rtok complete
+  const int P = n * k, d4 = d >> 2;
+  const int r0 = blockIdx.x * pp.gather_rows, r1 = min(P, r0 + pp.gather_rows);
+  const int items = (r1 - r0) * d4;
+  // kBatch loads in flight per thread before their stores
+  constexpr int kBatch = 4;
+  for (int i0 = tid; i0 < items; i0 += kBatch * blockDim.x) {
+    float4 v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = i0 + b * blockDim.x;
+      if (i < items) {
+        const int r = r0 + i / d4, c = i - (i / d4) * d4;
+        v[b] = __ldg(reinterpret_cast<const float4*>(x + (size_t)rtok[r] * d) + c);
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int i = i0 + b * blockDim.x;
+      if (i < items) {
+        const int r = r0 + i / d4, c = i - (i / d4) * d4;
+        reinterpret_cast<float4*>(pp.xg + (size_t)r * d)[c] = v[b];
+        if (pp.xg16)
+          split_bf16x4(v[b], reinterpret_cast<uint2*>(pp.xg16 + (size_t)r * d) + c,
+                       reinterpret_cast<uint2*>(pp.xg16lo + (size_t)r * d) + c);
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- combine --
@@ -393,8 +472,10 @@ cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float
                          const float* bias, int bias_in_weights, float* logits, int32_t* topk_idx,
                          float* topk_w, cudaStream_t stream) {
   dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
+  PassPrep none;
+  memset(&none, 0, sizeof none);
   cudaError_t e = launch_pdl(gate_logits_kernel, g1, dim3(kGateWarps * 32), 0, stream, d, E, n, x,
-                             w_router, logits);
+                             w_router, logits, none);
   if (e != cudaSuccess) return e;
   dim3 g2((n + kTopkWarps - 1) / kTopkWarps);
   return launch_pdl(topk_kernel, g2, dim3(kTopkWarps * 32), 0, stream, E, k, n,
@@ -416,16 +497,20 @@ cudaError_t launch_route_union(int d, int I, int E, int k, int s, int wbytes, in
                                int bias_in_weights, float* logits, int32_t* topk_idx,
                                float* topk_w, int32_t* union_ids, int32_t* union_count,
                                int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,
-                               uint64_t* bytes, cudaStream_t stream) {
+                               uint64_t* bytes, const PassPrep* prep, cudaStream_t stream) {
+  PassPrep pp;
+  memset(&pp, 0, sizeof pp);
+  if (prep) pp = *prep;
   dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
   cudaError_t e = launch_pdl(gate_logits_kernel, g1, dim3(kGateWarps * 32), 0, stream, d, E, n, x,
-                             w_router, logits);
+                             w_router, logits, pp);
   if (e != cudaSuccess) return e;
   const uint64_t eb = 3ull * (uint64_t)d * (uint64_t)I * (uint64_t)wbytes;
   const UnionOut o{union_ids, union_count, offsets, pair_tok, pair_slot, bytes};
-  return launch_pdl(topk_union_kernel, dim3(1), dim3(kRouteUnionThreads), 0, stream, E, k, n, eb,
-                    s, static_cast<const float*>(logits), bias, bias_in_weights, topk_idx, topk_w,
-                    o);
+  const int ctas = pp.xg ? (n * k + pp.gather_rows - 1) / pp.gather_rows : 1;
+  return launch_pdl(topk_union_kernel, dim3(ctas), dim3(kRouteUnionThreads), 0, stream, E, k, n,
+                    eb, s, static_cast<const float*>(logits), bias, bias_in_weights, topk_idx,
+                    topk_w, o, d, x, pp);
 }
 
 cudaError_t launch_combine(int d, int slots, int n, const float* y_slot, float* y,

@@ -102,7 +102,7 @@ def test_headline_step_plan_covers_both_engines_at_every_pass_size():
             (n, e) for n in w.pass_sizes for e in ("perslot", "dedup"))
         assert {q for _, _, q in plan} == {step % bench.N_PASSES_PER_N}
     assert sum(n for n, _, _ in bench.step_plan(w, 0)) == 90
-    assert bench.kernels_per_pass() * 2 * len(w.pass_sizes) * w.layers == 2340
+    assert bench.kernels_per_pass() * 2 * len(w.pass_sizes) * w.layers == 1872
 
 
 def test_best_engine_rate_takes_the_faster_engine_at_each_n():

@@ -360,6 +360,37 @@ def test_v2_lite_stack_layers_full_size():
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("shape,ns", [(LayerShape(576, 16, 4, 320, 1, W_BF16), [5, 16]),
+                                      (LayerShape(192, 6, 3, 256, 1, W_F32), [7]),
+                                      (LayerShape(2048, 64, 6, 1408, 2, W_BF16), [9])],
+                         ids=["bf16-ragged", "f32-ragged", "v2-lite"])
+def test_pass_reads_nothing_stale_from_the_workspace(shape, ns):
+    """A pass writes every workspace byte it reads (counters, converted and
+    gathered rows, activations, partial sums) before reading it: the same
+    pass over a workspace of zeros and over one of 0xFF bytes (NaN as float,
+    -1 as int), with y_slot and y set to NaN, gives the same y bit for bit,
+    through both engines, with the combine separate and fused."""
+    L = synth.make_layer(shape, 29, "cuda")
+    R = PassRunner(L, max(ns))
+    for n in ns:
+        x = torch.from_numpy(synth.make_pass(shape.d, n, 0.9, [431 + n])).cuda()
+        for eng in (PERSLOT, DEDUP):
+            for fused in (False, True):
+                ys = []
+                for fill in (0, 255):
+                    R.workspace.fill_(fill)
+                    R.y_slot.fill_(float("nan"))
+                    R.y.fill_(float("nan"))
+                    ys.append(R.forward(x, eng, fused=fused).cpu().numpy().copy())
+                np.testing.assert_array_equal(ys[1].view(np.uint32), ys[0].view(np.uint32),
+                                              err_msg="n=%d %s fused=%s" % (n, eng, fused))
+                assert np.all(np.isfinite(ys[0]))
+    from moe_expert_layer_warp_gb300 import api
+    assert api.moe_last_device_error() == api.MOE_OK
+    del L, R
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("min_m", ["1000", "1", "3"],
                          ids=["cuda-core-only", "tensor-core-only", "both-kernels-in-one-call"])
 def test_small_layers_on_each_expert_kernel(min_m):
@@ -380,6 +411,7 @@ def test_small_layers_on_each_expert_kernel(min_m):
                         "tests/test_parity.py::test_gate_up_storage",
                         "tests/test_parity.py::test_identical_tokens_select_k_experts",
                         "tests/test_parity.py::test_repeated_runs_are_bitwise_identical",
-                        "tests/test_parity.py::test_verify_pass_equals_single_calls"],
+                        "tests/test_parity.py::test_verify_pass_equals_single_calls",
+                        "tests/test_parity.py::test_pass_reads_nothing_stale_from_the_workspace"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
