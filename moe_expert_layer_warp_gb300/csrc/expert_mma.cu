@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_mma_kernel(const __grid_co
     fence_mbar_init();
   }
   if (warp == 1) umma::tmem_alloc(tmem_base, kTmemCols);
+  if (threadIdx.x == 32 * 3 && a.prefetch_shared) shared_l2_prefetch(a);
   if (threadIdx.x == 32 * 2) {
     prefetch_tmap(prm.maps.pair ? &prm.maps.gu : &prm.maps.wg);
     prefetch_tmap(&prm.maps.wd);

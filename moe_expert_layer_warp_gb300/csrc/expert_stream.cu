@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_engine_kernel(const __grid
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (threadIdx.x == (kConsumerWarps + 1) * 32 && a.prefetch_shared) shared_l2_prefetch(a);
   if (threadIdx.x == kConsumerWarps * 32) {
     prefetch_tmap(prm.maps.pair ? &prm.maps.gu : &prm.maps.w0);
     prefetch_tmap(&prm.maps.w2);

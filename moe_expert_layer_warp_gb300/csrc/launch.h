@@ -114,6 +114,8 @@ struct ExpertArgs {
   int keep_weights;     // 1: weight loads use normal L2 eviction (per-slot calls of 3+ tokens,
                         //   whose repeated experts L2 can serve), else evict-first
   float* y_slot;
+  int prefetch_shared;  // 1: each CTA prefetches its share of the shared experts' weights into
+                        //   L2 while it waits for the kernel before it
   float* y;             // [n][d] or null: the combine fused into the kernel's last phase
   int* ydone;           // [1] phase-1 units stored by the call's CTAs, when y is set
   unsigned int* err;

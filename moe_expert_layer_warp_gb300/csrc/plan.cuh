@@ -10,9 +10,10 @@
 //   both:     each shared expert over all n tokens, rows n·k + i·n + t.
 // Groups with at least `mma_min_m` tokens belong to the tensor-core kernel,
 // the others to the CUDA-core kernel. Each kernel splits its groups into
-// sub-groups of at most SUB tokens (one plan entry each). Sibling sub-groups
-// of one group take consecutive jobs tile by tile (job_entry), so their CTAs
-// read each weight tile at nearly the same time and L2 serves the repeats.
+// sub-groups of at most SUB tokens (one plan entry each), the shared experts'
+// entries first. Sibling sub-groups of one group take consecutive jobs tile
+// by tile (job_entry), so their CTAs read each weight tile at nearly the same
+// time and L2 serves the repeats.
 #pragma once
 
 #include "common.cuh"
@@ -111,6 +112,10 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
   const int tid = threadIdx.x, nt = blockDim.x;
   const int P = a.n * a.k, S = a.k + a.s;
   auto mine = [&](int m) { return (m >= a.mma_min_m) == MMA_SIDE; };
+  // the shared experts' entries come first: their jobs are the first handed
+  // out, while their weights are still in L2 when the call prefetched them
+  const int per = mine(a.n) ? (a.n + SUB - 1) / SUB : 0;
+  const int Sh = a.s * per;
   int nr = 0;
   if (a.engine == 0) {
     // every global load first, so that one round trip serves them (a thread
@@ -162,7 +167,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
         const int e = eid[p];
         int rank = 0;
         for (int q = 0; q < p; ++q) rank += (eid[q] == e);
-        plan[start[e] + rank] = make_entry(e, p, 1, p / a.k, start[e], cnt[e]);
+        plan[Sh + start[e] + rank] = make_entry(e, p, 1, p / a.k, Sh + start[e], cnt[e]);
       }
       __syncthreads();
       nr = P;
@@ -205,7 +210,7 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
     const int pos = block_exclusive_scan(nsub, scratch, &nr);
     for (int q = 0; q < nsub; ++q) {
       const int rr = r0 + q * SUB;
-      plan[pos + q] = make_entry(e, rr, min(SUB, m - q * SUB), rr, pos, nsub);
+      plan[Sh + pos + q] = make_entry(e, rr, min(SUB, m - q * SUB), rr, Sh + pos, nsub);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -221,23 +226,43 @@ MOE_DEV int build_plan(const ExpertArgs& a, Entry* plan, uint16_t* row_out, floa
       }
     }
   }
-  const int per = mine(a.n) ? (a.n + SUB - 1) / SUB : 0;
-  for (int q = tid; q < a.s * per; q += nt) {
+  for (int q = tid; q < Sh; q += nt) {
     const int i = q / per, c = q - (q / per) * per;
     const int rr = P + i * a.n + c * SUB;
-    plan[nr + q] = make_entry(-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB, nr + i * per, per);
+    plan[q] = make_entry(-(i + 1), rr, min(SUB, a.n - c * SUB), c * SUB, i * per, per);
   }
   for (int r = tid; r < a.s * a.n; r += nt) {
     const int i = r / a.n, t = r - (r / a.n) * a.n;
     row_out[P + r] = (uint16_t)(t * S + a.k + i);
     row_w[P + r] = 1.f;
   }
-  return nr + a.s * per;
+  return Sh + nr;
 }
 
 // Upper bound of a kernel's entries for sub-groups of SUB tokens.
 constexpr int max_entries(int sub) {
   return MOE_MAX_PAIRS + MOE_MAX_SHARED * ((MOE_MAX_TOKENS + sub - 1) / sub);
+}
+
+// This CTA's share of an L2 prefetch of the shared experts' weights (they
+// do not depend on the routing), issued by one thread while the CTA waits for
+// the kernel before it: gridDim.x slices of each of W_gate, W_up and W_down,
+// in bulk prefetches of at most 32 KB (16-byte aligned, sizes multiples of
+// 16: the arrays are 16-byte aligned and d is a multiple of 64).
+MOE_DEV void shared_l2_prefetch(const ExpertArgs& a) {
+  if (a.s <= 0) return;
+  const size_t bytes = (size_t)a.s * a.I * a.d * (a.wdtype == 1 ? 2 : 4);
+  const char* arr[3] = {static_cast<const char*>(a.ws_gate), static_cast<const char*>(a.ws_up),
+                        static_cast<const char*>(a.ws_down)};
+  const size_t chunk = ((bytes / gridDim.x) + 15) & ~size_t(15);
+  for (int j = 0; j < 3; ++j) {
+    const size_t end = min(bytes, (size_t)(blockIdx.x + 1) * chunk);
+    for (size_t off = (size_t)blockIdx.x * chunk; off < end; off += 32768) {
+      const uint32_t sz = (uint32_t)min((size_t)32768, end - off);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(arr[j] + off), "r"(sz)
+                   : "memory");
+    }
+  }
 }
 
 MOE_DEV int ld_acquire(const int* p) {
