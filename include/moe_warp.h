@@ -194,18 +194,22 @@ moe_status moe_combine(const moe_layer_desc* desc, const float* y_slot, int32_t 
 /* Engines of moe_verify_pass. */
 typedef enum { MOE_ENGINE_PERSLOT = 0, MOE_ENGINE_DEDUP = 1 } moe_engine;
 
-/* One whole verification pass in one call: moe_route_union (routing with
- * the optional bias, and the union), then moe_verify_perslot or
- * moe_verify_dedup, then moe_combine, on one stream; the same launches and
- * results as those calls made one by one. For callers that issue passes
- * from the host one at a time (no CUDA graph), it saves the per-call host
- * cost of three calls.
+/* One whole verification pass in one call: what moe_route_union (routing
+ * with the optional bias, and the union), then moe_verify_perslot or
+ * moe_verify_dedup, then moe_combine compute, on one stream, with bitwise
+ * the same results as those calls made one by one. The routing kernels also
+ * do the engine's prep work (its counters zeroed, x split into bf16 halves,
+ * the dedup rows gathered), so the expert kernel follows them directly: four
+ * kernels, one fewer than the single calls. For callers that issue passes
+ * from the host one at a time (no CUDA graph), it also saves the per-call
+ * host cost of three calls.
  *   weights->w_router is W_g; bias, bias_in_weights as moe_route_biased.
  *   engine   MOE_ENGINE_PERSLOT or MOE_ENGINE_DEDUP (else MOE_EINVAL).
  *   topk_idx, topk_w, u, y_slot   the intermediate outputs, written as the
  *            single calls write them (caller-owned device buffers).
  *   y        [n][d] fp32 out (16-byte aligned), as moe_combine.
- * Returns the first failing call's status; nothing after it is launched.   */
+ * Every argument is checked before anything is launched; the status is
+ * the first failing check's, or a launch failure's.                        */
 moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* weights,
                            const float* bias, int32_t bias_in_weights, const float* x, int32_t n,
                            int32_t engine, int32_t* topk_idx, float* topk_w, const moe_union* u,
@@ -221,10 +225,10 @@ moe_status moe_verify_pass(const moe_layer_desc* desc, const moe_layer_weights* 
  * call's rows are all stored, and sums its share of y in slot order, the
  * same additions in the same order as moe_combine. Same arguments and
  * bitwise the same outputs as moe_verify_pass, one launch fewer. Measured
- * on GB300 (DeepSeek-V2-Lite-shaped layer), a pass this way takes 1-2 us
- * longer than moe_verify_pass: the in-kernel release and wait cost more
- * than the combine launch they replace, which the previous kernel's tail
- * hides (programmatic dependent launch). A call whose groups are split
+ * on GB300 (DeepSeek-V2-Lite-shaped layer), a pass this way takes within
+ * about 1 us of moe_verify_pass either way: the in-kernel release and wait
+ * cost about what the combine launch they replace costs, which the previous
+ * kernel's tail hides (programmatic dependent launch). A call whose groups are split
  * between the tensor-core and CUDA-core kernels (only when MOE_MMA_MIN_M
  * forces it) runs the combine as a launch of its own.                      */
 moe_status moe_verify_pass_fused(const moe_layer_desc* desc, const moe_layer_weights* weights,
