@@ -124,6 +124,17 @@ moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const fl
                      int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* Gate GEMV alone ("Deep Dive into Mixture of Experts", §2, top-k gating
+ * sketch: the logits are x·W_g), the first step of moe_route:
+ *   logits[t][e] = Σ_i x[t][i]·w_router[e][i], with the compensated dot
+ *   described under moe_route.
+ *   x        [n][d] fp32, 16-byte aligned;  w_router [E][d] fp32, 16-byte aligned.
+ *   logits   [n][E] fp32 out (caller-owned, 4-byte aligned).
+ * MOE_EINVAL for a bad descriptor, n out of range or a null or misaligned
+ * pointer.                                                                  */
+moe_status moe_gate(const moe_layer_desc* desc, const float* w_router, const float* x, int32_t n,
+                    float* logits, void* stream);
+
 /* Gate GEMV and top-k with a per-expert routing bias ("Deep Dive into
  * Mixture of Experts", §5, DeepSeek-style routing sketch: a bias, adjusted
  * for load balance, is added to the gate's scores before the top-k).

@@ -25,7 +25,7 @@ EXPORTED = ("moe_workspace_bytes", "moe_route", "moe_build_union", "moe_verify_p
             "moe_verify_dedup", "moe_combine", "moe_last_device_error", "moe_status_str",
             "moe_last_cuda_error_string", "moe_verify_dedup_noalloc", "moe_noalloc_scratch_limit",
             "moe_diag_bounded_wait", "moe_route_biased", "moe_route_union", "moe_verify_pass",
-            "moe_verify_pass_fused")
+            "moe_verify_pass_fused", "moe_gate")
 
 
 class MoeError(RuntimeError):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
     U = ctypes.POINTER(UnionC)
     lib.moe_workspace_bytes.argtypes = [D, I32]
     lib.moe_workspace_bytes.restype = SZ
+    lib.moe_gate.argtypes = [D, P, P, I32, P, P]
     lib.moe_route.argtypes = [D, P, P, I32, P, P, P, SZ, P]
     lib.moe_route_biased.argtypes = [D, P, P, I32, P, I32, P, P, P, SZ, P]
     lib.moe_build_union.argtypes = [D, P, I32, U, P]
@@ -91,7 +92,7 @@ def load(path: str = LIB_PATH):
     for f in ("moe_route", "moe_build_union", "moe_verify_perslot", "moe_verify_dedup",
               "moe_combine", "moe_last_device_error", "moe_verify_dedup_noalloc",
               "moe_diag_bounded_wait", "moe_route_biased", "moe_route_union", "moe_verify_pass",
-              "moe_verify_pass_fused"):
+              "moe_verify_pass_fused", "moe_gate"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -138,6 +139,11 @@ def make_weights(w) -> LayerWeightsC:
 
 def moe_workspace_bytes(desc: LayerDesc, n_max: int) -> int:
     return int(load().moe_workspace_bytes(ctypes.byref(desc), n_max))
+
+
+def moe_gate(desc, w_router, x, n, logits, stream=None):
+    _check(load().moe_gate(ctypes.byref(desc), _ptr(w_router), _ptr(x), n, _ptr(logits),
+                           _stream(stream)), "moe_gate")
 
 
 def moe_route(desc, w_router, x, n, topk_idx, topk_w, workspace, stream=None):

@@ -204,6 +204,20 @@ size_t moe_workspace_bytes(const moe_layer_desc* desc, int32_t n_max) {
   return ws_layout(desc, n_max).total;
 }
 
+moe_status moe_gate(const moe_layer_desc* desc, const float* w_router, const float* x, int32_t n,
+                    float* logits, void* stream) {
+  MOE_TRY(check_desc(desc));
+  MOE_TRY(check_n(desc, n));
+  if (!w_router || !x || !logits) return MOE_EINVAL;
+  if (!aligned16(w_router) || !aligned16(x) || (reinterpret_cast<uintptr_t>(logits) & 3u) != 0)
+    return MOE_EINVAL;
+  DeviceInfo* di;
+  MOE_TRY(device_info(&di));
+  cudaError_t e = moe::launch_gate(desc->d, desc->n_experts, n, x, w_router, logits,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "moe_gate launch");
+}
+
 moe_status moe_route(const moe_layer_desc* desc, const float* w_router, const float* x,
                      int32_t n, int32_t* topk_idx, float* topk_w, void* workspace,
                      size_t workspace_bytes, void* stream) {

@@ -35,6 +35,10 @@ cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float
                          const float* bias, int bias_in_weights, float* logits, int32_t* topk_idx,
                          float* topk_w, cudaStream_t stream);
 
+// The gate GEMV alone: logits[n][E] = x·W_gᵀ (compensated fp32 dots).
+cudaError_t launch_gate(int d, int E, int n, const float* x, const float* w_router, float* logits,
+                        cudaStream_t stream);
+
 // Union of selected experts, pairs grouped by (expert, token), byte counts.
 cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
                          const int32_t* topk_idx, int32_t* union_ids, int32_t* union_count,

@@ -482,6 +482,15 @@ cudaError_t launch_route(int d, int E, int k, int n, const float* x, const float
                     static_cast<const float*>(logits), bias, bias_in_weights, topk_idx, topk_w);
 }
 
+cudaError_t launch_gate(int d, int E, int n, const float* x, const float* w_router, float* logits,
+                        cudaStream_t stream) {
+  dim3 g1(E, (n + kGateTokens - 1) / kGateTokens);
+  PassPrep none;
+  memset(&none, 0, sizeof none);
+  return launch_pdl(gate_logits_kernel, g1, dim3(kGateWarps * 32), 0, stream, d, E, n, x,
+                    w_router, logits, none);
+}
+
 cudaError_t launch_union(int d, int I, int E, int k, int s, int wbytes, int n,
                          const int32_t* topk_idx, int32_t* union_ids, int32_t* union_count,
                          int32_t* offsets, int32_t* pair_tok, int32_t* pair_slot,

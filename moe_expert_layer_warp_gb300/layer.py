@@ -5,8 +5,8 @@ union, slot outputs, output) for passes of up to ``n_max`` tokens and calls
 the library's entry points: forward() makes one moe_verify_pass call
 (moe_route_union → moe_verify_perslot or moe_verify_dedup → moe_combine), or
 one moe_verify_pass_fused call (the combine inside the expert kernel);
-route(), build_union(), route_union(), experts() and combine() make the
-single calls. Buffers are allocated
+gate(), route(), build_union(), route_union(), experts() and combine() make
+the single calls. Buffers are allocated
 once, through torch, at construction, and so are the C arguments that point
 at them: a call only marshals x and the stream.
 """
@@ -56,6 +56,7 @@ class PassRunner:
         self.u = api.UnionC(*(api._ptr(t) for t in (self.union_ids, self.union_count,
                                                      self.offsets, self.pair_tok,
                                                      self.pair_slot, self.bytes)))
+        self.logits = torch.empty(n_max * E, **f32)
         self.y_slot = torch.empty(n_max * (k + s) * d, **f32)
         self.y = torch.empty(n_max * d, **f32)
         # C arguments fixed for the runner's lifetime
@@ -69,6 +70,7 @@ class PassRunner:
         self._router = V(weights.w_router.data_ptr())
         self._idx = V(self.topk_idx.data_ptr())
         self._tw = V(self.topk_w.data_ptr())
+        self._logits = V(self.logits.data_ptr())
         self._yslot = V(self.y_slot.data_ptr())
         self._y = V(self.y.data_ptr())
         self.bias = None
@@ -90,6 +92,12 @@ class PassRunner:
         return ctypes.c_void_p(x.data_ptr())
 
     # -- single steps ---------------------------------------------------------
+    def gate(self, x: torch.Tensor, stream=None, _xp=None):
+        """The gate GEMV alone: self.logits[:n·E] = x·W_gᵀ."""
+        xp = _xp or self._x(x)
+        api._check(self._lib.moe_gate(self._desc, self._router, xp, x.shape[0], self._logits,
+                                      api._stream(stream)), "moe_gate")
+
     def route(self, x: torch.Tensor, stream=None, _xp=None):
         xp = _xp or self._x(x)
         if self._bias is None:

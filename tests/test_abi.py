@@ -95,6 +95,13 @@ def test_null_and_misaligned_pointers_return_einval(lib):
                                 one, 1 << 20, one, z) == api.MOE_EINVAL
     assert lib.moe_combine(ctypes.byref(d), z, 4, one, z) == api.MOE_EINVAL
     assert lib.moe_combine(ctypes.byref(d), one, 0, one, z) == api.MOE_EINVAL
+    # moe_gate: null router, x or logits; misaligned x or logits; n out of range
+    assert lib.moe_gate(ctypes.byref(d), z, one, 4, one, z) == api.MOE_EINVAL
+    assert lib.moe_gate(ctypes.byref(d), one, z, 4, one, z) == api.MOE_EINVAL
+    assert lib.moe_gate(ctypes.byref(d), one, one, 4, z, z) == api.MOE_EINVAL
+    assert lib.moe_gate(ctypes.byref(d), one, odd, 4, one, z) == api.MOE_EINVAL
+    assert lib.moe_gate(ctypes.byref(d), one, one, 4, ctypes.c_void_p(4096 + 2), z) == api.MOE_EINVAL
+    assert lib.moe_gate(ctypes.byref(d), one, one, 0, one, z) == api.MOE_EINVAL
 
 
 def test_status_strings(lib):

@@ -264,7 +264,8 @@ def test_verify_pass_equals_single_calls(bias_mode, shape, fused):
     """forward() — one moe_verify_pass call, or one moe_verify_pass_fused
     call (the combine as the expert kernel's last phase) — against
     moe_route_union, moe_verify_* and moe_combine made one by one: y, slot
-    outputs and routing bit for bit, for both engines."""
+    outputs, the selection and its weights, and the union bit for bit, for
+    both engines."""
     L = synth.make_layer(shape, 71, "cuda")
     n = 11
     x = torch.from_numpy(synth.make_pass(shape.d, n, 0.9, [19])).cuda()
@@ -273,13 +274,25 @@ def test_verify_pass_equals_single_calls(bias_mode, shape, fused):
         bias = torch.from_numpy(np.random.default_rng(4).standard_normal(shape.n_experts)
                                 .astype(np.float32) * 0.05).cuda()
     R = PassRunner(L, n, bias=bias, bias_in_weights=bool(bias_mode))
+
+    def poison_routing():
+        for t in (R.topk_idx, R.pair_tok, R.pair_slot, R.union_ids, R.offsets, R.union_count):
+            t.fill_(-7)
+        R.topk_w.fill_(float("nan"))
+        R.bytes.fill_(-7)
+
     for eng in (PERSLOT, DEDUP):
         R.y.fill_(float("nan"))     # an element the fused combine missed would stay NaN
+        poison_routing()            # and so would routing outputs the pass did not write
         y1 = R.forward(x, eng, fused=fused).cpu().numpy().copy()
         s1 = R.slots(n).cpu().numpy().copy()
         i1 = R.routing(n)[0].cpu().numpy().copy()
+        w1 = R.routing(n)[1].cpu().numpy().copy()
+        u1 = {k: (v.cpu().numpy().copy() if torch.is_tensor(v) else v)
+              for k, v in R.union(n).items()}
         R.y.fill_(-1.0)
         R.y_slot.fill_(-1.0)
+        poison_routing()
         R.route_union(x)
         R.experts(x, eng)
         R.combine(n)
@@ -289,6 +302,36 @@ def test_verify_pass_equals_single_calls(bias_mode, shape, fused):
         np.testing.assert_array_equal(y1.view(np.uint32), y2.view(np.uint32))
         np.testing.assert_array_equal(s1.view(np.uint32), R.slots(n).cpu().numpy().view(np.uint32))
         np.testing.assert_array_equal(i1, R.routing(n)[0].cpu().numpy())
+        np.testing.assert_array_equal(w1.view(np.uint32),
+                                      R.routing(n)[1].cpu().numpy().view(np.uint32))
+        u2 = R.union(n)
+        assert u1["count"] == u2["count"]
+        for key in ("union_ids", "offsets", "pair_tok", "pair_slot", "bytes"):
+            np.testing.assert_array_equal(u1[key], u2[key].cpu().numpy(), err_msg=key)
+
+
+@pytest.mark.parametrize("name,shape,ns", [SMALL[0], SMALL[1], SMALL[6]],
+                         ids=[SMALL[0][0], SMALL[1][0], SMALL[6][0]])
+def test_gate_logits_within_certified_bound(name, shape, ns):
+    """moe_gate (the gate GEMV alone) against the oracle's float64 logits:
+    every logit within the certified error bound of the compensated fp32
+    dot, and bit for bit the logits moe_route_union leaves in the workspace
+    (the same kernel)."""
+    L = synth.make_layer(shape, 23, "cuda")
+    R = PassRunner(L, max(ns))
+    E = shape.n_experts
+    for n in ns:
+        x_np = synth.make_pass(shape.d, n, 0.5, [31 + n])
+        x = torch.from_numpy(x_np).cuda()
+        R.logits.fill_(float("nan"))
+        R.gate(x)
+        got = R.logits[: n * E].view(n, E).cpu().numpy().astype(np.float64)
+        orc = oracle.route(x_np, L.w_router.cpu().numpy(), shape.top_k)
+        bound = pu.logit_error_bound(orc, shape.d)
+        assert np.all(np.abs(got - orc["logits"]) <= bound), "n=%d" % n
+        R.route_union(x)
+        ws = R.workspace[: n * E * 4].view(torch.float32).view(n, E).cpu().numpy()
+        np.testing.assert_array_equal(got.astype(np.float32).view(np.uint32), ws.view(np.uint32))
 
 
 def test_identical_tokens_select_k_experts():
