@@ -1070,9 +1070,9 @@ def run_ours(args):
                          "another layer's weights than the one before it",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "timing": "CUDA-graph replay of each step, CUDA events on the stream"},
-        "roofline": {"kernel": "expert call: prep kernel + expert_mma_kernel (tensor cores) or "
+        "roofline": {"kernel": "expert call: expert_mma_kernel (tensor cores) or "
                                "expert_engine_kernel (CUDA cores), chosen per call; up/gate and "
-                               "down of every group",
+                               "down of every group (a whole pass runs no prep kernel)",
                      "bound": "hbm",
                      "bytes": "requested: the call's expert-weight bytes as the method counts them "
                               "(per-slot n*k*E_b + s*E_b, dedup |U|*E_b + s*E_b) plus its "
