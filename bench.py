@@ -50,7 +50,7 @@ HEADLINE_RHO = 0.9
 N_PASSES_PER_N = 2        # distinct hidden-state passes per n, alternated across steps
 EXPERT_BYTES = 3 * 2048 * 1408 * 2
 BREAKDOWN_PASSES = 8      # passes per (pass size, engine) in the per-call breakdown
-BREAKDOWN_ROUNDS = 5      # replays of each breakdown graph (median taken)
+BREAKDOWN_ROUNDS = 9      # replays of each breakdown graph (median taken)
 SPIN_CYCLES = 2_000_000   # ~1 ms of device spin before a timed pass: the host queues the whole
                           # pass meanwhile, so no launch waits on the host inside the timed span
 
@@ -256,15 +256,17 @@ def unique_bytes(R):
 
 
 def measure_breakdown(w, runners, xs):
-    """The expert call's time inside a pipelined pass, per pass size and
-    engine, on the stack's layers. Each of BREAKDOWN_PASSES passes (pass i on
-    layer i, so consecutive passes read different weights) is captured twice
-    as a CUDA graph: the whole pass (one moe_verify_pass: route, union,
-    expert call, combine) — and its routing, union and combine alone. The
-    graphs are replayed round-robin between CUDA events on the stream; the
-    expert call's time is the difference of a pass's two medians, the fixed
-    time the second median. Returns samples for the step-time model,
-    per-pass times and the calls' requested bytes."""
+    """The expert call's time inside pipelined passes, per pass size and
+    engine, on the stack's layers. BREAKDOWN_PASSES passes (pass i on layer
+    i, so consecutive passes read different weights) run back to back, as in
+    the headline step, in one CUDA graph: the whole passes (moe_verify_pass:
+    route, union, expert call, combine), and in a second graph their
+    routing, union and combine alone. The two graphs are replayed
+    round-robin between CUDA events on the stream; a pass's time is the
+    first graph's median over the passes it holds, the fixed time the
+    second's, the expert call's time their difference. Returns samples for
+    the step-time model (each pass's requested bytes with the call time per
+    pass), the fixed and pass times and the passes' unique bytes."""
     samples = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     uniq = {"perslot": {n: [] for n in w.pass_sizes}, "dedup": {n: [] for n in w.pass_sizes}}
     tfix = {n: [] for n in w.pass_sizes}
@@ -281,21 +283,23 @@ def measure_breakdown(w, runners, xs):
                 reqs.append(requested(R, eng))
                 uniq[eng][n].append(unique_bytes(R))
 
-            def one(s, li, q, with_expert):
-                R, x = runners[li], xs[n][q]
-                if with_expert:          # the whole pass, as the user calls it
-                    R.forward(x, eng, s)
-                else:                    # its fixed part: routing, union and combine
-                    R.route_union(x, s)
-                    R.combine(n, s)
-            ga = [capture_graph(lambda s, li=li, q=q: one(s, li, q, True)) for li, q in plan]
-            gb = [capture_graph(lambda s, li=li, q=q: one(s, li, q, False)) for li, q in plan]
-            t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
-            ta, tb = t[:len(plan)], t[len(plan):]
-            for i in range(len(plan)):
-                samples[eng][n].append((reqs[i], max(ta[i] - tb[i], 1e-9)))
-                tfix[n].append(tb[i])
-                pass_ms[eng][n].append(ta[i] * 1e3)
+            def chain(s, with_expert):
+                for li, q in plan:
+                    R, x = runners[li], xs[n][q]
+                    if with_expert:      # the whole pass, as the user calls it
+                        R.forward(x, eng, s)
+                    else:                # its fixed part: routing, union and combine
+                        R.route_union(x, s)
+                        R.combine(n, s)
+            ga = capture_graph(lambda s: chain(s, True))
+            gb = capture_graph(lambda s: chain(s, False))
+            ta, tb = time_graphs([ga, gb], BREAKDOWN_ROUNDS)
+            k = len(plan)
+            call = max(ta - tb, 1e-9) / k
+            for i in range(k):
+                samples[eng][n].append((reqs[i], call))
+            tfix[n].append(tb / k)
+            pass_ms[eng][n].append(ta / k * 1e3)
             del ga, gb
     t_fix = {n: statistics.median(v) for n, v in tfix.items()}
     return samples, t_fix, pass_ms, uniq
@@ -307,22 +311,23 @@ FUSED_PASSES = 4   # passes per (pass size, engine) in the fused-combine compari
 def measure_fused(w, runners, xs):
     """Pass time with the combine as a launch of its own (moe_verify_pass)
     and fused into the expert kernel (moe_verify_pass_fused), per pass size
-    and engine: FUSED_PASSES passes on as many layers, each captured both
-    ways as a CUDA graph and replayed round-robin between CUDA events;
-    medians in microseconds."""
+    and engine: FUSED_PASSES passes on as many layers back to back in one
+    CUDA graph each way, replayed round-robin between CUDA events; medians
+    per pass in microseconds."""
     out = {"separate_us": {}, "fused_us": {}}
     for eng in ("perslot", "dedup"):
         sep, fus = [], []
         for n in w.pass_sizes:
             plan = [(i % len(runners), i % N_PASSES_PER_N) for i in range(FUSED_PASSES)]
-            ga = [capture_graph(lambda s, li=li, q=q: runners[li].forward(xs[n][q], eng, s))
-                  for li, q in plan]
-            gb = [capture_graph(lambda s, li=li, q=q: runners[li].forward(xs[n][q], eng, s,
-                                                                         fused=True))
-                  for li, q in plan]
-            t = time_graphs(ga + gb, BREAKDOWN_ROUNDS)
-            sep.append(round(statistics.median(t[:len(plan)]) * 1e6, 2))
-            fus.append(round(statistics.median(t[len(plan):]) * 1e6, 2))
+
+            def chain(s, fused):
+                for li, q in plan:
+                    runners[li].forward(xs[n][q], eng, s, fused=fused)
+            ga = capture_graph(lambda s: chain(s, False))
+            gb = capture_graph(lambda s: chain(s, True))
+            ta, tb = time_graphs([ga, gb], BREAKDOWN_ROUNDS)
+            sep.append(round(ta / len(plan) * 1e6, 2))
+            fus.append(round(tb / len(plan) * 1e6, 2))
             del ga, gb
         out["separate_us"][eng] = sep
         out["fused_us"][eng] = fus
@@ -1100,12 +1105,12 @@ def run_ours(args):
                       "note": "the same passes and copies issued call by call from Python"},
         "clocks": clk,
         "layer_breakdown": {
-            "what": "one layer pass at a time on the stack's layers (8 passes per point, each on "
-                    "another layer), expert call = graph with minus graph without the call; "
-                    "t_fix = routing, union and combine",
+            "what": "8 layer passes back to back (each on another layer of the stack) in one "
+                    "CUDA graph per point, times per pass; expert call = graph with minus graph "
+                    "without the calls; t_fix = routing, union and combine",
             "engines": per_engine, "stepmodel": rep.as_dict(),
-            "fused_combine": dict(fused, what="one layer pass (graph replay, median of %d passes "
-                                  "on as many layers) with the combine as a launch of its own "
+            "fused_combine": dict(fused, what="layer passes back to back (graph replay, %d passes "
+                                  "on as many layers, time per pass) with the combine as a launch of its own "
                                   "(moe_verify_pass, the headline's path) and fused into the "
                                   "expert kernel's last phase (moe_verify_pass_fused)"
                                   % FUSED_PASSES)},
