@@ -141,14 +141,17 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
 // any count when an expert spans 128 or more 128-row tiles (Mixtral: 3-6 %
 // faster; V3, 72 tiles, is 9 % faster on the tensor cores); dedup groups,
 // which hold several tokens, go faster on the tensor cores from ~350 tiles
-// with 15 groups or more, or with 3 tokens or more per group.
+// with 15 groups or more, or with 3 tokens or more per group, or in passes
+// of more tokens than a CUDA-core sub-group holds (kCcSub): there a group
+// of correlated tokens outgrows one sub-group, and its sub-groups each read
+// the expert again (measured, Mixtral-shaped dedup at 5 tokens: 13 % slower
+// on CUDA cores at rho = 0.9, 59 % at 0.99).
 // The groups of a dedup call are known only on the device: the estimate
 // takes half of min(E, n·k) distinct experts, which the union reaches at
-// hidden-state correlations near 0.9; far from it (0 or 0.99) the estimate
-// can pick the slower kernel for mid-size passes (measured: up to 6-10 % on
-// the V2-Lite- and Mixtral-shaped calls at 4-6 tokens). MOE_MMA_MIN_M in the
-// environment (read once; for tuning) fixes instead the smallest group that
-// runs on the tensor cores.
+// hidden-state correlations near 0.9; far from it the estimate can pick the
+// slower kernel (measured: up to 6 % on the Mixtral-shaped calls at 5-6
+// tokens and rho = 0). MOE_MMA_MIN_M in the environment (read once; for
+// tuning) fixes instead the smallest group that runs on the tensor cores.
 int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   static const int forced = [] {
     const char* e = getenv("MOE_MMA_MIN_M");
@@ -166,7 +169,7 @@ int mma_min_m(const moe_layer_desc* d, int engine, int32_t n) {
   } else {
     const int routed = std::max(1, std::min(d->n_experts, pairs) / 2);
     const int groups = routed + shared;
-    mma = groups * tiles >= 350 && (groups >= 15 || pairs >= 3 * routed);
+    mma = groups * tiles >= 350 && (groups >= 15 || pairs >= 3 * routed || n > moe::kCcSub);
   }
   return mma ? 1 : 0x7fffffff;
 }
