@@ -138,7 +138,7 @@ WsLayout ws_layout(const moe_layer_desc* d, int32_t n_max) {
 // kernel forced (DeepSeek-V2-Lite-, Mixtral- and DeepSeek-V3-shaped layers,
 // per-slot pairs of one expert run side by side): one-token groups
 // (per-slot) go faster on CUDA cores below ~400 tiles or 12 groups, and at
-// any count when an expert spans 128 or more 128-row tiles (Mixtral: 3-6 %
+// any count when an expert spans 128 or more 128-row tiles (Mixtral: 1-15 %
 // faster; V3, 72 tiles, is 9 % faster on the tensor cores); dedup groups,
 // which hold several tokens, go faster on the tensor cores from ~350 tiles
 // with 15 groups or more, or with 3 tokens or more per group, or in passes
