@@ -9,9 +9,10 @@ the smallest dimensions (d = I = 64), n = 1 and identical tokens. The five
 workload shapes run at full size in the launch configuration the benchmark
 times and are compared with the oracle on every token — the V2-Lite layer at
 every pass size, two layers of the 26-layer stack, the Mixtral layer at
-n = 1, 2, 8 and 16 (rho = 0) and the V3 layer's 64 tokens — except one
-Mixtral pass (n = 16, rho = 0.9), sampled on its last token (routing, union
-and bytes on every token).
+n = 1, 2, 8 and 16 (rho = 0) and at n = 5 and 12 (rho = 0.99, large dedup
+groups), and the V3 layer's 64 tokens — except one Mixtral pass (n = 16,
+rho = 0.9), sampled on its last token (routing, union and bytes on every
+token).
 Both engines are checked, and against each other.
 """
 import gc
@@ -374,8 +375,10 @@ def test_mixtral_layer_full_size():
     L = synth.make_layer(w.shape, w.weight_seed, "cuda")
     R = PassRunner(L, max(w.pass_sizes))
     # n = 16 at rho = 0 (the most distinct experts) and n <= 8 on every
-    # token; n = 16 at rho = 0.9 on its last token
-    for n, rho in [(1, 0.9), (2, 0.0), (8, 0.5), (16, 0.9), (16, 0.0)]:
+    # token; n = 16 at rho = 0.9 on its last token; n = 5 and 12 at rho = 0.99
+    # (nearly identical tokens: dedup groups of five and twelve tokens on the
+    # tensor cores) on every token
+    for n, rho in [(1, 0.9), (2, 0.0), (8, 0.5), (16, 0.9), (16, 0.0), (5, 0.99), (12, 0.99)]:
         x = _workload_pass(w, n, rho, 0)
         check_pass(L, x, tokens=[n - 1] if (n, rho) == (16, 0.9) else None, runner=R)
     del L, R
